@@ -1,0 +1,340 @@
+/*
+ * CPU oracle for the MACaQ W4A4 (MXFP4) linear layer -- TEST INFRASTRUCTURE.
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg may load this library.  The product path (the CUDA library) never does,
+ * and the two share no code, table or constant.
+ *
+ * What it states, step by step, in plain loops:
+ *
+ *   balance scales   MACaQ page "What is MACaQ quantization", section "How
+ *                    MACaQ works", step "Channel balancing": one scale per
+ *                    input channel evens out channel magnitudes.  The rule
+ *                    s_j = sqrt(max|Xc[:,j]| / max|W[:,j]|), clamped to
+ *                    [1e-2, 1e2], is the plainest reading; activations are
+ *                    divided by s, weights multiplied by s.
+ *   block Hadamard   same section, step "A small Hadamard transform": a block
+ *                    Hadamard rotation over 32 channels, with the inverse
+ *                    folded into the weights so the output is unchanged
+ *                    before rounding.  Normalised Sylvester order 32, applied
+ *                    as butterflies at strides 1, 2, 4, 8, 16 and one multiply
+ *                    by fp32(1/sqrt 32).
+ *   MXFP4 encode     same page, FAQ "What is W4A4 quantization": 4-bit floats
+ *                    in blocks of 32 sharing one scale.  Scale exponent
+ *                    floor(log2 amax) - 2 (E8M0), element grid E2M1
+ *                    {0, 0.5, 1, 1.5, 2, 3, 4, 6}, round to nearest with ties
+ *                    to the even code, saturating at 6.
+ *   GEMM reference   Y = deq(A) . deq(W)^T accumulated in fp64.
+ *
+ * Precision: the transform is stated in fp32 (IEEE, round to nearest, no
+ * contraction: build with -ffp-contract=off, no fast-math), because the
+ * quantised codes depend on its exact bits.  The fp64 variant exists for the
+ * fold identity (output unchanged before rounding).
+ *
+ * Parity pins live in tests/test_oracle_*.py: closed forms (Sylvester
+ * entries, scipy's Hadamard, the fold identity), a brute-force argmin for the
+ * rounding, E8M0 boundary cases and an independent numpy restatement.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static float bf16_bits_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t f32_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- balance */
+
+/* Per-channel balance scale from a calibration batch Xc [mc, k] and the
+ * weight W [n, k] (both bf16 bits, row-major).  Column maxima are exact in
+ * fp64; the ratio and square root are taken in fp64 and rounded once to fp32
+ * after clamping.  A channel with zero weight gets the upper clamp (1e2), a
+ * channel zero on both sides gets 1.  inv_s = 1/s in fp32. */
+void oracle_balance_scales(const uint16_t *xc, int64_t mc, const uint16_t *w, int64_t n,
+                           int64_t k, float *s, float *inv_s)
+{
+    for (int64_t j = 0; j < k; ++j) {
+        double cx = 0.0, cw = 0.0;
+        for (int64_t m = 0; m < mc; ++m) {
+            double a = fabs((double)bf16_bits_to_f32(xc[m * k + j]));
+            if (a > cx) cx = a;
+        }
+        for (int64_t r = 0; r < n; ++r) {
+            double a = fabs((double)bf16_bits_to_f32(w[r * k + j]));
+            if (a > cw) cw = a;
+        }
+        double r;
+        if (cw == 0.0) {
+            r = (cx == 0.0) ? 1.0 : 1e2;
+        } else {
+            r = sqrt(cx / cw);
+            if (r < 1e-2) r = 1e-2;
+            if (r > 1e2) r = 1e2;
+        }
+        s[j] = (float)r;
+        inv_s[j] = 1.0f / s[j];
+    }
+}
+
+/* ------------------------------------------------------- block Hadamard */
+
+/* One 32-channel block: v <- H32 . v with H32 the Sylvester matrix, as five
+ * butterfly stages (stride h = 1, 2, 4, 8, 16; pair (i, i+h) for bit h of i
+ * clear becomes (a + b, a - b)), then the 1/sqrt(32) normalisation. */
+static void fwht32_f32(float v[32])
+{
+    for (int h = 1; h < 32; h <<= 1) {
+        for (int i = 0; i < 32; ++i) {
+            if (i & h) continue;
+            float a = v[i];
+            float b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+    const float c = (float)(1.0 / sqrt(32.0));
+    for (int i = 0; i < 32; ++i) v[i] = v[i] * c;
+}
+
+static void fwht32_f64(double v[32])
+{
+    for (int h = 1; h < 32; h <<= 1) {
+        for (int i = 0; i < 32; ++i) {
+            if (i & h) continue;
+            double a = v[i];
+            double b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+    const double c = 1.0 / sqrt(32.0);
+    for (int i = 0; i < 32; ++i) v[i] = v[i] * c;
+}
+
+/* y = (x . diag(f)) . (I_{k/32} kron H32), fp32.  x: bf16 bits [rows, k];
+ * f: [k] fp32 (1/s for activations, s for weights); y: [rows, k] fp32. */
+void oracle_transform_f32(const uint16_t *x, int64_t rows, int64_t k, const float *f, float *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            float v[32];
+            for (int i = 0; i < 32; ++i) {
+                int64_t j = 32 * b + i;
+                v[i] = bf16_bits_to_f32(x[r * k + j]) * f[j];
+            }
+            fwht32_f32(v);
+            for (int i = 0; i < 32; ++i) y[r * k + 32 * b + i] = v[i];
+        }
+    }
+}
+
+/* The same transform in fp64 on fp64 input (no rounding to fp32). */
+void oracle_transform_f64(const double *x, int64_t rows, int64_t k, const double *f, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            double v[32];
+            for (int i = 0; i < 32; ++i) {
+                int64_t j = 32 * b + i;
+                v[i] = x[r * k + j] * f[j];
+            }
+            fwht32_f64(v);
+            for (int i = 0; i < 32; ++i) y[r * k + 32 * b + i] = v[i];
+        }
+    }
+}
+
+/* ------------------------------------------------------------ MXFP4 */
+
+/* floor(log2 |a|) for a finite, non-zero fp32, read from its bits (normal:
+ * biased exponent - 127; subnormal: position of the top mantissa bit - 149). */
+static int floor_log2_f32(float a)
+{
+    uint32_t u = f32_bits(a) & 0x7fffffffu;
+    uint32_t e = u >> 23;
+    if (e != 0) return (int)e - 127;
+    int p = 31;
+    while (!((u >> p) & 1u)) --p;
+    return p - 149;
+}
+
+/* Shared scale exponent of one block from its absolute maximum:
+ * se = clamp(floor(log2 amax) - 2, -127, 127); amax = 0 gives -127. */
+int oracle_scale_exponent(float amax)
+{
+    if (amax == 0.0f) return -127;
+    int se = floor_log2_f32(amax) - 2;
+    if (se < -127) se = -127;
+    if (se > 127) se = 127;
+    return se;
+}
+
+/* E2M1 encode of one fp32 value: round |t| to the format's spacing at its
+ * binade (0.5 below 1, one mantissa bit above), ties to even, saturate at 6.
+ * Returns the 4-bit code sign|exp(2)|man(1); the sign of t is kept, also for
+ * results that round to zero. */
+uint8_t oracle_e2m1_encode(float t)
+{
+    uint8_t sign = (f32_bits(t) >> 31) ? 0x8 : 0x0;
+    double a = fabs((double)t);
+    int ex;
+    double quantum = 0.5;
+    if (a >= 1.0) {
+        frexp(a, &ex);                 /* a = f * 2^ex, f in [0.5, 1) */
+        quantum = ldexp(1.0, ex - 2);  /* 2^(floor(log2 a) - 1) */
+    }
+    double q = nearbyint(a / quantum) * quantum; /* default mode: ties to even */
+    if (q > 6.0) q = 6.0;
+    uint8_t mag;
+    if (q < 1.0) {
+        mag = (uint8_t)(q * 2.0); /* 0 -> 0, 0.5 -> 1 (exp field 0) */
+    } else {
+        double f = frexp(q, &ex);      /* q = 2^(ex-1) * (2f), 2f in [1, 2) */
+        int man = (2.0 * f > 1.0) ? 1 : 0;
+        mag = (uint8_t)((ex << 1) | man);  /* exp field = floor(log2 q) + 1 */
+    }
+    return (uint8_t)(sign | mag);
+}
+
+/* Value of a 4-bit E2M1 code: exp field 0 is subnormal (0.5 * man), else
+ * 2^(exp-1) * (1 + man/2). */
+double oracle_e2m1_value(uint8_t code)
+{
+    int s = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* Quantise y [rows, k] fp32 into MXFP4: codes [rows, k/2] (element 2i in the
+ * low nibble of byte i) and one E8M0 byte (se + 127) per 32-block, row-major
+ * scales [rows, k/32]. */
+void oracle_quantize_mx(const float *y, int64_t rows, int64_t k, uint8_t *codes, uint8_t *scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            const float *blk = y + r * k + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(blk[i]);
+                if (a > amax) amax = a;
+            }
+            int se = oracle_scale_exponent(amax);
+            scales[r * (k / 32) + b] = (uint8_t)(se + 127);
+            for (int i = 0; i < 32; i += 2) {
+                float t0 = ldexpf(blk[i], -se);
+                float t1 = ldexpf(blk[i + 1], -se);
+                uint8_t c0 = oracle_e2m1_encode(t0);
+                uint8_t c1 = oracle_e2m1_encode(t1);
+                codes[r * (k / 2) + 16 * b + i / 2] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+    }
+}
+
+/* Whole activation (or weight) transform: balance, block Hadamard, MXFP4. */
+void oracle_quant(const uint16_t *x, int64_t rows, int64_t k, const float *f, uint8_t *codes,
+                  uint8_t *scales, float *work /* [rows, k] */)
+{
+    oracle_transform_f32(x, rows, k, f, work);
+    oracle_quantize_mx(work, rows, k, codes, scales);
+}
+
+/* deq[r, j] = value(code) * 2^(scale - 127), exactly, in fp64. */
+void oracle_dequant(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t k,
+                    double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < k; ++j) {
+            uint8_t byte = codes[r * (k / 2) + j / 2];
+            uint8_t code = (j & 1) ? (byte >> 4) : (byte & 0xf);
+            int se = (int)scales[r * (k / 32) + j / 32] - 127;
+            out[r * k + j] = ldexp(oracle_e2m1_value(code), se);
+        }
+    }
+}
+
+/* Y[m, n] = sum_k A[m, k] * B[n, k] in fp64, plain triple loop (small sizes;
+ * the Python wrapper uses a library matmul for large ones). */
+void oracle_gemm_f64(const double *a, const double *b, int64_t m, int64_t n, int64_t k, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double acc = 0.0;
+            for (int64_t p = 0; p < k; ++p) acc += a[i * k + p] * b[j * k + p];
+            y[i * n + j] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------ scale-factor tiling */
+
+/* Rearrange row-major E8M0 scales [rows, nkb] into the library's tiled
+ * layout.  Rows pad to a multiple of 128, scale columns to a multiple of 8;
+ * padding bytes are 0.  Tile (rb, ka) covers rows 128*rb.. and scale columns
+ * 4*ka..4*ka+3 and holds 512 bytes at ((rb * nka) + ka) * 512; inside it row
+ * r = 32*q + p, column c sits at byte 16*p + 4*q + c. */
+int64_t oracle_tiled_scale_bytes(int64_t rows, int64_t nkb)
+{
+    int64_t rp = (rows + 127) / 128 * 128;
+    int64_t kp = (nkb + 7) / 8 * 8;
+    return rp * kp;
+}
+
+void oracle_tile_scales(const uint8_t *src, int64_t rows, int64_t nkb, uint8_t *dst)
+{
+    int64_t rp = (rows + 127) / 128 * 128;
+    int64_t kp = (nkb + 7) / 8 * 8;
+    int64_t nka = kp / 4;
+    for (int64_t r = 0; r < rp; ++r) {
+        for (int64_t c = 0; c < kp; ++c) {
+            uint8_t v = (r < rows && c < nkb) ? src[r * nkb + c] : 0;
+            int64_t tile = (r / 128) * nka + c / 4;
+            int64_t p = r % 32, q = (r % 128) / 32;
+            dst[tile * 512 + 16 * p + 4 * q + (c % 4)] = v;
+        }
+    }
+}
+
+/* ------------------------------------------------ batch helpers (tests) */
+
+void oracle_e2m1_encode_many(const float *t, int64_t n, uint8_t *codes)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) codes[i] = oracle_e2m1_encode(t[i]);
+}
+
+void oracle_scale_exponent_many(const float *amax, int64_t n, int32_t *se)
+{
+    for (int64_t i = 0; i < n; ++i) se[i] = oracle_scale_exponent(amax[i]);
+}
