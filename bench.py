@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of the MACaQ W4A4 (MXFP4) linear layer on B300.
+
+One step = the whole online hot path on one batch: the activation transform
+(balance, 32-channel block Hadamard, MXFP4 encode; one CUDA kernel) followed by
+the block-scaled MXFP4 GEMM (one tcgen05 kernel), i.e. ``macaq_linear`` on the
+prefill attention projection M=4096 tokens, K=5120, N=5120 (``--config`` picks
+another dense workload).  Weights are prepared once, outside the timed region
+(balance from a 512-row calibration batch, fold, quantise).
+
+Reported (one JSON line on rank 0):
+  value          W4A4 linear TFLOP/s (2*M*N*K per step / device time), whole job
+  roofline       the GEMM kernel against the dense MXFP4 tensor peak (measured
+                 bf16 peak x the nominal fp4/bf16 ratio 13.5/2.25)
+  act_quant      the transform kernel's GB/s against measured HBM bandwidth
+  e2e            the same metric through the C ABI with pinned host buffers,
+                 host->device of X and device->host of Y inside the timing
+  cpu_baseline   the CPU oracle on a bounded row sample of the same workload
+
+Timing: W warm-up steps, then exactly K steps between a barrier and a device
+synchronise, CUDA events on the launching stream around every kernel; inputs
+rotate over enough copies that each step's working set was evicted from L2
+(126 MB) by the steps in between.  Multi-GPU: one independent replica per rank
+(rows are independent; no collective on the data path), max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense fp4 : bf16 tensor throughput on B300
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {
+        0x0000000000000001: "gpu_idle", 0x0000000000000002: "applications_clocks_setting",
+        0x0000000000000004: "sw_power_cap", 0x0000000000000008: "hw_slowdown",
+        0x0000000000000010: "sync_boost", 0x0000000000000020: "sw_thermal_slowdown",
+        0x0000000000000040: "hw_thermal_slowdown", 0x0000000000000080: "hw_power_brake_slowdown",
+        0x0000000000000100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.samples = []
+        self.reasons = set()
+        self.period = period_s
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # noqa: BLE001 - clocks are reported as unavailable
+            self.err = str(e)
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        n = self.nvml
+        while not self._stop.is_set():
+            try:
+                self.samples.append(n.nvmlDeviceGetClockInfo(self.h, n.NVML_CLOCK_SM))
+                r = n.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._t is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.err}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- oracle leg
+
+def oracle_linear_rate(d, rows: int, target_s: float):
+    """Time the CPU oracle (transform + MXFP4 of sampled rows, fp64 GEMM against
+    the prepared weight) and return (TFLOP/s, rows used, seconds, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    wl = d["workload"]
+    s, inv = oracle.balance_scales(d["X_calib"], d["W"])
+    cw, sw = oracle.quantize(d["W"], s)
+    deq_w = oracle.dequant(cw, sw)          # weight preparation: outside the timing
+
+    def run(n):
+        X = d["X"][:n]
+        t0 = time.perf_counter()
+        ca, sa = oracle.quantize(X, inv)
+        Y = oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
+        torch.from_numpy(Y).to(torch.bfloat16)
+        return time.perf_counter() - t0
+
+    run(min(rows, 4))
+    n = max(1, min(rows, 16))
+    dt = run(n)
+    while dt < target_s * 0.5 and n < min(rows, wl.M):
+        n = min(wl.M, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+        dt = run(n)
+    flops = 2.0 * n * wl.N * wl.K
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    return flops / dt / 1e12, n, dt, threads
+
+
+def reference_arm(args, rank: int, world: int):
+    """--impl reference: the CPU oracle as it stands, rank 0 only."""
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    import workloads
+    import oracle
+
+    d = workloads.make_dense(args.config)
+    wl = d["workload"]
+    s, inv = oracle.balance_scales(d["X_calib"], d["W"])
+    cw, sw = oracle.quantize(d["W"], s)
+    deq_w = oracle.dequant(cw, sw)
+    # size one step (a row sample) so the whole run takes about two minutes
+    t0 = time.perf_counter()
+    ca, sa = oracle.quantize(d["X"][:8], inv)
+    oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
+    per_row = (time.perf_counter() - t0) / 8
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(wl.M, budget / max(per_row, 1e-6))))
+
+    def step(i):
+        r0 = (i * rows) % max(1, wl.M - rows + 1)
+        ca, sa = oracle.quantize(d["X"][r0:r0 + rows], inv)
+        oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * wl.N * wl.K * args.steps
+    value = flops / dt / 1e12
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    sample = f"{rows} of {wl.M} rows per step (full N={wl.N}, K={wl.K})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (fp32 transform)", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "W4A4 linear TFLOPS + act-quant GB/s, as fraction of B300 FP4/HBM roofline"
+
+
+def workload_config(wl):
+    return {"workload": f"{wl.name}: M={wl.M} tokens, K={wl.K}, N={wl.N}, bf16 in/out, "
+                        f"MXFP4 W4A4",
+            "M": wl.M, "K": wl.K, "N": wl.N, "calib_rows": wl.calib_rows,
+            "l2": "inputs rotate over copies larger than L2 between steps"}
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    import w4a4_mxfp4_quantized_02_b300 as mq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mq.lib()
+    peaks = load_peaks()
+    d = workloads.make_dense(args.config)
+    wl = d["workload"]
+    M, N, K = wl.M, wl.N, wl.K
+    stream = torch.cuda.current_stream()
+
+    # offline preparation (not timed): calibration, fold, weight quantisation
+    Xc = d["X_calib"].to(dev)
+    W = d["W"].to(dev)
+    s, inv = mq.macaq_balance_scales(Xc, W)
+    w_codes, w_scales = mq.macaq_quant_weight(W, s)
+    del W, Xc
+
+    ws_bytes = mq.macaq_linear_workspace_bytes(M, K)
+    step_bytes = M * K * 2 + ws_bytes * 2 + w_codes.numel() + w_scales.numel() + M * N * 2
+    nsets = max(2, math.ceil(2.5 * L2_BYTES / step_bytes) + 1)
+    X0 = d["X"].to(dev)
+    sets = []
+    for i in range(nsets):
+        sets.append({
+            "X": X0.clone() if i else X0,
+            "wc": w_codes.clone() if i else w_codes,
+            "ws": w_scales.clone() if i else w_scales,
+            "Y": torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+            "a_codes": torch.empty(M, K // 2, dtype=torch.uint8, device=dev),
+            "a_scales": torch.empty(mq.macaq_scale_bytes(M, K), dtype=torch.uint8, device=dev),
+        })
+
+    def step(i, ev=None):
+        b = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        mq.macaq_quant_act(b["X"], inv, b["a_codes"], b["a_scales"])
+        if ev is not None:
+            ev[1].record(stream)
+        mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error during warm-up: {mq.macaq_status_string(status)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    with sampler:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
+
+    flops = 2.0 * M * N * K
+    value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    gemm_avg = statistics.mean(g_ms)
+    quant_avg = statistics.mean(q_ms)
+    gemm_tflops = flops / (gemm_avg * 1e-3) / 1e12
+    quant_bytes = M * K * 2 + M * K // 2 + M * K // 32
+    quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+
+    # end to end through the C ABI: pinned host X in, pinned host Y out
+    e2e_steps = max(3, min(args.steps, 50))
+    Xh = d["X"].pin_memory()
+    Yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    b = sets[0]
+    for _ in range(2):
+        b["X"].copy_(Xh, non_blocking=True)
+        mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+        Yh.copy_(b["Y"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        b["X"].copy_(Xh, non_blocking=True)
+        mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+        Yh.copy_(b["Y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tj = json.load(f)
+        if tj.get("workload") == wl.name and tj.get("kernel_rev") == KERNEL_REV:
+            traffic = tj.get("dram_bytes_per_launch")
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            rate, rows, dt, threads = oracle_linear_rate(d, wl.M, args.cpu_seconds)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{rows} of {wl.M} rows (full N={N}, K={K}), {dt:.1f} s; "
+                             "weight prepared outside the timing"}
+        except Exception as e:  # noqa: BLE001 - reported, not fatal
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
+                   "sample": f"failed: {e}"}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
+        "data": "synthetic",
+        "config": workload_config(wl),
+        "roofline": {"bound": "tensor", "kernel": "gemm_mxf4_kernel",
+                     "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / fp4_peak, "traffic": traffic,
+                     "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x "
+                                  f"{FP4_OVER_BF16:g} (nominal fp4/bf16)",
+                     "avg_launch_us": gemm_avg * 1e3},
+        "act_quant": {"kernel": "quant_kernel<Dense>", "achieved": quant_gbs,
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
+                      "avg_launch_us": quant_avg * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
+                "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+KERNEL_REV = "gemm-v1"
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["macaq", "reference"], default="macaq")
+    ap.add_argument("--config", default="attn")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        return gpu_arm(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,210 @@
+/*
+ * macaq.h -- C ABI of the MACaQ W4A4 (MXFP4) linear-layer library for B300
+ * (sm_103a).
+ *
+ * The method (MACaQ page "What is MACaQ quantization", section "How MACaQ
+ * works"): each linear layer balances its input channels with a per-channel
+ * scale, rotates each block of 32 channels with a Hadamard transform whose
+ * inverse is folded into the weights ahead of time (so the output is unchanged
+ * before rounding), and runs in W4A4 MXFP4 (FAQ "What is W4A4 quantization":
+ * 4-bit floats in blocks of 32 sharing one scale).  Scale and rotation run
+ * online at inference time (same section, closing paragraph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is device memory owned by the caller (unless the
+ *   comment says host).  The library allocates and frees nothing.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means the
+ *   legacy default stream).  No entry point synchronises, except
+ *   macaq_check_device_error and macaq_set_wait_timeout_ns.
+ * - Arguments are validated on the host before any launch; a rejected call
+ *   launches nothing and returns the matching MACAQ_ERR_* code.  A failed
+ *   launch returns MACAQ_ERR_CUDA.
+ * - bf16 means IEEE bfloat16 bits (uint16).  Inputs must be finite.
+ * - All pointers must be 16-byte aligned; leading dimensions (ldx, ldy) are
+ *   counted in elements and must be multiples of 8.  K must be a positive
+ *   multiple of 32.  M, N, rows may be 0 (nothing is launched).
+ *
+ * MXFP4 data layout
+ * -----------------
+ * codes   [rows, K/2] uint8, row-major, row pitch K/2 bytes.  Byte i of a row
+ *         holds element 2i in its low nibble and element 2i+1 in its high
+ *         nibble.  A nibble is E2M1: sign<<3 | exponent(2)<<1 | mantissa(1),
+ *         magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7.
+ * scales  one E8M0 byte (2^(byte-127)) per 32 consecutive elements of a row,
+ *         stored TILED: rows pad to a multiple of 128, scale columns (K/32)
+ *         to a multiple of 8, padding bytes are 0.  Tile (rb, ka) holds rows
+ *         128*rb .. 128*rb+127 and scale columns 4*ka .. 4*ka+3 in 512
+ *         contiguous bytes at offset (rb * nka + ka) * 512, nka = padded
+ *         columns / 4; within a tile, row 32*q + p, column c is byte
+ *         16*p + 4*q + c.  Size: macaq_scale_bytes(rows, K).
+ * The value of element (r, j) is E2M1(code) * 2^(scale - 127).
+ */
+#ifndef MACAQ_H
+#define MACAQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MACAQ_OK = 0,
+    MACAQ_ERR_INVALID_ARG = 1,  /* null pointer, negative size, K % 32 != 0 */
+    MACAQ_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned, ld % 8 != 0 */
+    MACAQ_ERR_UNSUPPORTED = 3,  /* size outside the supported range */
+    MACAQ_ERR_WORKSPACE = 4,    /* workspace missing or too small */
+    MACAQ_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+    MACAQ_ERR_TIMEOUT = 6       /* a device-side wait ran out (see below) */
+} macaq_status;
+
+typedef void *macaq_stream_t; /* cudaStream_t */
+
+/* Human-readable name of a status code (static string). */
+const char *macaq_status_string(macaq_status s);
+
+/* Bytes of a tiled scale array for `rows` rows of K elements. */
+size_t macaq_scale_bytes(int64_t rows, int64_t K);
+
+/* ----------------------------------------------------------- balance */
+
+/* Per-channel balance scales from calibration data (offline preparation).
+ * Source: section "How MACaQ works", step "Channel balancing" (a per-channel
+ * scale evens out the size of the input channels).
+ *   s[j]     = fp32( clamp( sqrt(cx_j / cw_j), 1e-2, 1e2 ) ), ratio and root in
+ *              fp64; cx_j = max_m |Xc[m, j]|, cw_j = max_n |W[n, j]|; cw_j = 0
+ *              gives 1e2, cx_j = cw_j = 0 gives 1.
+ *   inv_s[j] = 1.0f / s[j] (IEEE fp32 division).
+ * Xc      bf16 [Mc, ldxc]: calibration rows.  If xc_rows is not NULL, row m
+ *         of the batch is Xc row xc_rows[m] (int32, device), else row m.
+ * W       bf16 [N, K], row pitch K.
+ * s,inv_s fp32 [K] outputs.  Mc >= 0, N >= 0. */
+macaq_status macaq_balance_scales(const void *Xc, int64_t ldxc, const int32_t *xc_rows,
+                                  int64_t Mc, const void *W, int64_t N, int64_t K,
+                                  float *s, float *inv_s, macaq_stream_t stream);
+
+/* ------------------------------------------------- transform + MXFP4 */
+
+/* Online activation transform (the hot path's first half).
+ * Source: section "How MACaQ works" (balance, then 32-channel block Hadamard,
+ * run online) and FAQ "What is W4A4 quantization" (MXFP4).
+ * For each row m and 32-block b (j = 32b + i):
+ *   v_i = fp32(X[m, j]) * inv_s[j]                        (fp32, rounded)
+ *   v  <- butterflies at stride 1, 2, 4, 8, 16: (a, b) -> (a + b, a - b)
+ *   y_i = v_i * fp32(1/sqrt 32)
+ *   se  = clamp(floor(log2 max_i |y_i|) - 2, -127, 127)   (all-zero: -127)
+ *   code_i = E2M1(y_i * 2^-se), round to nearest, ties to even code,
+ *            saturate at 6, sign kept (also on values that round to 0)
+ * X       bf16 [M, ldx]; inv_s fp32 [K].
+ * a_codes [M, K/2]; a_scales tiled, macaq_scale_bytes(M, K) bytes (every
+ *         byte written, padding included). */
+macaq_status macaq_quant_act(const void *X, int64_t ldx, const float *inv_s, int64_t M,
+                             int64_t K, uint8_t *a_codes, uint8_t *a_scales,
+                             macaq_stream_t stream);
+
+/* Offline weight preparation: the same transform with factor s (the inverse
+ * balance and the Hadamard folded into the weights, section "How MACaQ works",
+ * "A small Hadamard transform"), then MXFP4.
+ * W [N, K] bf16 row pitch K; s fp32 [K]; w_codes [N, K/2];
+ * w_scales macaq_scale_bytes(N, K) bytes. */
+macaq_status macaq_quant_weight(const void *W, const float *s, int64_t N, int64_t K,
+                                uint8_t *w_codes, uint8_t *w_scales, macaq_stream_t stream);
+
+/* Grouped (per-expert) weight preparation: E experts, W [E, N, K] bf16,
+ * s [E, K] fp32 (expert e uses row e); w_codes [E, N, K/2]; w_scales holds E
+ * consecutive tiled arrays of macaq_scale_bytes(N, K) bytes each. */
+macaq_status macaq_quant_weight_grouped(const void *W, const float *s, int64_t E, int64_t N,
+                                        int64_t K, uint8_t *w_codes, uint8_t *w_scales,
+                                        macaq_stream_t stream);
+
+/* ------------------------------------------------------------ GEMM */
+
+/* Block-scaled MXFP4 x MXFP4 GEMM with bf16 output (the hot path's second
+ * half; W4A4 is the default inference mode, page "Huawei MACaQ", section
+ * "MACaQ Backends").
+ *   Y[m, n] = bf16_rn( sum_k A(m, k) * Wq(n, k) ), each operand an E2M1 code
+ *             times its block's 2^(scale-127); products exact, accumulation
+ *             in fp32 on the tensor cores (tcgen05, kind::mxf4).
+ * a_codes [M, K/2], a_scales tiled for M rows; w_codes [N, K/2], w_scales
+ * tiled for N rows; Y bf16 [M, ldy], ldy >= N. */
+macaq_status macaq_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
+                             const uint8_t *w_codes, const uint8_t *w_scales, int64_t M,
+                             int64_t N, int64_t K, void *Y, int64_t ldy, macaq_stream_t stream);
+
+/* Workspace bytes macaq_linear needs for M rows of K channels. */
+size_t macaq_linear_workspace_bytes(int64_t M, int64_t K);
+
+/* The whole online layer: macaq_quant_act into `workspace`, then
+ * macaq_w4a4_gemm, both on `stream`.  Y = X diag(1/s) H (W diag(s) H)^T up
+ * to MXFP4 rounding.  workspace: device, ws_bytes >=
+ * macaq_linear_workspace_bytes(M, K), 256-byte aligned, contents scratch. */
+macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s,
+                          const uint8_t *w_codes, const uint8_t *w_scales, int64_t M,
+                          int64_t N, int64_t K, void *Y, int64_t ldy, void *workspace,
+                          size_t ws_bytes, macaq_stream_t stream);
+
+/* ---------------------------------------------------- grouped (MoE) */
+
+/* Rows of the expert-padded layout the grouped kernels use for `rows`
+ * expert-sorted rows over E experts: every expert's rows start on a multiple
+ * of 128 (an upper bound; the exact layout follows expert_offsets). */
+int64_t macaq_grouped_padded_rows(int64_t rows, int64_t E);
+
+/* Grouped activation transform for routed MoE experts (the routed experts
+ * run W4A4, page "Huawei MACaQ", section "MACaQ Backends").
+ * Rows are sorted by expert: sorted row r belongs to expert e for
+ * expert_offsets[e] <= r < expert_offsets[e+1] (int32 [E+1], device,
+ * nondecreasing, offsets[0] = 0, offsets[E] = rows) and reads token row
+ * X[row_src[r]] (int32 [rows], device).  It is transformed with inv_s row e
+ * (fp32 [E, K]) and written to padded row p = P_e + (r - offsets[e]) with
+ * P_e = sum_{e' < e} 128 * ceil(count_e' / 128).
+ * a_codes [P, K/2], a_scales tiled for P rows, P =
+ * macaq_grouped_padded_rows(rows, E).  Scale bytes of padding rows are 0;
+ * code bytes of padding rows are left unspecified.  E <= 256. */
+macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *row_src,
+                                     const int32_t *expert_offsets, const float *inv_s,
+                                     int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
+                                     uint8_t *a_scales, macaq_stream_t stream);
+
+/* Grouped GEMM: for each expert e and sorted row r of e,
+ *   Y[r, n] = bf16_rn( sum_k A(P_e + r - offsets[e], k) * Wq_e(n, k) )
+ * with A from macaq_quant_act_grouped and Wq_e from
+ * macaq_quant_weight_grouped (w_codes [E, N, K/2], w_scales E tiled arrays).
+ * Y bf16 [rows, ldy] in sorted row order.  E <= 256. */
+macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
+                                     const uint8_t *w_codes, const uint8_t *w_scales,
+                                     const int32_t *expert_offsets, int64_t rows, int64_t E,
+                                     int64_t N, int64_t K, void *Y, int64_t ldy,
+                                     macaq_stream_t stream);
+
+/* --------------------------------------------------- device errors */
+
+/* Every device-side wait of the GEMM kernels is bounded in time.  A wait that
+ * runs out sets a device error flag and the kernel returns early (its output
+ * is then undefined) instead of hanging.
+ * macaq_check_device_error synchronises `stream`, reads and clears the flag
+ * of the current device, and returns MACAQ_ERR_TIMEOUT if it was set. */
+macaq_status macaq_check_device_error(macaq_stream_t stream);
+
+/* Sets the bound of each device-side wait on the current device, in
+ * nanoseconds (default 4e9).  Synchronous. */
+macaq_status macaq_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for the bounded wait: launches one thread that waits on a
+ * barrier nothing ever signals; it gives up after the configured bound and
+ * sets the device error flag. */
+macaq_status macaq_debug_wait_probe(macaq_stream_t stream);
+
+/* Test hook for the element encoder: codes[i] = E2M1 code of t[i] (fp32, any
+ * finite value; |t| > 6 saturates), as the quantisation kernels compute it.
+ * t fp32 [n], codes uint8 [n]. */
+macaq_status macaq_debug_e2m1(const float *t, int64_t n, uint8_t *codes,
+                              macaq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MACAQ_H */

@@ -1,0 +1,121 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports every
+entry point the header declares, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a4_mxfp4_quantized_02_b300 as mq
+from w4a4_mxfp4_quantized_02_b300 import build as mq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "macaq.h")
+
+OK, INVALID, ALIGN, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def L():
+    mq_build.build()
+    return mq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(macaq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in mq._SIGS, f"binding lacks {n}"
+
+
+def test_sizes(L):
+    assert mq.macaq_scale_bytes(16, 128) == 128 * 8
+    assert mq.macaq_scale_bytes(129, 256) == 256 * 8
+    assert mq.macaq_scale_bytes(1, 5120) == 128 * 160
+    assert mq.macaq_scale_bytes(4096, 768) == 4096 * 24
+    assert mq.macaq_scale_bytes(10, 100) == 0          # K % 32 != 0
+    assert mq.macaq_linear_workspace_bytes(16, 128) == 1024 + 1024
+    assert mq.macaq_grouped_padded_rows(32768, 128) == 32768 + 127 * 128
+    assert mq.macaq_status_string(6) == "device-side wait timed out"
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_quant_act_rejections(L):
+    f = L.macaq_quant_act
+    p = _fake()
+    assert f(p, 128, p, 16, 100, p, p, None) == INVALID        # K % 32
+    assert f(p, 128, p, 16, 0, p, p, None) == INVALID          # K = 0
+    assert f(p, 128, p, -1, 128, p, p, None) == INVALID        # negative M
+    assert f(None, 128, p, 16, 128, p, p, None) == INVALID     # null X
+    assert f(p, 64, p, 16, 128, p, p, None) == INVALID         # ldx < K
+    assert f(_fake(0x10008), 128, p, 16, 128, p, p, None) == ALIGN
+    assert f(p, 132, p, 16, 128, p, p, None) == ALIGN          # ldx % 8
+    assert f(p, 128, p, 0, 128, p, p, None) == OK              # empty: no launch
+    assert f(p, 1 << 33, p, 1 << 32, 128, p, p, None) == UNSUPPORTED
+
+
+def test_gemm_rejections(L):
+    g = L.macaq_w4a4_gemm
+    p = _fake()
+    assert g(p, p, p, p, 16, 64, 100, p, 64, None) == INVALID
+    assert g(p, p, p, p, 16, 64, 128, None, 64, None) == INVALID
+    assert g(p, p, p, p, 16, 64, 128, p, 32, None) == INVALID  # ldy < N
+    assert g(p, p, p, p, 16, 64, 128, p, 68, None) == ALIGN
+    assert g(p, _fake(0x10004), p, p, 16, 64, 128, p, 64, None) == ALIGN
+    assert g(p, p, p, p, 0, 64, 128, p, 64, None) == OK
+    assert g(p, p, p, p, 16, 0, 128, p, 64, None) == OK
+
+
+def test_linear_workspace_rejections(L):
+    f = L.macaq_linear
+    p = _fake()
+    need = mq.macaq_linear_workspace_bytes(16, 128)
+    assert f(p, 128, p, p, p, 16, 64, 128, p, 64, None, need, None) == WORKSPACE
+    assert f(p, 128, p, p, p, 16, 64, 128, p, 64, p, need - 1, None) == WORKSPACE
+    assert f(p, 128, p, p, p, 16, 64, 128, p, 64, _fake(0x10010), need, None) == ALIGN
+
+
+def test_grouped_rejections(L):
+    q = L.macaq_quant_act_grouped
+    g = L.macaq_grouped_w4a4_gemm
+    p = _fake()
+    assert q(p, 128, p, p, p, 100, 0, 128, p, p, None) == INVALID      # E = 0
+    assert q(p, 128, p, p, p, 100, 257, 128, p, p, None) == UNSUPPORTED
+    assert q(p, 128, p, None, p, 100, 4, 128, p, p, None) == INVALID
+    assert g(p, p, p, p, p, 100, 300, 64, 128, p, 64, None) == UNSUPPORTED
+    assert g(p, p, p, p, None, 100, 4, 64, 128, p, 64, None) == INVALID
+    assert g(p, p, p, p, p, 0, 4, 64, 128, p, 64, None) == OK
+
+
+def test_balance_rejections(L):
+    b = L.macaq_balance_scales
+    p = _fake()
+    assert b(p, 128, None, 4, p, 8, 100, p, p, None) == INVALID
+    assert b(p, 128, None, 4, p, 8, 128, None, p, None) == INVALID
+    assert b(p, 64, None, 4, p, 8, 128, p, p, None) == INVALID       # ldxc < K
+    assert b(p, 136, None, 4, p, 8, 128, p, _fake(0x10004), None) == ALIGN
+
+
+def test_no_cross_imports():
+    """The oracle and the product path share no code and never import each other."""
+    pkg = os.path.join(ROOT, "w4a4_mxfp4_quantized_02_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.lower(), f"{fn} mentions the oracle"
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "w4a4_mxfp4_quantized_02_b300" not in text
+            assert "macaq.h" not in text

@@ -1,0 +1,176 @@
+"""GPU parity of the grouped (MoE expert) path: per-expert balance, grouped
+activation transform into the expert-padded layout (bit-exact), grouped weight
+preparation (bit-exact) and the grouped block-scaled GEMM (2 bf16 ulps).
+
+Routed experts run W4A4 (page "Huawei MACaQ Is an Open-Source Model
+Quantizer", section "MACaQ Backends").
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import w4a4_mxfp4_quantized_02_b300 as mq
+from gpu_common import DEV, require_gpu, to_dev, u8
+from helpers import bf16_to_np, check_gemm, untile_scales
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def padded_positions(offsets: np.ndarray) -> np.ndarray:
+    """Padded row of every sorted row (each expert starts on a multiple of 128)."""
+    cnt = np.diff(offsets)
+    pstart = np.concatenate([[0], np.cumsum((cnt + 127) // 128 * 128)])
+    pos = np.empty(int(offsets[-1]), np.int64)
+    for e in range(len(cnt)):
+        pos[offsets[e]:offsets[e + 1]] = pstart[e] + np.arange(cnt[e])
+    return pos
+
+
+@functools.lru_cache(maxsize=2)
+def moe(name: str):
+    return workloads.make_moe(workloads.MOE_SMALL if name == "small" else workloads.MOE)
+
+
+def _calib_rows(routing, e):
+    off = routing["offsets"].numpy()
+    return routing["row_src"][off[e]:off[e + 1]]
+
+
+def run_gate_up(d, experts=None):
+    """CUDA path and oracle for the gate+up projection; returns both sides."""
+    wl = d["workload"]
+    E, K, F = wl.E, wl.K, wl.F
+    W = to_dev(d["W_gu"])
+    Xc = to_dev(d["X_calib"])
+    s = torch.empty(E, K, dtype=torch.float32, device=DEV)
+    inv = torch.empty_like(s)
+    for e in range(E):
+        rows = to_dev(_calib_rows(d["calib_routing"], e))
+        se, ie = mq.macaq_balance_scales(Xc, W[e], xc_rows=rows)
+        s[e], inv[e] = se, ie
+    w_codes, w_scales = mq.macaq_quant_weight_grouped(W, s)
+    r = d["routing"]
+    rows_n = int(r["offsets"][-1])
+    offs = to_dev(r["offsets"])
+    a_codes, a_scales = mq.macaq_quant_act_grouped(to_dev(d["X"]), to_dev(r["row_src"]), offs, inv,
+                                                   rows_n, E)
+    Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, 2 * F, K)
+    torch.cuda.synchronize()
+    return dict(s=s, inv=inv, w_codes=w_codes, w_scales=w_scales, a_codes=a_codes,
+                a_scales=a_scales, Y=Y)
+
+
+def check_expert(d, gpu, e, Wkey, Xrows_bf16, s_ref, inv_ref, N, K, row_lo, row_hi):
+    """Bit-exact weight/activation codes and GEMM tolerance for expert e."""
+    cw, sw = oracle.quantize(d[Wkey][e], s_ref)
+    sb = mq.macaq_scale_bytes(N, K)
+    np.testing.assert_array_equal(u8(gpu["w_codes"][e]), cw)
+    np.testing.assert_array_equal(u8(gpu["w_scales"][e * sb:(e + 1) * sb]), oracle.tile_scales(sw))
+    if row_hi == row_lo:
+        return
+    ca, sa = oracle.quantize(Xrows_bf16, inv_ref)
+    pos = gpu["pos"][row_lo:row_hi]
+    np.testing.assert_array_equal(u8(gpu["a_codes"])[pos], ca)
+    P = gpu["a_codes"].shape[0]
+    np.testing.assert_array_equal(untile_scales(u8(gpu["a_scales"]), P, K)[pos], sa)
+    da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+    check_gemm(bf16_to_np(gpu["Y"][row_lo:row_hi]), oracle.gemm_ref(da, dw),
+               oracle.abs_gemm_ref(da, dw), K)
+
+
+@pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 1, 64, 127))])
+def test_gate_up(name, experts):
+    d = moe(name)
+    wl = d["workload"]
+    gpu = run_gate_up(d)
+    r = d["routing"]
+    off = r["offsets"].numpy()
+    gpu["pos"] = padded_positions(off)
+    for e in (range(wl.E) if experts is None else experts):
+        s_ref, inv_ref = oracle.balance_scales(d["X_calib"][_calib_rows(d["calib_routing"], e).long()],
+                                               d["W_gu"][e])
+        np.testing.assert_array_equal(gpu["s"][e].cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+        np.testing.assert_array_equal(gpu["inv"][e].cpu().numpy().view(np.uint32),
+                                      inv_ref.view(np.uint32))
+        Xrows = d["X"][r["row_src"][off[e]:off[e + 1]].long()]
+        check_expert(d, gpu, e, "W_gu", Xrows, s_ref, inv_ref, 2 * wl.F, wl.K, off[e], off[e + 1])
+
+
+@pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 5, 99, 127))])
+def test_down(name, experts):
+    """Down projection on stand-alone SiLU(a)*b inputs in sorted-row order."""
+    d = moe(name)
+    wl = d["workload"]
+    E, F, Kh = wl.E, wl.F, wl.K
+    W = to_dev(d["W_down"])
+    cr = d["calib_routing"]["offsets"].numpy()
+    Xdc = to_dev(d["Xd_calib"])
+    s = torch.empty(E, F, dtype=torch.float32, device=DEV)
+    inv = torch.empty_like(s)
+    for e in range(E):
+        se, ie = mq.macaq_balance_scales(Xdc[cr[e]:cr[e + 1]], W[e])
+        s[e], inv[e] = se, ie
+    w_codes, w_scales = mq.macaq_quant_weight_grouped(W, s)
+    r = d["routing"]
+    off = r["offsets"].numpy()
+    rows_n = int(off[-1])
+    ident = torch.arange(rows_n, dtype=torch.int32, device=DEV)
+    offs = to_dev(r["offsets"])
+    a_codes, a_scales = mq.macaq_quant_act_grouped(to_dev(d["Xd"]), ident, offs, inv, rows_n, E)
+    Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, Kh, F)
+    torch.cuda.synchronize()
+    gpu = dict(w_codes=w_codes, w_scales=w_scales, a_codes=a_codes, a_scales=a_scales, Y=Y,
+               pos=padded_positions(off))
+    for e in (range(E) if experts is None else experts):
+        s_ref, inv_ref = oracle.balance_scales(d["Xd_calib"][cr[e]:cr[e + 1]], d["W_down"][e])
+        np.testing.assert_array_equal(s[e].cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+        check_expert(d, gpu, e, "W_down", d["Xd"][off[e]:off[e + 1]], s_ref, inv_ref, Kh, F,
+                     off[e], off[e + 1])
+
+
+@pytest.mark.parametrize("counts", [(0, 300, 0, 5, 0, 129, 128, 1), (0, 0, 0, 0, 0, 0, 0, 77),
+                                    (256, 0, 0, 0, 0, 0, 0, 0)])
+def test_uneven_and_empty_experts(counts):
+    E, K, N = 8, 256, 264
+    rows_n = int(sum(counts))
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    X = workloads.make_matrix(rows_n + 3, K, seed=rows_n, outlier_channels=(4, 200))
+    row_src = np.random.default_rng(rows_n).integers(0, rows_n + 3, rows_n).astype(np.int32)
+    W = torch.stack([workloads.make_weight(N, K, seed=100 + e) for e in range(E)])
+    rng = np.random.default_rng(1)
+    s_np = rng.uniform(0.05, 20.0, (E, K)).astype(np.float32)
+    inv_np = (np.float32(1.0) / s_np).astype(np.float32)
+    w_codes, w_scales = mq.macaq_quant_weight_grouped(to_dev(W), torch.from_numpy(s_np).to(DEV))
+    offs = torch.from_numpy(offsets).to(DEV)
+    a_codes, a_scales = mq.macaq_quant_act_grouped(
+        to_dev(X), torch.from_numpy(row_src).to(DEV), offs, torch.from_numpy(inv_np).to(DEV),
+        rows_n, E)
+    Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, N, K)
+    torch.cuda.synchronize()
+    pos = padded_positions(offsets)
+    P = a_codes.shape[0]
+    sc = untile_scales(u8(a_scales), P, K)
+    # padding rows inside the used range carry zero scales
+    used = int(np.sum((np.diff(offsets) + 127) // 128 * 128))
+    pad_rows = np.setdiff1d(np.arange(used), pos)
+    assert not sc[pad_rows].any()
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue
+        Xrows = X[torch.from_numpy(row_src[lo:hi]).long()]
+        ca, sa = oracle.quantize(Xrows, inv_np[e])
+        np.testing.assert_array_equal(u8(a_codes)[pos[lo:hi]], ca)
+        np.testing.assert_array_equal(sc[pos[lo:hi]], sa)
+        cw, sw = oracle.quantize(W[e], s_np[e])
+        da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+        check_gemm(bf16_to_np(Y[lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)

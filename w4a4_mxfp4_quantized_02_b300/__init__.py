@@ -1,0 +1,263 @@
+"""MACaQ W4A4 (MXFP4) linear layer on B300: thin Python binding of ``libmacaq.so``.
+
+Every function here only marshals arguments -- it allocates outputs with torch
+on the device when the caller passes none, takes raw device pointers and the
+current CUDA stream, and calls the C entry point of the same name declared in
+``include/macaq.h``.  All arithmetic runs in the library's CUDA kernels; there
+is no CPU fallback, and a missing library raises ``MacaqLibraryMissing``.
+
+Layouts (see the header): codes [rows, K/2] uint8 (element 2i in the low
+nibble), scales tiled E8M0 bytes of ``macaq_scale_bytes(rows, K)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmacaq.so")
+
+MACAQ_OK = 0
+STATUS_NAMES = {
+    0: "MACAQ_OK", 1: "MACAQ_ERR_INVALID_ARG", 2: "MACAQ_ERR_ALIGNMENT",
+    3: "MACAQ_ERR_UNSUPPORTED", 4: "MACAQ_ERR_WORKSPACE", 5: "MACAQ_ERR_CUDA",
+    6: "MACAQ_ERR_TIMEOUT",
+}
+
+
+class MacaqLibraryMissing(RuntimeError):
+    pass
+
+
+class MacaqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_SIGS = {
+    "macaq_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "macaq_scale_bytes": ([_I64, _I64], _SZ),
+    "macaq_grouped_padded_rows": ([_I64, _I64], _I64),
+    "macaq_linear_workspace_bytes": ([_I64, _I64], _SZ),
+    "macaq_balance_scales": ([_P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_act": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_weight": ([_P, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_weight_grouped": ([_P, _P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_w4a4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_linear": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
+                     ctypes.c_int),
+    "macaq_quant_act_grouped": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P],
+                                ctypes.c_int),
+    "macaq_grouped_w4a4_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P],
+                                ctypes.c_int),
+    "macaq_check_device_error": ([_P], ctypes.c_int),
+    "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
+    "macaq_debug_wait_probe": ([_P], ctypes.c_int),
+    "macaq_debug_e2m1": ([_P, _I64, _P, _P], ctypes.c_int),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MacaqLibraryMissing(
+                f"{LIB_PATH} not found: build it with "
+                "`python -m w4a4_mxfp4_quantized_02_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != MACAQ_OK:
+        raise MacaqError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+# ------------------------------------------------------------------ sizes
+
+def macaq_scale_bytes(rows: int, K: int) -> int:
+    return int(lib().macaq_scale_bytes(rows, K))
+
+
+def macaq_grouped_padded_rows(rows: int, E: int) -> int:
+    return int(lib().macaq_grouped_padded_rows(rows, E))
+
+
+def macaq_linear_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().macaq_linear_workspace_bytes(M, K))
+
+
+def macaq_status_string(status: int) -> str:
+    return lib().macaq_status_string(status).decode()
+
+
+# --------------------------------------------------------------- balance
+
+def macaq_balance_scales(X_calib: torch.Tensor, W: torch.Tensor, xc_rows: torch.Tensor | None = None,
+                         stream=None):
+    """(s, inv_s) fp32 [K] on the device from calibration rows and the weight."""
+    _dev(X_calib, "X_calib")
+    _dev(W, "W")
+    K = W.shape[-1]
+    Mc = X_calib.shape[0] if xc_rows is None else xc_rows.numel()
+    s = torch.empty(K, dtype=torch.float32, device=W.device)
+    inv = torch.empty_like(s)
+    _check("macaq_balance_scales", lib().macaq_balance_scales(
+        _ptr(X_calib), _ld(X_calib), _ptr(xc_rows), Mc, _ptr(W), W.reshape(-1, K).shape[0], K,
+        _ptr(s), _ptr(inv), _stream(stream)))
+    return s, inv
+
+
+# ------------------------------------------------------ transform + MXFP4
+
+def macaq_quant_act(X: torch.Tensor, inv_s: torch.Tensor, a_codes=None, a_scales=None, stream=None):
+    _dev(X, "X")
+    M, K = X.shape
+    if a_codes is None:
+        a_codes = torch.empty(M, K // 2, dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty(macaq_scale_bytes(M, K), dtype=torch.uint8, device=X.device)
+    _check("macaq_quant_act", lib().macaq_quant_act(
+        _ptr(X), _ld(X), _ptr(inv_s), M, K, _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    return a_codes, a_scales
+
+
+def macaq_quant_weight(W: torch.Tensor, s: torch.Tensor, w_codes=None, w_scales=None, stream=None):
+    _dev(W, "W")
+    N, K = W.shape
+    if W.stride(0) != K or W.stride(1) != 1:
+        raise ValueError("W must be contiguous [N, K]")
+    if w_codes is None:
+        w_codes = torch.empty(N, K // 2, dtype=torch.uint8, device=W.device)
+    if w_scales is None:
+        w_scales = torch.empty(macaq_scale_bytes(N, K), dtype=torch.uint8, device=W.device)
+    _check("macaq_quant_weight", lib().macaq_quant_weight(
+        _ptr(W), _ptr(s), N, K, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
+    return w_codes, w_scales
+
+
+def macaq_quant_weight_grouped(W: torch.Tensor, s: torch.Tensor, w_codes=None, w_scales=None,
+                               stream=None):
+    _dev(W, "W")
+    E, N, K = W.shape
+    if not W.is_contiguous():
+        raise ValueError("W must be contiguous [E, N, K]")
+    if w_codes is None:
+        w_codes = torch.empty(E, N, K // 2, dtype=torch.uint8, device=W.device)
+    if w_scales is None:
+        w_scales = torch.empty(E * macaq_scale_bytes(N, K), dtype=torch.uint8, device=W.device)
+    _check("macaq_quant_weight_grouped", lib().macaq_quant_weight_grouped(
+        _ptr(W), _ptr(s), E, N, K, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
+    return w_codes, w_scales
+
+
+# ------------------------------------------------------------------ GEMM
+
+def macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M: int, N: int, K: int, Y=None,
+                    stream=None):
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=a_codes.device)
+    _check("macaq_w4a4_gemm", lib().macaq_w4a4_gemm(
+        _ptr(a_codes), _ptr(a_scales), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
+        _stream(stream)))
+    return Y
+
+
+def macaq_linear(X: torch.Tensor, inv_s, w_codes, w_scales, N: int, Y=None, workspace=None,
+                 stream=None):
+    _dev(X, "X")
+    M, K = X.shape
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
+    ws_need = macaq_linear_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=X.device)
+    _check("macaq_linear", lib().macaq_linear(
+        _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return Y
+
+
+# ----------------------------------------------------------- grouped (MoE)
+
+def macaq_quant_act_grouped(X, row_src, expert_offsets, inv_s, rows: int, E: int, a_codes=None,
+                            a_scales=None, stream=None):
+    _dev(X, "X")
+    K = X.shape[1]
+    P = macaq_grouped_padded_rows(rows, E)
+    if a_codes is None:
+        a_codes = torch.empty(P, K // 2, dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty(macaq_scale_bytes(P, K), dtype=torch.uint8, device=X.device)
+    _check("macaq_quant_act_grouped", lib().macaq_quant_act_grouped(
+        _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
+        _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    return a_codes, a_scales
+
+
+def macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, expert_offsets, rows: int,
+                            E: int, N: int, K: int, Y=None, stream=None):
+    if Y is None:
+        Y = torch.empty(rows, N, dtype=torch.bfloat16, device=a_codes.device)
+    _check("macaq_grouped_w4a4_gemm", lib().macaq_grouped_w4a4_gemm(
+        _ptr(a_codes), _ptr(a_scales), _ptr(w_codes), _ptr(w_scales), _ptr(expert_offsets), rows,
+        E, N, K, _ptr(Y), _ld(Y), _stream(stream)))
+    return Y
+
+
+# ---------------------------------------------------------- device errors
+
+def macaq_check_device_error(stream=None) -> int:
+    """Synchronise the stream; return the status (MACAQ_ERR_TIMEOUT if a wait ran out)."""
+    return int(lib().macaq_check_device_error(_stream(stream)))
+
+
+def macaq_set_wait_timeout_ns(ns: int):
+    _check("macaq_set_wait_timeout_ns", lib().macaq_set_wait_timeout_ns(ns))
+
+
+def macaq_debug_wait_probe(stream=None):
+    _check("macaq_debug_wait_probe", lib().macaq_debug_wait_probe(_stream(stream)))
+
+
+def macaq_debug_e2m1(t: torch.Tensor, stream=None) -> torch.Tensor:
+    _dev(t, "t")
+    t = t.contiguous().float()
+    out = torch.empty(t.numel(), dtype=torch.uint8, device=t.device)
+    _check("macaq_debug_e2m1", lib().macaq_debug_e2m1(_ptr(t), t.numel(), _ptr(out),
+                                                       _stream(stream)))
+    return out

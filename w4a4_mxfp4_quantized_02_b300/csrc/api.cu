@@ -1,0 +1,287 @@
+// C ABI of the MACaQ W4A4 library: argument checks, then launches.  Every
+// check runs on the host before anything is enqueued; nothing here allocates,
+// frees or synchronises (except the two documented error helpers).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "macaq.h"
+
+using namespace macaq;
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+macaq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MACAQ_OK : MACAQ_ERR_CUDA; }
+
+macaq_status check_k(int64_t K)
+{
+    if (K <= 0 || K % 32 != 0) return MACAQ_ERR_INVALID_ARG;
+    if (K > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    return MACAQ_OK;
+}
+
+macaq_status check_rows(int64_t rows)
+{
+    if (rows < 0) return MACAQ_ERR_INVALID_ARG;
+    if (rows > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    return MACAQ_OK;
+}
+
+#define MACAQ_TRY(expr)                       \
+    do {                                      \
+        macaq_status s__ = (expr);            \
+        if (s__ != MACAQ_OK) return s__;      \
+    } while (0)
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char *macaq_status_string(macaq_status s)
+{
+    switch (s) {
+    case MACAQ_OK: return "ok";
+    case MACAQ_ERR_INVALID_ARG: return "invalid argument";
+    case MACAQ_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case MACAQ_ERR_UNSUPPORTED: return "unsupported size";
+    case MACAQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case MACAQ_ERR_CUDA: return "CUDA error";
+    case MACAQ_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t macaq_scale_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0) return 0;
+    return tiled_scale_bytes(rows, K);
+}
+
+int64_t macaq_grouped_padded_rows(int64_t rows, int64_t E)
+{
+    if (rows < 0 || E <= 0) return 0;
+    return grouped_padded_rows(rows, E);
+}
+
+macaq_status macaq_balance_scales(const void *Xc, int64_t ldxc, const int32_t *xc_rows, int64_t Mc,
+                                  const void *W, int64_t N, int64_t K, float *s, float *inv_s,
+                                  macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(Mc));
+    MACAQ_TRY(check_rows(N));
+    if (!s || !inv_s || (Mc > 0 && !Xc) || (N > 0 && !W)) return MACAQ_ERR_INVALID_ARG;
+    if (Mc > 0 && ldxc < K) return MACAQ_ERR_INVALID_ARG;
+    if ((Xc && !aligned16(Xc)) || (W && !aligned16(W)) || !aligned16(s) || !aligned16(inv_s) ||
+        (Mc > 0 && ldxc % 8 != 0))
+        return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_balance(static_cast<const uint16_t *>(Xc), ldxc, xc_rows, Mc,
+                                    static_cast<const uint16_t *>(W), N, K, s, inv_s,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_quant_act(const void *X, int64_t ldx, const float *inv_s, int64_t M, int64_t K,
+                             uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(M));
+    if (M == 0) return MACAQ_OK;
+    if (!X || !inv_s || !a_codes || !a_scales || ldx < K) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(inv_s) || !aligned16(a_codes) || !aligned16(a_scales) ||
+        ldx % 8 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(X);
+    a.ld_src = ldx;
+    a.f = inv_s;
+    a.K = K;
+    a.rows_valid = M;
+    a.rows_out = pad_rows(M);
+    a.E = 1;
+    a.codes = a_codes;
+    a.scales = a_scales;
+    return from_cuda(launch_quant(QuantMode::Dense, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_quant_weight(const void *W, const float *s, int64_t N, int64_t K,
+                                uint8_t *w_codes, uint8_t *w_scales, macaq_stream_t stream)
+{
+    return macaq_quant_act(W, K, s, N, K, w_codes, w_scales, stream);
+}
+
+macaq_status macaq_quant_weight_grouped(const void *W, const float *s, int64_t E, int64_t N,
+                                        int64_t K, uint8_t *w_codes, uint8_t *w_scales,
+                                        macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(N));
+    if (E < 0) return MACAQ_ERR_INVALID_ARG;
+    if (E == 0 || N == 0) return MACAQ_OK;
+    if (E * pad_rows(N) > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (!W || !s || !w_codes || !w_scales) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(s) || !aligned16(w_codes) || !aligned16(w_scales))
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(W);
+    a.ld_src = K;
+    a.f = s;
+    a.K = K;
+    a.rows_valid = N;
+    a.group_rows_pad = pad_rows(N);
+    a.rows_out = E * pad_rows(N);
+    a.E = static_cast<int32_t>(E);
+    a.codes = w_codes;
+    a.scales = w_scales;
+    a.scale_group_stride = tiled_scale_bytes(N, K);
+    return from_cuda(launch_quant(QuantMode::WeightGrouped, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
+                             const uint8_t *w_codes, const uint8_t *w_scales, int64_t M, int64_t N,
+                             int64_t K, void *Y, int64_t ldy, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(M));
+    MACAQ_TRY(check_rows(N));
+    if (M == 0 || N == 0) return MACAQ_OK;
+    if (!a_codes || !a_scales || !w_codes || !w_scales || !Y || ldy < N) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) ||
+        !aligned16(Y) || ldy % 8 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    GemmArgs g{};
+    g.a_codes = a_codes;
+    g.a_scales = a_scales;
+    g.w_codes = w_codes;
+    g.w_scales = w_scales;
+    g.M = M;
+    g.a_rows = M;
+    g.N = N;
+    g.K = K;
+    g.E = 0;
+    g.Y = Y;
+    g.ldy = ldy;
+    return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
+size_t macaq_linear_workspace_bytes(int64_t M, int64_t K)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0) return 0;
+    return align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2)) + tiled_scale_bytes(M, K);
+}
+
+macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s, const uint8_t *w_codes,
+                          const uint8_t *w_scales, int64_t M, int64_t N, int64_t K, void *Y,
+                          int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(M));
+    MACAQ_TRY(check_rows(N));
+    if (M == 0 || N == 0) return MACAQ_OK;
+    if (!X || !inv_s || !w_codes || !w_scales || !Y || ldx < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < macaq_linear_workspace_bytes(M, K)) return MACAQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MACAQ_ERR_ALIGNMENT;
+    uint8_t *a_codes = static_cast<uint8_t *>(workspace);
+    uint8_t *a_scales = a_codes + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
+    MACAQ_TRY(macaq_quant_act(X, ldx, inv_s, M, K, a_codes, a_scales, stream));
+    return macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K, Y, ldy, stream);
+}
+
+macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *row_src,
+                                     const int32_t *expert_offsets, const float *inv_s,
+                                     int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
+                                     uint8_t *a_scales, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(rows));
+    if (E <= 0) return MACAQ_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
+    if (grouped_padded_rows(rows, E) > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (!expert_offsets || !inv_s || !a_codes || !a_scales) return MACAQ_ERR_INVALID_ARG;
+    if (rows > 0 && (!X || !row_src || ldx < K)) return MACAQ_ERR_INVALID_ARG;
+    if ((X && !aligned16(X)) || !aligned16(inv_s) || !aligned16(a_codes) || !aligned16(a_scales) ||
+        (X && ldx % 8 != 0))
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(X);
+    a.ld_src = ldx;
+    a.row_src = row_src;
+    a.offsets = expert_offsets;
+    a.f = inv_s;
+    a.K = K;
+    a.rows_valid = rows;
+    a.rows_out = grouped_padded_rows(rows, E);
+    a.E = static_cast<int32_t>(E);
+    a.codes = a_codes;
+    a.scales = a_scales;
+    return from_cuda(launch_quant(QuantMode::ActGrouped, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
+                                     const uint8_t *w_codes, const uint8_t *w_scales,
+                                     const int32_t *expert_offsets, int64_t rows, int64_t E,
+                                     int64_t N, int64_t K, void *Y, int64_t ldy,
+                                     macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(rows));
+    MACAQ_TRY(check_rows(N));
+    if (E <= 0) return MACAQ_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
+    if (grouped_padded_rows(rows, E) > kMaxDim || E * N > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (rows == 0 || N == 0) return MACAQ_OK;
+    if (!a_codes || !a_scales || !w_codes || !w_scales || !expert_offsets || !Y || ldy < N)
+        return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) ||
+        !aligned16(Y) || ldy % 8 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    GemmArgs g{};
+    g.a_codes = a_codes;
+    g.a_scales = a_scales;
+    g.w_codes = w_codes;
+    g.w_scales = w_scales;
+    g.offsets = expert_offsets;
+    g.M = rows;
+    g.a_rows = grouped_padded_rows(rows, E);
+    g.N = N;
+    g.K = K;
+    g.E = static_cast<int32_t>(E);
+    g.Y = Y;
+    g.ldy = ldy;
+    return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_check_device_error(macaq_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return MACAQ_ERR_CUDA;
+    unsigned flags = 0;
+    if (read_and_clear_device_error(&flags) != cudaSuccess) return MACAQ_ERR_CUDA;
+    return flags ? MACAQ_ERR_TIMEOUT : MACAQ_OK;
+}
+
+macaq_status macaq_set_wait_timeout_ns(uint64_t ns)
+{
+    return from_cuda(set_wait_timeout_ns(ns));
+}
+
+macaq_status macaq_debug_wait_probe(macaq_stream_t stream)
+{
+    return from_cuda(launch_wait_probe(static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_debug_e2m1(const float *t, int64_t n, uint8_t *codes, macaq_stream_t stream)
+{
+    if (n < 0) return MACAQ_ERR_INVALID_ARG;
+    if (n == 0) return MACAQ_OK;
+    if (!t || !codes) return MACAQ_ERR_INVALID_ARG;
+    return from_cuda(launch_debug_e2m1(t, n, codes, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,567 @@
+// Block-scaled MXFP4 x MXFP4 GEMM (dense and grouped-by-expert) on the
+// 5th-generation tensor cores of sm_103a.
+//
+// MACaQ runs its linear layers in W4A4 MXFP4 (page "Huawei MACaQ Is an
+// Open-Source Model Quantizer", section "MACaQ Backends": W4A4 is the default
+// inference mode; routed MoE experts run W4A4).  Y = A . Wq^T with both
+// operands E2M1 codes scaled per 32 elements by E8M0 powers of two.
+//
+// Kernel shape (persistent, one CTA per SM, 320 threads):
+//   warp 0      TMA producer: per 256-wide K stage, the A tile (128 rows x
+//               128 B), the B tile (BN rows x 128 B), both 128B-swizzled, and
+//               the scale tiles (512-byte atoms) by bulk copy, into a ring of
+//               STAGES shared-memory buffers guarded by mbarriers.
+//   warp 1      MMA issuer (one thread): copies the stage's scale atoms to
+//               tensor memory (tcgen05.cp 32x128b.warpx4) and issues four
+//               tcgen05.mma.kind::mxf4.block_scale (M=128, N=BN, K=64)
+//               accumulating in tensor memory; tcgen05.commit frees the stage.
+//   warps 2..9  epilogue: tcgen05.ld of the 128 x BN fp32 accumulator (each
+//               warp 32 lanes x 128 columns, all in registers), release of
+//               the accumulator, then bf16 rounding and TMA stores of
+//               32 x 16 boxes through a per-warp double buffer.
+// Every mbarrier wait is bounded in time; a wait that runs out sets a device
+// error flag and the CTA leaves in order (drains its copies and MMAs, frees
+// tensor memory).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace macaq {
+
+__device__ unsigned int g_error_flags;
+__device__ unsigned long long g_wait_ns = 4000000000ull;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK_BYTES = 128;  // 256 fp4 values per stage row
+constexpr int A_STAGE = BM * BK_BYTES;
+constexpr int SF_ATOM = 512;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int SF_TMEM_BASE = 256;
+constexpr int EPI_BUF = 32 * 32;  // 32 rows x 16 bf16
+
+constexpr unsigned kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u,
+                   kErrProbe = 16u;
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+template <int BN, int STAGES>
+struct Layout {
+    static constexpr int B_STAGE = BN * BK_BYTES;
+    static constexpr int SFA_STAGE = 2 * SF_ATOM;
+    static constexpr int SFB_STAGE = (BN / 128) * 2 * SF_ATOM;
+    static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // tensor-memory columns per stage
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
+    static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * 2 * EPI_BUF;
+    static constexpr int NUM_BARS = 2 * STAGES + 3;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_OFFS = OFF_MISC + 16;
+    static constexpr int BYTES = OFF_OFFS + 2 * (static_cast<int>(kMaxExperts) + 1) * 4;
+    static constexpr int ALLOC = BYTES + 1024;
+    static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
+    static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static_assert(BN <= SF_TMEM_BASE, "accumulator overlaps scale columns");
+};
+
+struct Params {
+    const uint8_t *sfa;
+    const uint8_t *sfb;
+    size_t sfb_expert_stride;
+    const int32_t *offsets;
+    uint16_t *Y;
+    int64_t ldy;
+    int32_t E;
+    int32_t M;
+    int32_t N;
+    int32_t num_kstages;
+    int32_t nka;
+    int32_t num_mb;
+    int32_t num_nb;
+    int32_t n_rb;
+};
+
+struct Tile {
+    int32_t a_row;      // row coordinate in the A code tensor (= scale row block * 128)
+    int32_t n0;
+    int32_t expert;
+    int32_t y_row0;     // first output row
+    int32_t rows_valid; // rows of this tile that exist in Y
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned code)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = *reinterpret_cast<volatile unsigned long long *>(&g_wait_ns);
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((i & 15u) == 0 && globaltimer() - t0 > limit) {
+            atomicOr(&g_error_flags, code);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_fixed(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0 && globaltimer() - t0 > kDrainNs) {
+            atomicOr(&g_error_flags, kErrDrain);
+            return false;
+        }
+    }
+}
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ void decode_tile(int64_t t, const Params &p, const int32_t *s_off,
+                                            const int32_t *s_pmb, Tile &ti)
+{
+    if (!GROUPED) {
+        const int32_t mb = static_cast<int32_t>(t % p.num_mb);
+        const int32_t nb = static_cast<int32_t>(t / p.num_mb);
+        ti.a_row = mb * BM;
+        ti.n0 = nb * BN;
+        ti.expert = 0;
+        ti.y_row0 = mb * BM;
+        ti.rows_valid = min(BM, p.M - mb * BM);
+    } else {
+        const int32_t total_mb = s_pmb[p.E];
+        const int32_t mb = static_cast<int32_t>(t % total_mb);
+        const int32_t nb = static_cast<int32_t>(t / total_mb);
+        int lo = 0, hi = p.E;  // s_pmb[lo] <= mb < s_pmb[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_pmb[mid] <= mb) lo = mid; else hi = mid;
+        }
+        // skip experts with no rows (equal prefix values)
+        while (lo + 1 <= p.E && s_pmb[lo + 1] <= mb) ++lo;
+        const int32_t j = mb - s_pmb[lo];
+        const int32_t cnt = s_off[lo + 1] - s_off[lo];
+        ti.a_row = mb * BM;
+        ti.n0 = nb * BN;
+        ti.expert = lo;
+        ti.y_row0 = s_off[lo] + j * BM;
+        ti.rows_valid = min(BM, cnt - j * BM);
+    }
+}
+
+template <int BN, int STAGES, bool GROUPED>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmY, const Params p)
+{
+    using L = Layout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1 KB alignment of the shared-window address (128B-swizzled tiles need it)
+    const uint32_t raw_base = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_base = sbase + L::OFF_BAR;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    const uint32_t acc_full = bar_base + 8u * (2 * STAGES);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t drain_bar = acc_full + 16u;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+    int32_t *s_off = reinterpret_cast<int32_t *>(smem + L::OFF_OFFS);
+    int32_t *s_pmb = s_off + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, NUM_EPI_WARPS);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (GROUPED) {
+        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t acc = 0;
+            s_pmb[0] = 0;
+            for (int e = 0; e < p.E; ++e) {
+                acc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+                s_pmb[e + 1] = acc;
+            }
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::OFF_MISC, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t total_tiles = GROUPED ? static_cast<int64_t>(s_pmb[p.E]) * p.num_nb
+                                        : static_cast<int64_t>(p.num_mb) * p.num_nb;
+    const int nks = p.num_kstages;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t it = 0;
+            uint32_t issued = 0;  // bit s: stage s has had a load issued
+            uint32_t last_parity = 0;
+            for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+                Tile ti;
+                decode_tile<BN, GROUPED>(t, p, s_off, s_pmb, ti);
+                const int32_t n_rb0 = ti.n0 / 128;
+                const int32_t sfb_valid = min(BN / 128, p.n_rb - n_rb0);
+                const uint8_t *sfb = p.sfb + static_cast<size_t>(ti.expert) * p.sfb_expert_stride;
+                const uint32_t bytes = A_STAGE + L::B_STAGE + L::SFA_STAGE + sfb_valid * 2 * SF_ATOM;
+                bool ok = true;
+                for (int ks = 0; ks < nks; ++ks, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(s);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    tma_load_2d(sbase + L::OFF_A + s * A_STAGE, &tmA, fb, ks * BK_BYTES, ti.a_row);
+                    if (GROUPED)
+                        tma_load_3d(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * BK_BYTES, ti.n0,
+                                    ti.expert);
+                    else
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * BK_BYTES, ti.n0);
+                    bulk_load(sbase + L::OFF_SFA + s * L::SFA_STAGE,
+                              p.sfa + (static_cast<size_t>(ti.a_row / BM) * p.nka + 2 * ks) * SF_ATOM,
+                              2 * SF_ATOM, fb);
+                    for (int r = 0; r < sfb_valid; ++r)
+                        bulk_load(sbase + L::OFF_SFB + s * L::SFB_STAGE + r * 2 * SF_ATOM,
+                                  sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + 2 * ks) * SF_ATOM,
+                                  2 * SF_ATOM, fb);
+                    issued |= 1u << s;
+                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
+                }
+                if (!ok) break;
+            }
+            // every issued copy must land before the CTA may leave
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s)) wait_fixed(full_bar(s), (last_parity >> s) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++tc) {
+                if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < nks; ++ks, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_TMEM_BASE + s * L::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + 8;
+                    const uint32_t sfa_s = sbase + L::OFF_SFA + s * L::SFA_STAGE;
+                    const uint32_t sfb_s = sbase + L::OFF_SFB + s * L::SFB_STAGE;
+#pragma unroll
+                    for (int at = 0; at < 2; ++at) {
+                        tc_cp_32x128b_warpx4(sfa_t + 4 * at,
+                                             smem_desc(sfa_s + at * SF_ATOM, 0, 128, kSwizzleNone));
+#pragma unroll
+                        for (int r = 0; r < BN / 128; ++r)
+                            tc_cp_32x128b_warpx4(
+                                sfb_t + at * 4 * (BN / 128) + 4 * r,
+                                smem_desc(sfb_s + r * 2 * SF_ATOM + at * SF_ATOM, 0, 128, kSwizzleNone));
+                    }
+                    const uint32_t a_s = sbase + L::OFF_A + s * A_STAGE;
+                    const uint32_t b_s = sbase + L::OFF_B + s * L::B_STAGE;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, kSwizzle128B);
+                        const uint32_t sf_id = (j & 1) * 2;
+                        tc_mma_mxf4(tmem, adesc, bdesc, idesc_mxf4(BM, BN, sf_id, sf_id),
+                                    sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
+                                    (ks > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                tc_commit(acc_full);
+            }
+            // all issued tensor-core work must finish before tensor memory is freed
+            tc_commit(drain_bar);
+            wait_fixed(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int q = warp & 3;     // tensor-memory lane quarter this warp may access
+        const int half = ew >> 2;   // which 128 accumulator columns
+        const uint32_t ebuf = sbase + L::OFF_EPI + ew * 2 * EPI_BUF;
+        uint32_t tc = 0, chunk = 0;
+        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tc) {
+            Tile ti;
+            decode_tile<BN, GROUPED>(t, p, s_off, s_pmb, ti);
+            if (!wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue)) break;
+            tc_fence_after();
+            uint32_t acc[4][32];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, acc[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+
+            const int row0 = 32 * q;  // first tile row of this warp
+            const bool any_row = row0 < ti.rows_valid;
+            const bool all_rows = row0 + 32 <= ti.rows_valid;
+            const bool use_tma = GROUPED ? all_rows : any_row;
+            const bool my_row = row0 + lane < ti.rows_valid;
+            if (!any_row) continue;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int32_t ncol = ti.n0 + half * 128 + 16 * c;
+                if (ncol >= p.N) break;
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
+                    const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                if (use_tma) {
+                    const uint32_t buf = ebuf + (chunk & 1u) * EPI_BUF;
+                    ++chunk;
+                    if (lane == 0) bulk_wait_read_le1();
+                    __syncwarp();
+                    const uint32_t sw = (lane >> 2) & 1;
+                    const uint32_t r0 = buf + lane * 32 + 16 * (0 ^ sw);
+                    const uint32_t r1 = buf + lane * 32 + 16 * (1 ^ sw);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r0), "r"(packed[0]),
+                                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r1), "r"(packed[4]),
+                                 "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
+                                 : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, buf, ncol, ti.y_row0 + row0);
+                        bulk_commit();
+                    }
+                } else if (my_row) {
+                    uint16_t *dst = p.Y + static_cast<int64_t>(ti.y_row0 + row0 + lane) * p.ldy + ncol;
+                    if (ncol + 16 <= p.N) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                        d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    } else {
+                        for (int i = 0; i < 16 && ncol + i < p.N; ++i)
+                            dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+__global__ void wait_probe_kernel()
+{
+    __shared__ alignas(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        wait_bounded(smem_u32(&bar), 0, &abort_flag, kErrProbe);
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base,
+            const uint64_t *dims, const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    uint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool attr_set[4] = {false, false, false, false};
+};
+DeviceInfo g_dev[64];
+std::mutex g_dev_mu;
+
+template <int BN, int STAGES, bool GROUPED>
+cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
+{
+    using L = Layout<BN, STAGES>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kern = gemm_mxf4_kernel<BN, STAGES, GROUPED>;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        DeviceInfo &di = g_dev[dev];
+        if (di.sms == 0) {
+            err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err != cudaSuccess) return err;
+        }
+        if (!di.attr_set[slot]) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+            if (err != cudaSuccess) return err;
+            di.attr_set[slot] = true;
+        }
+    }
+    const int sms = g_dev[dev].sms;
+
+    const uint64_t kb = static_cast<uint64_t>(g.K / 2);
+    CUtensorMap tmA, tmB, tmY;
+    {
+        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.a_rows)};
+        uint64_t strides[1] = {kb};
+        uint32_t box[2] = {BK_BYTES, BM};
+        if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    if (GROUPED) {
+        uint64_t dims[3] = {kb, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.E)};
+        uint64_t strides[2] = {kb, kb * static_cast<uint64_t>(g.N)};
+        uint32_t box[3] = {BK_BYTES, BN, 1};
+        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else {
+        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
+        uint64_t strides[1] = {kb};
+        uint32_t box[2] = {BK_BYTES, BN};
+        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.M)};
+        uint64_t strides[1] = {static_cast<uint64_t>(g.ldy) * 2};
+        uint32_t box[2] = {16, 32};
+        if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.Y, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_32B))
+            return cudaErrorInvalidValue;
+    }
+
+    Params p;
+    p.sfa = g.a_scales;
+    p.sfb = g.w_scales;
+    p.sfb_expert_stride = tiled_scale_bytes(g.N, g.K);
+    p.offsets = g.offsets;
+    p.Y = static_cast<uint16_t *>(g.Y);
+    p.ldy = g.ldy;
+    p.E = g.E;
+    p.M = static_cast<int32_t>(g.M);
+    p.N = static_cast<int32_t>(g.N);
+    p.num_kstages = static_cast<int32_t>((g.K + 255) / 256);
+    p.nka = static_cast<int32_t>(pad_scale_cols(g.K) / 4);
+    p.num_mb = static_cast<int32_t>((g.M + BM - 1) / BM);
+    p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
+    p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
+
+    int64_t max_tiles = GROUPED ? (g.a_rows / BM) * p.num_nb : static_cast<int64_t>(p.num_mb) * p.num_nb;
+    int64_t grid = max_tiles < sms ? max_tiles : sms;
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<unsigned>(grid), THREADS, L::ALLOC, stream>>>(tmA, tmB, tmY, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
+{
+    if (g.E > 0) return launch_impl<256, 4, true>(g, stream, 1);
+    return launch_impl<256, 4, false>(g, stream, 0);
+}
+
+cudaError_t read_and_clear_device_error(unsigned *flags)
+{
+    cudaError_t err = cudaMemcpyFromSymbol(flags, g_error_flags, sizeof(unsigned));
+    if (err != cudaSuccess) return err;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_error_flags, &zero, sizeof(unsigned));
+}
+
+cudaError_t set_wait_timeout_ns(uint64_t ns)
+{
+    const unsigned long long v = ns;
+    return cudaMemcpyToSymbol(g_wait_ns, &v, sizeof(v));
+}
+
+cudaError_t launch_wait_probe(cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
+}  // namespace macaq

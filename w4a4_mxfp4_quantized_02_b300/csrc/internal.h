@@ -1,0 +1,72 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "macaq.h"
+
+namespace macaq {
+
+constexpr int64_t kRowTile = 128;     // rows per scale tile / GEMM M tile
+constexpr int64_t kMaxExperts = 256;  // grouped kernels keep expert offsets in shared memory
+
+inline int64_t pad_rows(int64_t rows) { return (rows + kRowTile - 1) / kRowTile * kRowTile; }
+inline int64_t pad_scale_cols(int64_t K) { return (K / 32 + 7) / 8 * 8; }
+inline size_t tiled_scale_bytes(int64_t rows, int64_t K)
+{
+    return static_cast<size_t>(pad_rows(rows)) * static_cast<size_t>(pad_scale_cols(K));
+}
+inline int64_t grouped_padded_rows(int64_t rows, int64_t E)
+{
+    return pad_rows(rows + (kRowTile - 1) * E);
+}
+
+enum class QuantMode : int { Dense = 0, WeightGrouped = 1, ActGrouped = 2 };
+
+struct QuantArgs {
+    const uint16_t *src;      // bf16 bits
+    int64_t ld_src;           // row pitch of src in elements
+    const int32_t *row_src;   // ActGrouped: token row of each sorted row
+    const int32_t *offsets;   // ActGrouped: expert offsets [E+1]
+    const float *f;           // balance factors; group g uses f + g*K
+    int64_t K;
+    int64_t rows_valid;       // Dense: M; WeightGrouped: N per expert; ActGrouped: sorted rows
+    int64_t rows_out;         // output row positions to visit (padded space)
+    int64_t group_rows_pad;   // WeightGrouped: pad_rows(N)
+    int32_t E;
+    uint8_t *codes;
+    uint8_t *scales;
+    size_t scale_group_stride;  // WeightGrouped: tiled_scale_bytes(N, K)
+};
+
+cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream);
+
+cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_rows, int64_t mc,
+                           const uint16_t *w, int64_t n, int64_t k, float *s, float *inv_s,
+                           cudaStream_t stream);
+
+cudaError_t launch_debug_e2m1(const float *t, int64_t n, uint8_t *codes, cudaStream_t stream);
+
+struct GemmArgs {
+    const uint8_t *a_codes;
+    const uint8_t *a_scales;
+    const uint8_t *w_codes;
+    const uint8_t *w_scales;
+    const int32_t *offsets;  // grouped only
+    int64_t M;               // dense: rows of A; grouped: sorted rows (rows of Y)
+    int64_t a_rows;          // rows of the A code tensor (grouped: padded capacity)
+    int64_t N, K;
+    int32_t E;               // 0 = dense
+    void *Y;
+    int64_t ldy;
+};
+
+cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);
+
+cudaError_t read_and_clear_device_error(unsigned *flags);
+cudaError_t set_wait_timeout_ns(uint64_t ns);
+cudaError_t launch_wait_probe(cudaStream_t stream);
+
+}  // namespace macaq
