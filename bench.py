@@ -85,7 +85,9 @@ class ClockSampler:
         while not self._stop.is_set():
             try:
                 self.samples.append(n.nvmlDeviceGetClockInfo(self.h, n.NVML_CLOCK_SM))
-                r = n.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                fn = getattr(n, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    getattr(n, "nvmlDeviceGetCurrentClocksThrottleReasons")
+                r = fn(self.h)
                 for bit, name in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)

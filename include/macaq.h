@@ -203,6 +203,13 @@ macaq_status macaq_debug_wait_probe(macaq_stream_t stream);
 macaq_status macaq_debug_e2m1(const float *t, int64_t n, uint8_t *codes,
                               macaq_stream_t stream);
 
+/* Tensor-core rate probe: `ctas` CTAs (at most one per SM) each issue
+ * 4 * iters back-to-back block-scaled MXFP4 MMAs of shape 128 x bn x 64 on
+ * operands already in shared memory.  out (device uint64 [2 * ctas]) receives
+ * per CTA the elapsed SM cycles and nanoseconds.  16 <= bn <= 256, bn % 16 == 0. */
+macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, uint64_t *out,
+                                  macaq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

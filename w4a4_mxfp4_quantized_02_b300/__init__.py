@@ -60,6 +60,8 @@ _SIGS = {
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
     "macaq_debug_e2m1": ([_P, _I64, _P, _P], ctypes.c_int),
+    "macaq_debug_mma_rate": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P],
+                             ctypes.c_int),
 }
 
 _lib = None
@@ -261,3 +263,11 @@ def macaq_debug_e2m1(t: torch.Tensor, stream=None) -> torch.Tensor:
     _check("macaq_debug_e2m1", lib().macaq_debug_e2m1(_ptr(t), t.numel(), _ptr(out),
                                                        _stream(stream)))
     return out
+
+
+def macaq_debug_mma_rate(bn: int, iters: int, ctas: int, stream=None) -> torch.Tensor:
+    """Per-CTA (cycles, ns) of 4*iters back-to-back 128 x bn x 64 MXFP4 MMAs."""
+    out = torch.zeros(2 * ctas, dtype=torch.int64, device="cuda")
+    _check("macaq_debug_mma_rate", lib().macaq_debug_mma_rate(bn, iters, ctas, _ptr(out),
+                                                              _stream(stream)))
+    return out.view(ctas, 2)

@@ -276,6 +276,15 @@ macaq_status macaq_debug_wait_probe(macaq_stream_t stream)
     return from_cuda(launch_wait_probe(static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, uint64_t *out,
+                                  macaq_stream_t stream)
+{
+    if (bn < 16 || bn > 256 || bn % 16 != 0 || iters <= 0 || ctas <= 0 || !out)
+        return MACAQ_ERR_INVALID_ARG;
+    return from_cuda(launch_mma_rate(bn, iters, reinterpret_cast<unsigned long long *>(out), ctas,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 macaq_status macaq_debug_e2m1(const float *t, int64_t n, uint8_t *codes, macaq_stream_t stream)
 {
     if (n < 0) return MACAQ_ERR_INVALID_ARG;

@@ -104,19 +104,26 @@ struct Tile {
     int32_t rows_valid; // rows of this tile that exist in Y
 };
 
+// Wait for the phase of `bar` with parity `parity`.  The fast path only polls
+// (try_wait suspends the thread in hardware between polls); after 64 misses
+// the wait starts a clock and gives up after limit_ns, raising the CTA's
+// abort flag and the device error flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             unsigned code)
+                                             unsigned code, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t limit = *reinterpret_cast<volatile unsigned long long *>(&g_wait_ns);
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if ((i & 15u) == 0 && globaltimer() - t0 > limit) {
-            atomicOr(&g_error_flags, code);
-            *abort_flag = 1;
-            return false;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                atomicOr(&g_error_flags, code);
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
 }
@@ -191,6 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint64_t wait_ns = g_wait_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) {
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -280,12 +288,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0, tc = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++tc) {
-                if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma)) break;
+                if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma, wait_ns)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMma)) {
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMma, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tc) {
             Tile ti;
             decode_tile<BN, GROUPED>(t, p, s_off, s_pmb, ti);
-            if (!wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue)) break;
+            if (!wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
             tc_fence_after();
             uint32_t acc[4][32];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128;
@@ -416,7 +424,74 @@ __global__ void wait_probe_kernel()
         abort_flag = 0;
         mbar_init(smem_u32(&bar), 1);
         fence_mbar_init();
-        wait_bounded(smem_u32(&bar), 0, &abort_flag, kErrProbe);
+        wait_bounded(smem_u32(&bar), 0, &abort_flag, kErrProbe, g_wait_ns);
+    }
+}
+
+
+// Tensor-core rate probe: one CTA per SM issues `iters` x 4 back-to-back
+// kind::mxf4 block-scaled MMAs (M=128, N=bn, K=64) on operands resident in
+// shared memory and reports the elapsed SM cycles and nanoseconds.
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, unsigned long long *out)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    // A 16 KB | B 32 KB | SFA 1 KB | SFB 2 KB | barrier | tmem slot
+    const uint32_t a_s = sbase, b_s = sbase + 16384, sfa_s = sbase + 49152, sfb_s = sbase + 50176;
+    const uint32_t bar = sbase + 52224;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(smem + 52232);
+    for (int i = threadIdx.x; i < 52224 / 4; i += blockDim.x) {
+        const uint32_t x = static_cast<uint32_t>(i) * 2654435761u;
+        // codes: any byte is a finite E2M1 pair; scales: keep near 2^0
+        reinterpret_cast<uint32_t *>(smem)[i] = (i < 49152 / 4) ? x : 0x7f7f7f7fu;
+    }
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if ((threadIdx.x >> 5) == 0) {
+        tmem_alloc(sbase + 52232, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (threadIdx.x == 0) {
+        const uint32_t sfa_t = tmem + 256, sfb_t = tmem + 264;
+        for (int at = 0; at < 2; ++at) {
+            tc_cp_32x128b_warpx4(sfa_t + 4 * at, smem_desc(sfa_s + at * 512, 0, 128, kSwizzleNone));
+            for (int r = 0; r < 2; ++r)
+                tc_cp_32x128b_warpx4(sfb_t + at * 8 + 4 * r,
+                                     smem_desc(sfb_s + r * 1024 + at * 512, 0, 128, kSwizzleNone));
+        }
+        const int nsf = (bn + 127) / 128;
+        const long long c0 = clock64();
+        const uint64_t t0 = globaltimer();
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t sf_id = (j & 1) * 2;
+                tc_mma_mxf4(tmem, smem_desc(a_s + 32 * j, 16, 1024, kSwizzle128B),
+                            smem_desc(b_s + 32 * j, 16, 1024, kSwizzle128B),
+                            idesc_mxf4(BM, static_cast<uint32_t>(bn), sf_id, sf_id),
+                            sfa_t + 4 * (j >> 1), sfb_t + 4 * nsf * (j >> 1), (it | j) != 0 ? 1u : 0u);
+            }
+        }
+        tc_commit(bar);
+        wait_fixed(bar, 0);
+        const long long c1 = clock64();
+        const uint64_t t1 = globaltimer();
+        out[2 * blockIdx.x] = static_cast<unsigned long long>(c1 - c0);
+        out[2 * blockIdx.x + 1] = t1 - t0;
+    }
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -561,6 +636,15 @@ cudaError_t set_wait_timeout_ns(uint64_t ns)
 cudaError_t launch_wait_probe(cudaStream_t stream)
 {
     wait_probe_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, int ctas, cudaStream_t stream)
+{
+    const int smem = 52240 + 1024;
+    cudaError_t err = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    mma_rate_kernel<<<ctas, 128, smem, stream>>>(bn, iters, out);
     return cudaGetLastError();
 }
 

@@ -58,54 +58,178 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
 #endif
 }
 
+// Packed fp32x2 multiply / add / subtract, each lane rounded to nearest even.
+// The code generator fuses a packed multiply feeding a packed add into a
+// packed FMA (single rounding) even with an explicit .rn modifier and
+// -fmad=false, which would break bit-exactness.  So a packed multiply is only
+// ever used where no add consumes its result, and every product that feeds an
+// add is formed with scalar __fmul_rn.
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // One 32-element block: balance, butterflies (stride 1, 2, 4, 8, 16),
 // normalise, E8M0 scale, E2M1 codes.  raw: 16 words of bf16 pairs (element
-// 2i in the low half of word i).  Returns the scale byte.
-__device__ __forceinline__ uint32_t quant_block(const uint32_t (&raw)[16], const float (&f)[32],
+// 2i in the low half of word i); f[i] = (f_i, f_{i+16}).  Returns the scale
+// byte.
+//
+// Register layout: v[i] = (element i, element i + 16), so the stages at
+// strides 2, 4 and 8 pair whole float2 registers and run as packed fp32x2
+// adds (each lane rounded to nearest, exactly like two scalar adds); stride 1
+// (whose inputs are products) and stride 16 (which pairs the two halves of a
+// register) run as scalar adds.
+//
+// Scale and encode: the block maximum of |y| = |v * c| (c = fp32(1/sqrt 32))
+// equals RN(max|v| * c) because rounding is monotone, so one multiply gives
+// it.  The element to encode is RN(v * c) * 2^-se; when -124 <= se <= 122 it
+// equals RN(v * (c * 2^-se)) for every element that can get a non-zero code
+// (the constant c * 2^-se is exact and normal, products below the normal
+// range round to a zero code either way), so one packed multiply per pair
+// suffices.  Outside that range the two roundings are done separately.
+__device__ __forceinline__ uint32_t quant_block(const uint32_t (&raw)[16], const float2 (&f)[16],
                                                 uint4 &codes)
 {
-    float v[32];
+    float2 v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        v[2 * i] = __fmul_rn(bf16lo(raw[i]), f[2 * i]);
-        v[2 * i + 1] = __fmul_rn(bf16hi(raw[i]), f[2 * i + 1]);
+        const uint32_t w0 = raw[i >> 1];
+        const uint32_t w1 = raw[8 + (i >> 1)];
+        const float x0 = (i & 1) ? bf16hi(w0) : bf16lo(w0);
+        const float x1 = (i & 1) ? bf16hi(w1) : bf16lo(w1);
+        v[i] = make_float2(__fmul_rn(x0, f[i].x), __fmul_rn(x1, f[i].y));
+    }
+    // stride 1 in scalar form: its operands are products (see mul2_rn)
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float2 a = v[i];
+        const float2 b = v[i + 1];
+        v[i] = make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+        v[i + 1] = make_float2(__fsub_rn(a.x, b.x), __fsub_rn(a.y, b.y));
     }
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int h = 2; h < 16; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
             if (i & h) continue;
-            const float a = v[i];
-            const float b = v[i + h];
-            v[i] = __fadd_rn(a, b);
-            v[i + h] = __fsub_rn(a, b);
+            const float2 a = v[i];
+            const float2 b = v[i + h];
+            v[i] = add2_rn(a, b);
+            v[i + h] = sub2_rn(a, b);
         }
     }
-    float amax = 0.0f;
+    float vmax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        v[i] = __fmul_rn(v[i], kInvSqrt32);
-        amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 16; ++i) {
+        const float a = v[i].x;
+        const float b = v[i].y;
+        v[i].x = __fadd_rn(a, b);
+        v[i].y = __fsub_rn(a, b);
+        vmax = fmax3(fabsf(v[i].x), fabsf(v[i].y), vmax);
     }
+    const float amax = __fmul_rn(vmax, kInvSqrt32);
     // se = max(floor(log2 amax) - 2, -127) -> byte = max(exponent field - 2, 0)
     const int ef = static_cast<int>(__float_as_uint(amax) >> 23);
     const uint32_t sbyte = static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
-    // 2^-se = 2^(127 - se) biased = exponent field 254 - byte (always normal)
-    const float inv_scale = __uint_as_float((254u - sbyte) << 23);
+    const int se = static_cast<int>(sbyte) - 127;
+    if (se >= -124 && se <= 122) {
+        // c * 2^-se: exponent field of c (124) moved by -se
+        const float g = __int_as_float(__float_as_int(kInvSqrt32) - se * (1 << 23));
+        const float2 g2 = make_float2(g, g);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = mul2_rn(v[i], g2);
+    } else {
+        const float c = kInvSqrt32;
+        const float inv = __uint_as_float((254u - sbyte) << 23);  // 2^-se, normal
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = mul2_rn(v[i], make_float2(c, c));
+            v[i] = mul2_rn(v[i], make_float2(inv, inv));
+        }
+    }
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t word = 0;
+        uint32_t b[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int i = 8 * q + 2 * b;
-            const uint32_t byte = e2m1x2(__fmul_rn(v[i], inv_scale), __fmul_rn(v[i + 1], inv_scale));
-            word |= byte << (8 * b);
+        for (int k = 0; k < 4; ++k) {
+            const int j = 4 * q + k;  // output byte: elements 2j, 2j+1
+            const float lo = (j < 8) ? v[2 * j].x : v[2 * j - 16].y;
+            const float hi = (j < 8) ? v[2 * j + 1].x : v[2 * j - 15].y;
+            b[k] = e2m1x2(lo, hi);
         }
-        w[q] = word;
+        w[q] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
     }
     codes = make_uint4(w[0], w[1], w[2], w[3]);
     return sbyte;
+}
+
+// 64 bytes of one row's block: two 256-bit loads when 32-byte aligned,
+// otherwise four 128-bit loads.
+template <bool kWide>
+__device__ __forceinline__ void load_block(const uint16_t *src, uint32_t (&r)[16])
+{
+    if (kWide) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=r"(r[8 * h + 0]), "=r"(r[8 * h + 1]), "=r"(r[8 * h + 2]),
+                           "=r"(r[8 * h + 3]), "=r"(r[8 * h + 4]), "=r"(r[8 * h + 5]),
+                           "=r"(r[8 * h + 6]), "=r"(r[8 * h + 7])
+                         : "l"(src + 16 * h));
+        }
+    } else {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = __ldg(s4 + j);
+            r[4 * j + 0] = t.x;
+            r[4 * j + 1] = t.y;
+            r[4 * j + 2] = t.z;
+            r[4 * j + 3] = t.w;
+        }
+    }
 }
 
 struct RowRef {
@@ -167,9 +291,10 @@ __device__ __forceinline__ RowRef resolve_row(const QuantArgs &a, int64_t p, con
     return r;
 }
 
-template <QuantMode MODE>
+template <QuantMode MODE, bool kWide>
 __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_per_cta)
 {
+    constexpr int R = 2;  // rows per iteration (loads of all R rows in flight together)
     __shared__ int32_t s_off[kMaxExperts + 1];
     __shared__ int32_t s_poff[kMaxExperts + 1];
     if (MODE == QuantMode::ActGrouped) {
@@ -195,17 +320,17 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
     const int lane = threadIdx.x & 31;
     const bool writes_scale = (lane & 3) == 0 && kb < nkb_pad;
 
-    float f[32];
+    float2 f[16];
     int32_t cur_group = -1;
 
     const int64_t p_begin = static_cast<int64_t>(blockIdx.y) * rows_per_cta;
     const int64_t p_end = min(p_begin + rows_per_cta, a.rows_out);
 
-    for (int64_t p = p_begin; p < p_end; p += 2) {
-        RowRef rr[2];
-        uint32_t raw[2][16];
+    for (int64_t p = p_begin; p < p_end; p += R) {
+        RowRef rr[R];
+        uint32_t raw[R][16];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < R; ++u) {
             const int64_t pu = p + u;
             if (pu < p_end) {
                 rr[u] = resolve_row<MODE>(a, pu, s_off, s_poff);
@@ -217,36 +342,31 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
                 rr[u].group = cur_group;
             }
             if (rr[u].src != nullptr && has_kb) {
-                const uint4 *s4 = reinterpret_cast<const uint4 *>(rr[u].src + 32 * kb);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 t = __ldg(s4 + j);
-                    raw[u][4 * j + 0] = t.x;
-                    raw[u][4 * j + 1] = t.y;
-                    raw[u][4 * j + 2] = t.z;
-                    raw[u][4 * j + 3] = t.w;
-                }
+                load_block<kWide>(rr[u].src + 32 * kb, raw[u]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) raw[u][j] = 0u;
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < R; ++u) {
             if (p + u >= p_end) break;  // uniform across the CTA
             const bool valid = rr[u].src != nullptr;
             if (valid && rr[u].group != cur_group) {
                 cur_group = rr[u].group;
                 if (has_kb) {
                     const float4 *f4 = reinterpret_cast<const float4 *>(a.f + cur_group * a.K + 32 * kb);
+                    float ff[32];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float4 t = __ldg(f4 + j);
-                        f[4 * j + 0] = t.x;
-                        f[4 * j + 1] = t.y;
-                        f[4 * j + 2] = t.z;
-                        f[4 * j + 3] = t.w;
+                        ff[4 * j + 0] = t.x;
+                        ff[4 * j + 1] = t.y;
+                        ff[4 * j + 2] = t.z;
+                        ff[4 * j + 3] = t.w;
                     }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) f[i] = make_float2(ff[i], ff[i + 16]);
                 }
             }
             uint32_t sbyte = 0;
@@ -363,17 +483,24 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
     dim3 grid(static_cast<unsigned>(slabs),
               static_cast<unsigned>((a.rows_out + rows_per_cta - 1) / rows_per_cta));
     dim3 block(static_cast<unsigned>(best_t));
+    const bool wide = (reinterpret_cast<uintptr_t>(a.src) % 32 == 0) && ((a.ld_src * 2) % 32 == 0);
+#define MACAQ_LAUNCH_QUANT(M)                                                              \
+    if (wide)                                                                              \
+        quant_kernel<M, true><<<grid, block, 0, stream>>>(a, rows_per_cta);                \
+    else                                                                                   \
+        quant_kernel<M, false><<<grid, block, 0, stream>>>(a, rows_per_cta);
     switch (mode) {
     case QuantMode::Dense:
-        quant_kernel<QuantMode::Dense><<<grid, block, 0, stream>>>(a, rows_per_cta);
+        MACAQ_LAUNCH_QUANT(QuantMode::Dense)
         break;
     case QuantMode::WeightGrouped:
-        quant_kernel<QuantMode::WeightGrouped><<<grid, block, 0, stream>>>(a, rows_per_cta);
+        MACAQ_LAUNCH_QUANT(QuantMode::WeightGrouped)
         break;
     case QuantMode::ActGrouped:
-        quant_kernel<QuantMode::ActGrouped><<<grid, block, 0, stream>>>(a, rows_per_cta);
+        MACAQ_LAUNCH_QUANT(QuantMode::ActGrouped)
         break;
     }
+#undef MACAQ_LAUNCH_QUANT
     return cudaGetLastError();
 }
 
