@@ -52,8 +52,44 @@ def load_peaks():
             "source": "fallback"}
 
 
+class _NvmlCtypes:
+    """Minimal NVML binding through ctypes (the driver's libnvidia-ml)."""
+
+    def __init__(self, bus_id):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(0), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError("no NVML device handle")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c))  # NVML_CLOCK_SM
+        return c.value
+
+    def max_sm_clock(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(c))
+        return c.value
+
+    def reasons(self):
+        r = self.ct.c_ulonglong()
+        self._reasons(self.h, self.ct.byref(r))
+        return r.value
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples SM clock and clock-event (throttle) reasons through NVML while running."""
 
     REASONS = {
         0x0000000000000001: "gpu_idle", 0x0000000000000002: "applications_clocks_setting",
@@ -63,31 +99,26 @@ class ClockSampler:
         0x0000000000000100: "display_clock_setting",
     }
 
-    def __init__(self, index: int, period_s: float = 0.002):
+    def __init__(self, bus_id: str | None, period_s: float = 0.001):
         self.samples = []
         self.reasons = set()
         self.period = period_s
         self.ok = False
+        self.err = ""
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nvml = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _NvmlCtypes(bus_id)
+            self.max_mhz = self.nv.max_sm_clock()
             self.ok = True
-        except Exception as e:  # noqa: BLE001 - clocks are reported as unavailable
+        except Exception as e:  # noqa: BLE001 - clocks are then reported as unavailable
             self.err = str(e)
         self._stop = threading.Event()
         self._t = None
 
     def _run(self):
-        n = self.nvml
         while not self._stop.is_set():
             try:
-                self.samples.append(n.nvmlDeviceGetClockInfo(self.h, n.NVML_CLOCK_SM))
-                fn = getattr(n, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                    getattr(n, "nvmlDeviceGetCurrentClocksThrottleReasons")
-                r = fn(self.h)
+                self.samples.append(self.nv.sm_clock())
+                r = self.nv.reasons()
                 for bit, name in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)
@@ -112,6 +143,15 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
                 "samples": len(self.samples)}
+
+
+def pci_bus_id(dev) -> str | None:
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:  # noqa: BLE001
+        return None
 
 
 # ----------------------------------------------------------------- oracle leg
@@ -271,7 +311,7 @@ def gpu_arm(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler = ClockSampler(pci_bus_id(dev))
     with sampler:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)

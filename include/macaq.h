@@ -206,9 +206,15 @@ macaq_status macaq_debug_e2m1(const float *t, int64_t n, uint8_t *codes,
 /* Tensor-core rate probe: `ctas` CTAs (at most one per SM) each issue
  * 4 * iters back-to-back block-scaled MXFP4 MMAs of shape 128 x bn x 64 on
  * operands already in shared memory.  out (device uint64 [2 * ctas]) receives
- * per CTA the elapsed SM cycles and nanoseconds.  16 <= bn <= 256, bn % 16 == 0. */
-macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, uint64_t *out,
-                                  macaq_stream_t stream);
+ * per CTA the elapsed SM cycles and nanoseconds.  Low 16 bits of bn: N (16 <= N <= 256,
+ * N % 16 == 0); bits 16 and up: 0 = MMAs only, 1 = also the six scale-factor
+ * copies a 256-wide K stage needs before its four MMAs, 2 = also one
+ * tcgen05.commit per stage, 3 = MMAs while another thread streams 16 KB bulk
+ * copies from `src` (device, >= 1 MiB, 16-byte aligned) into shared memory;
+ * out then has 3 * ctas entries, the last ctas being bytes copied per CTA.
+ * src may be NULL for modes 0..2. */
+macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, const void *src,
+                                  uint64_t *out, macaq_stream_t stream);
 
 #ifdef __cplusplus
 }

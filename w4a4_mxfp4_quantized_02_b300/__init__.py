@@ -60,7 +60,7 @@ _SIGS = {
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
     "macaq_debug_e2m1": ([_P, _I64, _P, _P], ctypes.c_int),
-    "macaq_debug_mma_rate": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P],
+    "macaq_debug_mma_rate": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P, _P],
                              ctypes.c_int),
 }
 
@@ -265,9 +265,10 @@ def macaq_debug_e2m1(t: torch.Tensor, stream=None) -> torch.Tensor:
     return out
 
 
-def macaq_debug_mma_rate(bn: int, iters: int, ctas: int, stream=None) -> torch.Tensor:
-    """Per-CTA (cycles, ns) of 4*iters back-to-back 128 x bn x 64 MXFP4 MMAs."""
-    out = torch.zeros(2 * ctas, dtype=torch.int64, device="cuda")
-    _check("macaq_debug_mma_rate", lib().macaq_debug_mma_rate(bn, iters, ctas, _ptr(out),
-                                                              _stream(stream)))
-    return out.view(ctas, 2)
+def macaq_debug_mma_rate(bn: int, iters: int, ctas: int, src=None, stream=None) -> torch.Tensor:
+    """Per-CTA (cycles, ns[, bytes loaded]) of 4*iters back-to-back 128 x N x 64 MXFP4 MMAs
+    (bn = N | mode << 16, see the header)."""
+    out = torch.zeros(3 * ctas, dtype=torch.int64, device="cuda")
+    _check("macaq_debug_mma_rate", lib().macaq_debug_mma_rate(bn, iters, ctas, _ptr(src),
+                                                              _ptr(out), _stream(stream)))
+    return out

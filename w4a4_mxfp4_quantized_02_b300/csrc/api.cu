@@ -276,12 +276,15 @@ macaq_status macaq_debug_wait_probe(macaq_stream_t stream)
     return from_cuda(launch_wait_probe(static_cast<cudaStream_t>(stream)));
 }
 
-macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, uint64_t *out,
-                                  macaq_stream_t stream)
+macaq_status macaq_debug_mma_rate(int32_t bn, int32_t iters, int32_t ctas, const void *src,
+                                  uint64_t *out, macaq_stream_t stream)
 {
-    if (bn < 16 || bn > 256 || bn % 16 != 0 || iters <= 0 || ctas <= 0 || !out)
+    const int32_t n = bn & 0xffff, mode = bn >> 16;
+    if (n < 16 || n > 256 || n % 16 != 0 || mode < 0 || mode > 3 || iters <= 0 || ctas <= 0 || !out)
         return MACAQ_ERR_INVALID_ARG;
-    return from_cuda(launch_mma_rate(bn, iters, reinterpret_cast<unsigned long long *>(out), ctas,
+    if (mode == 3 && (!src || !aligned16(src))) return MACAQ_ERR_INVALID_ARG;
+    return from_cuda(launch_mma_rate(bn, iters, reinterpret_cast<unsigned long long *>(out),
+                                     static_cast<const uint8_t *>(src), ctas,
                                      static_cast<cudaStream_t>(stream)));
 }
 

@@ -34,6 +34,11 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#ifndef MACAQ_TRACE
+#define MACAQ_TRACE(slot, idx)
+#define MACAQ_TRACE_EDGE(which)
+#endif
+
 namespace macaq {
 
 __device__ unsigned int g_error_flags;
@@ -44,11 +49,10 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;
-constexpr int BK_BYTES = 128;  // 256 fp4 values per stage row
-constexpr int A_STAGE = BM * BK_BYTES;
 constexpr int SF_ATOM = 512;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int EPI_WARP0 = 3;  // warps 0..2: TMA producer, MMA issuer, scale copier
+constexpr int THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_TMEM_BASE = 256;
 constexpr int EPI_BUF = 32 * 32;  // 32 rows x 16 bf16
@@ -56,20 +60,30 @@ constexpr int EPI_BUF = 32 * 32;  // 32 rows x 16 bf16
 constexpr unsigned kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u,
                    kErrProbe = 16u;
 constexpr uint64_t kDrainNs = 2000000000ull;
+constexpr uint32_t kPollHintNs = 20000;  // longest hardware sleep per poll
 
-template <int BN, int STAGES>
+// Shared-memory plan of one CTA.  KB = bytes of each operand row per
+// pipeline stage (128: 256 fp4 values, 128-byte swizzle; 64: 128 values,
+// 64-byte swizzle); one stage holds KB/64 scale atoms per 128 rows.
+template <int BN, int STAGES, int KB>
 struct Layout {
-    static constexpr int B_STAGE = BN * BK_BYTES;
-    static constexpr int SFA_STAGE = 2 * SF_ATOM;
-    static constexpr int SFB_STAGE = (BN / 128) * 2 * SF_ATOM;
-    static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // tensor-memory columns per stage
+    static_assert(KB == 64 || KB == 128, "stage rows are 64 or 128 bytes");
+    static constexpr int KATOMS = KB / 64;     // 4-scale atoms (128 values) per stage
+    static constexpr int KSTEPS = KB / 32;     // MMAs (K = 64 values) per stage
+    static constexpr int A_STAGE = BM * KB;
+    static constexpr int B_STAGE = BN * KB;
+    static constexpr int SFA_STAGE = KATOMS * SF_ATOM;
+    static constexpr int SFB_STAGE = (BN / 128) * KATOMS * SF_ATOM;
+    static constexpr int SF_COLS = 4 * KATOMS + 4 * KATOMS * (BN / 128);  // tensor-memory columns per stage
+    static constexpr uint32_t SWZ_DESC = KB == 128 ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t SWZ_SBO = 8 * KB;  // bytes between 8-row groups
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
     static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * 2 * EPI_BUF;
-    static constexpr int NUM_BARS = 2 * STAGES + 3;
+    static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_OFFS = OFF_MISC + 16;
     static constexpr int BYTES = OFF_OFFS + 2 * (static_cast<int>(kMaxExperts) + 1) * 4;
@@ -77,6 +91,7 @@ struct Layout {
     static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
     static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
     static_assert(BN <= SF_TMEM_BASE, "accumulator overlaps scale columns");
+    static_assert(ALLOC <= 232448, "shared memory");
 };
 
 struct Params {
@@ -104,66 +119,77 @@ struct Tile {
     int32_t rows_valid; // rows of this tile that exist in Y
 };
 
-// Wait for the phase of `bar` with parity `parity`.  The fast path only polls
-// (try_wait suspends the thread in hardware between polls); after 64 misses
-// the wait starts a clock and gives up after limit_ns, raising the CTA's
-// abort flag and the device error flag.
+// Wait for the phase of `bar` with parity `parity`.  Each poll lets the
+// thread sleep in hardware until the phase completes (up to a short hint), so
+// waiting threads do not compete with the tensor cores for shared memory.
+// The clock starts after the first miss; past limit_ns the wait gives up,
+// raising the CTA's abort flag and the device error flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              unsigned code, uint64_t limit_ns)
 {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, kPollHintNs)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                atomicOr(&g_error_flags, code);
-                *abort_flag = 1;
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait(bar, parity, kPollHintNs)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            atomicOr(&g_error_flags, code);
+            *abort_flag = 1;
+            return false;
         }
     }
 }
 
+// The same wait taken by lane 0 of a warp on behalf of the whole warp.
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag, unsigned code,
+                                                  uint64_t limit_ns)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, code, limit_ns) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ bool wait_fixed(uint32_t bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, kPollHintNs)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0 && globaltimer() - t0 > kDrainNs) {
+    for (;;) {
+        if (mbar_try_wait(bar, parity, kPollHintNs)) return true;
+        if (globaltimer() - t0 > kDrainNs) {
             atomicOr(&g_error_flags, kErrDrain);
             return false;
         }
     }
 }
 
-template <int BN, bool GROUPED>
-__device__ __forceinline__ void decode_tile(int64_t t, const Params &p, const int32_t *s_off,
-                                            const int32_t *s_pmb, Tile &ti)
+// Work unit u -> the tile of this CTA.  Dense: units run over (m-group, n)
+// with m fastest; a cluster of CLUSTER CTAs takes one unit and CTA rank r
+// computes m-block CLUSTER*mg + r (the CTAs share the B tile).  Grouped: one
+// CTA per unit over (padded m-block, n), m fastest.
+template <int BN, int CLUSTER, bool GROUPED>
+__device__ __forceinline__ void decode_tile(int64_t u, uint32_t rank, const Params &p,
+                                            const int32_t *s_off, const int32_t *s_pmb, Tile &ti)
 {
     if (!GROUPED) {
-        const int32_t mb = static_cast<int32_t>(t % p.num_mb);
-        const int32_t nb = static_cast<int32_t>(t / p.num_mb);
+        const int32_t num_mg = (p.num_mb + CLUSTER - 1) / CLUSTER;
+        const int32_t mg = static_cast<int32_t>(u % num_mg);
+        const int32_t nb = static_cast<int32_t>(u / num_mg);
+        const int32_t mb = mg * CLUSTER + static_cast<int32_t>(rank);
         ti.a_row = mb * BM;
         ti.n0 = nb * BN;
         ti.expert = 0;
         ti.y_row0 = mb * BM;
-        ti.rows_valid = min(BM, p.M - mb * BM);
+        ti.rows_valid = min(BM, p.M - mb * BM);  // <= 0 for an m-block past the end
     } else {
         const int32_t total_mb = s_pmb[p.E];
-        const int32_t mb = static_cast<int32_t>(t % total_mb);
-        const int32_t nb = static_cast<int32_t>(t / total_mb);
+        const int32_t mb = static_cast<int32_t>(u % total_mb);
+        const int32_t nb = static_cast<int32_t>(u / total_mb);
         int lo = 0, hi = p.E;  // s_pmb[lo] <= mb < s_pmb[hi]
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (s_pmb[mid] <= mb) lo = mid; else hi = mid;
         }
-        // skip experts with no rows (equal prefix values)
-        while (lo + 1 <= p.E && s_pmb[lo + 1] <= mb) ++lo;
         const int32_t j = mb - s_pmb[lo];
         const int32_t cnt = s_off[lo + 1] - s_off[lo];
         ti.a_row = mb * BM;
@@ -174,12 +200,16 @@ __device__ __forceinline__ void decode_tile(int64_t t, const Params &p, const in
     }
 }
 
-template <int BN, int STAGES, bool GROUPED>
+template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const Params p)
 {
-    using L = Layout<BN, STAGES>;
+    static_assert(CLUSTER == 1 || (CLUSTER == 2 && !GROUPED), "clusters pair dense m-blocks");
+    using L = Layout<BN, STAGES, KB>;
+    constexpr int A_STAGE = L::A_STAGE;
+    constexpr int B_PART = L::B_STAGE / CLUSTER;  // bytes of B each CTA loads per stage
+    constexpr uint16_t kAll = (1u << CLUSTER) - 1u;
     extern __shared__ uint8_t smem_raw[];
     // 1 KB alignment of the shared-window address (128B-swizzled tiles need it)
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -188,9 +218,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_base = sbase + L::OFF_BAR;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-    const uint32_t acc_full = bar_base + 8u * (2 * STAGES);
+    auto ready_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };  // scales in TMEM
+    const uint32_t acc_full = bar_base + 8u * (3 * STAGES);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t drain_bar = acc_full + 16u;
+    const uint32_t drain_bar2 = acc_full + 24u;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
     int32_t *s_off = reinterpret_cast<int32_t *>(smem + L::OFF_OFFS);
@@ -198,16 +230,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    MACAQ_TRACE_EDGE(0);
     const uint64_t wait_ns = g_wait_ns;
+    const uint32_t rank = (CLUSTER > 1) ? cluster_ctarank() : 0u;
+    const int64_t first_unit = blockIdx.x / CLUSTER;
+    const int64_t unit_stride = gridDim.x / CLUSTER;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CLUSTER);  // one MMA commit from every CTA of the cluster
+            mbar_init(ready_bar(s), 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, NUM_EPI_WARPS);
         mbar_init(drain_bar, 1);
+        mbar_init(drain_bar2, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -228,13 +266,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // peers may signal our barriers only once they are initialised
+    if (CLUSTER > 1) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int64_t total_tiles = GROUPED ? static_cast<int64_t>(s_pmb[p.E]) * p.num_nb
-                                        : static_cast<int64_t>(p.num_mb) * p.num_nb;
+    const int64_t total_units =
+        GROUPED ? static_cast<int64_t>(s_pmb[p.E]) * p.num_nb
+                : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
     const int nks = p.num_kstages;
+    const int64_t my_units =
+        first_unit < total_units ? (total_units - 1 - first_unit) / unit_stride + 1 : 0;
+    const uint32_t total_stages = static_cast<uint32_t>(my_units) * static_cast<uint32_t>(nks);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -242,108 +285,198 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t it = 0;
             uint32_t issued = 0;  // bit s: stage s has had a load issued
             uint32_t last_parity = 0;
-            for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+            for (int64_t u = first_unit; u < total_units; u += unit_stride) {
                 Tile ti;
-                decode_tile<BN, GROUPED>(t, p, s_off, s_pmb, ti);
+                decode_tile<BN, CLUSTER, GROUPED>(u, rank, p, s_off, s_pmb, ti);
                 const int32_t n_rb0 = ti.n0 / 128;
                 const int32_t sfb_valid = min(BN / 128, p.n_rb - n_rb0);
+                const bool a_valid = ti.rows_valid > 0;
                 const uint8_t *sfb = p.sfb + static_cast<size_t>(ti.expert) * p.sfb_expert_stride;
-                const uint32_t bytes = A_STAGE + L::B_STAGE + L::SFA_STAGE + sfb_valid * 2 * SF_ATOM;
+                const uint32_t bytes = A_STAGE + L::B_STAGE + (a_valid ? L::SFA_STAGE : 0) +
+                                       sfb_valid * L::KATOMS * SF_ATOM;
                 bool ok = true;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
+                    MACAQ_TRACE(0, it);
                     if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer, wait_ns)) {
                         ok = false;
                         break;
                     }
+                    MACAQ_TRACE(1, it);
                     const uint32_t fb = full_bar(s);
                     mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(sbase + L::OFF_A + s * A_STAGE, &tmA, fb, ks * BK_BYTES, ti.a_row);
-                    if (GROUPED)
-                        tma_load_3d(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * BK_BYTES, ti.n0,
-                                    ti.expert);
-                    else
-                        tma_load_2d(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * BK_BYTES, ti.n0);
-                    bulk_load(sbase + L::OFF_SFA + s * L::SFA_STAGE,
-                              p.sfa + (static_cast<size_t>(ti.a_row / BM) * p.nka + 2 * ks) * SF_ATOM,
-                              2 * SF_ATOM, fb);
-                    for (int r = 0; r < sfb_valid; ++r)
-                        bulk_load(sbase + L::OFF_SFB + s * L::SFB_STAGE + r * 2 * SF_ATOM,
-                                  sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + 2 * ks) * SF_ATOM,
-                                  2 * SF_ATOM, fb);
+                    tma_load_2d(sbase + L::OFF_A + s * A_STAGE, &tmA, fb, ks * KB, ti.a_row);
+                    const uint32_t b_dst = sbase + L::OFF_B + s * L::B_STAGE;
+                    if (GROUPED) {
+                        tma_load_3d(b_dst, &tmB, fb, ks * KB, ti.n0, ti.expert);
+                    } else if (CLUSTER == 1) {
+                        tma_load_2d(b_dst, &tmB, fb, ks * KB, ti.n0);
+                    } else {
+                        // this CTA's share of the B tile, delivered to every CTA of the cluster
+                        tma_load_2d_mc(b_dst + rank * B_PART, &tmB, fb, ks * KB,
+                                       ti.n0 + static_cast<int32_t>(rank) * (BN / CLUSTER), kAll);
+                    }
+                    if (a_valid)
+                        bulk_load(sbase + L::OFF_SFA + s * L::SFA_STAGE,
+                                  p.sfa + (static_cast<size_t>(ti.a_row / BM) * p.nka + L::KATOMS * ks) * SF_ATOM,
+                                  L::SFA_STAGE, fb);
+                    const uint32_t sfb_dst = sbase + L::OFF_SFB + s * L::SFB_STAGE;
+                    if (CLUSTER == 1) {
+                        for (int r = 0; r < sfb_valid; ++r)
+                            bulk_load(sfb_dst + r * L::KATOMS * SF_ATOM,
+                                      sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + L::KATOMS * ks) * SF_ATOM,
+                                      L::KATOMS * SF_ATOM, fb);
+                    } else {
+                        // row atoms of B's scales are split over the cluster the same way
+                        for (int r = static_cast<int>(rank); r < sfb_valid; r += CLUSTER)
+                            bulk_load_mc(sfb_dst + r * L::KATOMS * SF_ATOM,
+                                         sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + L::KATOMS * ks) * SF_ATOM,
+                                         L::KATOMS * SF_ATOM, fb, kAll);
+                    }
                     issued |= 1u << s;
                     last_parity = (last_parity & ~(1u << s)) | (ph << s);
                 }
                 if (!ok) break;
             }
-            // every issued copy must land before the CTA may leave
-            for (int s = 0; s < STAGES; ++s)
-                if (issued & (1u << s)) wait_fixed(full_bar(s), (last_parity >> s) & 1u);
+            // every copy issued into this CTA must land, and every consumer of
+            // each stage (in every CTA of the cluster) must have released it,
+            // before the CTA may leave
+            for (int s = 0; s < STAGES; ++s) {
+                if (issued & (1u << s)) {
+                    wait_fixed(full_bar(s), (last_parity >> s) & 1u);
+                    wait_fixed(empty_bar(s), (last_parity >> s) & 1u);
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            uint32_t it = 0, tc = 0;
+            // Waits only on "scales ready" (which implies the stage's data has
+            // landed) and the accumulator; issues MMAs and commits.  The scale
+            // copies live in their own warp: a barrier wait issued after
+            // tcgen05.cp in the same thread waits for the copies, which
+            // drains the tensor pipe every stage.  Descriptors are
+            // precomputed and advanced by adds (one thread: its own
+            // instruction latency is on the critical path).
+            const uint64_t a_desc0 = smem_desc(sbase + L::OFF_A, 16, L::SWZ_SBO, L::SWZ_DESC);
+            const uint64_t b_desc0 = smem_desc(sbase + L::OFF_B, 16, L::SWZ_SBO, L::SWZ_DESC);
+            const uint32_t idesc0 = idesc_mxf4(BM, BN, 0, 0);
+            const uint32_t idesc2 = idesc_mxf4(BM, BN, 2, 2);
+            const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
+            constexpr uint32_t kAStep = A_STAGE >> 4, kBStep = L::B_STAGE >> 4;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++tc) {
-                if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma, wait_ns)) break;
-                tc_fence_after();
-                for (int ks = 0; ks < nks; ++ks, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMma, wait_ns)) {
+            uint32_t tc = 0, st = 0, ph = 0;
+            int ks = 0;
+            for (uint32_t it = 0; it < total_stages; ++it) {
+                MACAQ_TRACE(2, it);
+                if (!wait_bounded(ready_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                MACAQ_TRACE(3, it);
+                if (ks == 0) {
+                    // the epilogue must have drained the accumulator of the previous tile
+                    MACAQ_TRACE(4, tc);
+                    if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma, wait_ns)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem + SF_TMEM_BASE + s * L::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + 8;
-                    const uint32_t sfa_s = sbase + L::OFF_SFA + s * L::SFA_STAGE;
-                    const uint32_t sfb_s = sbase + L::OFF_SFB + s * L::SFB_STAGE;
-#pragma unroll
-                    for (int at = 0; at < 2; ++at) {
-                        tc_cp_32x128b_warpx4(sfa_t + 4 * at,
-                                             smem_desc(sfa_s + at * SF_ATOM, 0, 128, kSwizzleNone));
-#pragma unroll
-                        for (int r = 0; r < BN / 128; ++r)
-                            tc_cp_32x128b_warpx4(
-                                sfb_t + at * 4 * (BN / 128) + 4 * r,
-                                smem_desc(sfb_s + r * 2 * SF_ATOM + at * SF_ATOM, 0, 128, kSwizzleNone));
-                    }
-                    const uint32_t a_s = sbase + L::OFF_A + s * A_STAGE;
-                    const uint32_t b_s = sbase + L::OFF_B + s * L::B_STAGE;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, kSwizzle128B);
-                        const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, kSwizzle128B);
-                        const uint32_t sf_id = (j & 1) * 2;
-                        tc_mma_mxf4(tmem, adesc, bdesc, idesc_mxf4(BM, BN, sf_id, sf_id),
-                                    sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
-                                    (ks > 0 || j > 0) ? 1u : 0u);
-                    }
-                    tc_commit(empty_bar(s));
+                    MACAQ_TRACE(5, tc);
                 }
-                if (!ok) break;
-                tc_commit(acc_full);
+                // order these MMAs after the copies / TMEM reads other threads
+                // completed before the barriers above
+                tc_fence_after();
+                const uint32_t sfa_t = sf_t0 + st * L::SF_COLS;
+                const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
+                const uint64_t ad = a_desc0 + st * kAStep;
+                const uint64_t bd = b_desc0 + st * kBStep;
+#pragma unroll
+                for (int j = 0; j < L::KSTEPS; ++j) {
+                    // k step j: 32 bytes further along the swizzled rows; two
+                    // k steps share one scale atom (bytes 0-1, then 2-3)
+                    tc_mma_mxf4(tmem, ad + 2 * j, bd + 2 * j, (j & 1) ? idesc2 : idesc0,
+                                sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
+                                (ks > 0 || j > 0) ? 1u : 0u);
+                }
+                // the stage's buffers may be refilled (in every CTA that shares them)
+                // once these MMAs have read them
+                if (CLUSTER == 1) tc_commit(empty_bar(static_cast<int>(st)));
+                else tc_commit_mc(empty_bar(static_cast<int>(st)), kAll);
+                if (++ks == nks) {
+                    ks = 0;
+                    tc_commit(acc_full);
+                    ++tc;
+                }
+                if (++st == STAGES) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
+            (void)ok;
             // all issued tensor-core work must finish before tensor memory is freed
             tc_commit(drain_bar);
             wait_fixed(drain_bar, 0);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ------------------------------------------------ scale copier
+            // For each stage: wait for its data, copy its scale atoms from
+            // shared memory into the stage's tensor-memory slot, commit to
+            // "scales ready".  Slot reuse is safe: stage it's data (and so
+            // this wait) only arrives after the MMAs of stage it-STAGES have
+            // released the slot.
+            const uint64_t sfa_desc0 = smem_desc(sbase + L::OFF_SFA, 0, 128, kSwizzleNone);
+            const uint64_t sfb_desc0 = smem_desc(sbase + L::OFF_SFB, 0, 128, kSwizzleNone);
+            const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
+            constexpr uint32_t kSfaStep = L::SFA_STAGE >> 4, kSfbStep = L::SFB_STAGE >> 4;
+            constexpr uint32_t kAtom = SF_ATOM >> 4;
+            uint32_t st = 0, ph = 0;
+            for (uint32_t it = 0; it < total_stages; ++it) {
+                MACAQ_TRACE(9, it);
+                if (!wait_bounded(full_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) break;
+                MACAQ_TRACE(10, it);
+                const uint32_t sfa_t = sf_t0 + st * L::SF_COLS;
+                const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
+                const uint64_t da = sfa_desc0 + st * kSfaStep;
+                const uint64_t db = sfb_desc0 + st * kSfbStep;
+                // TMEM: atom `at` of A at column 4*at; atom `at` of B row block
+                // r at 4*(at*(BN/128) + r), the order one MMA's scale read expects
+#pragma unroll
+                for (int at = 0; at < L::KATOMS; ++at) {
+                    tc_cp_32x128b_warpx4(sfa_t + 4 * at, da + at * kAtom);
+#pragma unroll
+                    for (int r = 0; r < BN / 128; ++r)
+                        tc_cp_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r,
+                                             db + (r * L::KATOMS + at) * kAtom);
+                }
+                tc_commit(ready_bar(static_cast<int>(st)));
+                MACAQ_TRACE(11, it);
+                if (++st == STAGES) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            // its copies must complete before tensor memory is freed
+            tc_commit(drain_bar2);
+            wait_fixed(drain_bar2, 0);
+        }
+        __syncwarp();
     } else {
         // ---------------------------------------------------- epilogue
-        const int ew = warp - 2;
+        const int ew = warp - EPI_WARP0;
         const int q = warp & 3;     // tensor-memory lane quarter this warp may access
         const int half = ew >> 2;   // which 128 accumulator columns
         const uint32_t ebuf = sbase + L::OFF_EPI + ew * 2 * EPI_BUF;
         uint32_t tc = 0, chunk = 0;
-        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tc) {
+        for (int64_t u = first_unit; u < total_units; u += unit_stride, ++tc) {
             Tile ti;
-            decode_tile<BN, GROUPED>(t, p, s_off, s_pmb, ti);
-            if (!wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
+            decode_tile<BN, CLUSTER, GROUPED>(u, rank, p, s_off, s_pmb, ti);
+            if (warp == EPI_WARP0) MACAQ_TRACE(6, tc);
+            if (!warp_wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
+            if (warp == EPI_WARP0) MACAQ_TRACE(7, tc);
             tc_fence_after();
             uint32_t acc[4][32];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128;
@@ -353,6 +486,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
+            if (warp == EPI_WARP0) MACAQ_TRACE(8, tc);
 
             const int row0 = 32 * q;  // first tile row of this warp
             const bool any_row = row0 < ti.rows_valid;
@@ -410,6 +544,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     __syncthreads();
+    MACAQ_TRACE_EDGE(1);
+    // no CTA of the cluster may leave while a peer can still touch its shared memory
+    if (CLUSTER > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
@@ -432,7 +569,7 @@ __global__ void wait_probe_kernel()
 // Tensor-core rate probe: one CTA per SM issues `iters` x 4 back-to-back
 // kind::mxf4 block-scaled MMAs (M=128, N=bn, K=64) on operands resident in
 // shared memory and reports the elapsed SM cycles and nanoseconds.
-__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, unsigned long long *out)
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn_mode, int iters, unsigned long long *out, const uint8_t *src)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -440,7 +577,9 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
     const uint32_t sbase = smem_u32(smem);
     // A 16 KB | B 32 KB | SFA 1 KB | SFB 2 KB | barrier | tmem slot
     const uint32_t a_s = sbase, b_s = sbase + 16384, sfa_s = sbase + 49152, sfb_s = sbase + 50176;
+    const int bn = bn_mode & 0xffff;
     const uint32_t bar = sbase + 52224;
+    const uint32_t bar2 = sbase + 52240;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + 52232);
     for (int i = threadIdx.x; i < 52224 / 4; i += blockDim.x) {
         const uint32_t x = static_cast<uint32_t>(i) * 2654435761u;
@@ -450,6 +589,9 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
     fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar2, 1);
+        mbar_init(sbase + 52256, 1);
+        *reinterpret_cast<volatile int *>(smem + 52264) = 0;
         fence_mbar_init();
     }
     if ((threadIdx.x >> 5) == 0) {
@@ -469,9 +611,20 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
                                      smem_desc(sfb_s + r * 1024 + at * 512, 0, 128, kSwizzleNone));
         }
         const int nsf = (bn + 127) / 128;
+        const int mode = bn_mode >> 16;
         const long long c0 = clock64();
         const uint64_t t0 = globaltimer();
         for (int it = 0; it < iters; ++it) {
+            if (mode >= 1) {
+                // the scale copies one 256-wide K stage of the GEMM issues
+                const uint32_t sa = tmem + SF_TMEM_BASE + (it & 3) * 24, sb = sa + 8;
+                for (int at = 0; at < 2; ++at) {
+                    tc_cp_32x128b_warpx4(sa + 4 * at, smem_desc(sfa_s + at * 512, 0, 128, kSwizzleNone));
+                    for (int r = 0; r < 2; ++r)
+                        tc_cp_32x128b_warpx4(sb + at * 8 + 4 * r,
+                                             smem_desc(sfb_s + r * 1024 + at * 512, 0, 128, kSwizzleNone));
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t sf_id = (j & 1) * 2;
@@ -480,6 +633,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
                             idesc_mxf4(BM, static_cast<uint32_t>(bn), sf_id, sf_id),
                             sfa_t + 4 * (j >> 1), sfb_t + 4 * nsf * (j >> 1), (it | j) != 0 ? 1u : 0u);
             }
+            if (mode >= 2) tc_commit(bar2);
         }
         tc_commit(bar);
         wait_fixed(bar, 0);
@@ -487,6 +641,23 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
         const uint64_t t1 = globaltimer();
         out[2 * blockIdx.x] = static_cast<unsigned long long>(c1 - c0);
         out[2 * blockIdx.x + 1] = t1 - t0;
+        *reinterpret_cast<volatile int *>(smem + 52264) = 1;
+    }
+    if (threadIdx.x == 64 && (bn_mode >> 16) == 3 && src != nullptr) {
+        // shared-memory write traffic next to the MMAs: 16 KB bulk copies from
+        // an L2-resident buffer into a 64 KB region, four in flight
+        const uint32_t region = sbase + 53248, lbar = sbase + 52256;
+        uint64_t bytes = 0;
+        uint32_t ph = 0;
+        while (*reinterpret_cast<volatile int *>(smem + 52264) == 0) {
+            mbar_arrive_expect_tx(lbar, 4 * 16384);
+            for (int i = 0; i < 4; ++i)
+                bulk_load(region + i * 16384, src + ((bytes / 16384 + i) % 64) * 16384, 16384, lbar);
+            wait_fixed(lbar, ph);
+            ph ^= 1;
+            bytes += 4 * 16384;
+        }
+        out[2 * gridDim.x + blockIdx.x] = bytes;
     }
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) {
@@ -494,6 +665,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn, int iters, uns
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
+
 
 // ------------------------------------------------------------- host side
 
@@ -525,20 +697,21 @@ bool encode(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *b
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set[4] = {false, false, false, false};
+    bool attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 
-template <int BN, int STAGES, bool GROUPED>
+template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED>
 cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
 {
-    using L = Layout<BN, STAGES>;
+    using L = Layout<BN, STAGES, KB>;
+    constexpr CUtensorMapSwizzle kMapSwizzle = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kern = gemm_mxf4_kernel<BN, STAGES, GROUPED>;
+    auto kern = gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         DeviceInfo &di = g_dev[dev];
@@ -559,24 +732,21 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     {
         uint64_t dims[2] = {kb, static_cast<uint64_t>(g.a_rows)};
         uint64_t strides[1] = {kb};
-        uint32_t box[2] = {BK_BYTES, BM};
-        if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+        uint32_t box[2] = {KB, BM};
+        if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box, kMapSwizzle))
             return cudaErrorInvalidValue;
     }
     if (GROUPED) {
         uint64_t dims[3] = {kb, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.E)};
         uint64_t strides[2] = {kb, kb * static_cast<uint64_t>(g.N)};
-        uint32_t box[3] = {BK_BYTES, BN, 1};
-        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+        uint32_t box[3] = {KB, BN, 1};
+        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box, kMapSwizzle))
             return cudaErrorInvalidValue;
     } else {
         uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
         uint64_t strides[1] = {kb};
-        uint32_t box[2] = {BK_BYTES, BN};
-        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+        uint32_t box[2] = {KB, BN / CLUSTER};
+        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box, kMapSwizzle))
             return cudaErrorInvalidValue;
     }
     {
@@ -598,25 +768,40 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     p.E = g.E;
     p.M = static_cast<int32_t>(g.M);
     p.N = static_cast<int32_t>(g.N);
-    p.num_kstages = static_cast<int32_t>((g.K + 255) / 256);
+    p.num_kstages = static_cast<int32_t>((g.K + 2 * KB - 1) / (2 * KB));
     p.nka = static_cast<int32_t>(pad_scale_cols(g.K) / 4);
     p.num_mb = static_cast<int32_t>((g.M + BM - 1) / BM);
     p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
 
-    int64_t max_tiles = GROUPED ? (g.a_rows / BM) * p.num_nb : static_cast<int64_t>(p.num_mb) * p.num_nb;
-    int64_t grid = max_tiles < sms ? max_tiles : sms;
-    if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), THREADS, L::ALLOC, stream>>>(tmA, tmB, tmY, p);
-    return cudaGetLastError();
+    const int64_t units = GROUPED ? (g.a_rows / BM) * p.num_nb
+                                  : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
+    int64_t clusters = units < sms / CLUSTER ? units : sms / CLUSTER;
+    if (clusters < 1) clusters = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
 {
-    if (g.E > 0) return launch_impl<256, 4, true>(g, stream, 1);
-    return launch_impl<256, 4, false>(g, stream, 0);
+    // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
+    // (multicast) the B tile of adjacent m-blocks
+    if (g.E > 0) return launch_impl<256, 4, 128, 1, true>(g, stream, 1);
+    return launch_impl<256, 4, 128, 2, false>(g, stream, 2);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)
@@ -639,13 +824,15 @@ cudaError_t launch_wait_probe(cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, int ctas, cudaStream_t stream)
+cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, const uint8_t *src, int ctas,
+                            cudaStream_t stream)
 {
-    const int smem = 52240 + 1024;
+    const int smem = 53248 + 65536 + 1024;
     cudaError_t err = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    mma_rate_kernel<<<ctas, 128, smem, stream>>>(bn, iters, out);
+    mma_rate_kernel<<<ctas, 128, smem, stream>>>(bn, iters, out, src);
     return cudaGetLastError();
 }
+
 
 }  // namespace macaq

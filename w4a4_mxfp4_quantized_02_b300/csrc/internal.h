@@ -68,7 +68,7 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(unsigned *flags);
 cudaError_t set_wait_timeout_ns(uint64_t ns);
 cudaError_t launch_wait_probe(cudaStream_t stream);
-cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, int ctas,
+cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, const uint8_t *src, int ctas,
                             cudaStream_t stream);
 
 }  // namespace macaq
