@@ -145,6 +145,27 @@ macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s,
                           int64_t N, int64_t K, void *Y, int64_t ldy, void *workspace,
                           size_t ws_bytes, macaq_stream_t stream);
 
+/* macaq_linear for callers that cannot allocate device memory at the call
+ * site -- for example a plugin whose host framework owns every device
+ * allocation, or a runtime that fixes its device memory at start-up.  The
+ * workspace is instead a scratch array of MACAQ_LINEAR_STATIC_SCRATCH_BYTES
+ * inside the library's own module image; every GPU that loads the library
+ * holds that array until the process exits.  The pages describe no such
+ * entry point: it exists only for these callers.
+ * Arguments as macaq_linear, without workspace / ws_bytes.  A problem whose
+ * macaq_linear_workspace_bytes(M, K) exceeds the array is rejected with
+ * MACAQ_ERR_WORKSPACE before anything is launched.  Nothing is allocated:
+ * the first call on a device looks up the array's device address (make that
+ * first call before any stream capture).  All calls on a device share the
+ * one array, so calls that can overlap on the GPU (different streams without
+ * ordering) race; the array keeps the last call's contents, which no call
+ * depends on. */
+#define MACAQ_LINEAR_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+macaq_status macaq_linear_no_alloc(const void *X, int64_t ldx, const float *inv_s,
+                                   const uint8_t *w_codes, const uint8_t *w_scales, int64_t M,
+                                   int64_t N, int64_t K, void *Y, int64_t ldy,
+                                   macaq_stream_t stream);
+
 /* ---------------------------------------------------- grouped (MoE) */
 
 /* Rows of the expert-padded layout the grouped kernels use for `rows`

@@ -52,6 +52,7 @@ _SIGS = {
     "macaq_w4a4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_linear": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
                      ctypes.c_int),
+    "macaq_linear_no_alloc": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_quant_act_grouped": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P],
                                 ctypes.c_int),
     "macaq_grouped_w4a4_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P],
@@ -211,6 +212,20 @@ def macaq_linear(X: torch.Tensor, inv_s, w_codes, w_scales, N: int, Y=None, work
     _check("macaq_linear", lib().macaq_linear(
         _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return Y
+
+
+def macaq_linear_no_alloc(X: torch.Tensor, inv_s, w_codes, w_scales, N: int, Y=None,
+                          stream=None):
+    """macaq_linear with the library's own fixed scratch array as workspace
+    (for callers that cannot allocate device memory; see the header)."""
+    _dev(X, "X")
+    M, K = X.shape
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
+    _check("macaq_linear_no_alloc", lib().macaq_linear_no_alloc(
+        _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
+        _stream(stream)))
     return Y
 
 

@@ -27,6 +27,7 @@ UNITS = {
     "quant.cu": ["-fmad=false"],
     "gemm.cu": [],
     "api.cu": [],
+    "static_scratch.cu": [],
 }
 HEADERS = ["internal.h", "ptx.cuh"]
 
