@@ -369,7 +369,7 @@ def gpu_arm(args, rank: int, world: int):
     if os.path.exists(prof):
         with open(prof) as f:
             tj = json.load(f)
-        if tj.get("workload") == wl.name and tj.get("kernel_rev") == KERNEL_REV:
+        if tj.get("workload") == wl.name and tj.get("kernel_source_sha") == kernel_source_sha():
             traffic = tj.get("dram_bytes_per_launch")
 
     if rank != 0:
@@ -419,7 +419,34 @@ def gpu_arm(args, rank: int, world: int):
     return 0
 
 
-KERNEL_REV = "gemm-v1"
+def kernel_source_sha() -> str:
+    """Hash of the GEMM kernel sources: a recorded traffic figure is only used
+    while the kernel it was measured on is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "w4a4_mxfp4_quantized_02_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def mma_probe():
+    """Tensor-pipe rate of kind::mxf4 MMAs (M=128, N, K=64) per SM."""
+    import torch
+    import w4a4_mxfp4_quantized_02_b300 as mq
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    iters = 4000
+    print("| N | mode | cycles per 4 MMAs | PFLOP/s (all SMs, at the measured clock) | clock GHz |")
+    print("|---|---|---|---|---|")
+    names = {0: "MMAs only", 1: "+ 6 scale copies per 4 MMAs", 2: "+ copies + commit"}
+    for mode in (0, 1, 2):
+        for n in (64, 128, 192, 256):
+            out = mq.macaq_debug_mma_rate(n | (mode << 16), iters, sms).cpu().double()
+            cyc = out[0:2 * sms:2].median().item()
+            ns = out[1:2 * sms:2].median().item()
+            flops = sms * 4 * iters * 2 * 128 * n * 64
+            print(f"| {n} | {names[mode]} | {cyc / iters:.1f} | {flops / ns / 1e6:.2f} | {cyc / ns:.3f} |")
+    return 0
 
 
 def main():
@@ -431,7 +458,10 @@ def main():
     ap.add_argument("--config", default="attn")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe", choices=["mma"], help="print a hardware probe table and exit")
     args = ap.parse_args()
+    if args.probe == "mma":
+        return mma_probe()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
