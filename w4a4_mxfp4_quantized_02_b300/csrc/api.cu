@@ -261,9 +261,10 @@ macaq_status macaq_check_device_error(macaq_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MACAQ_ERR_CUDA;
-    unsigned flags = 0;
+    unsigned flags = 0, qflags = 0;
     if (read_and_clear_device_error(&flags) != cudaSuccess) return MACAQ_ERR_CUDA;
-    return flags ? MACAQ_ERR_TIMEOUT : MACAQ_OK;
+    if (read_and_clear_quant_error(&qflags) != cudaSuccess) return MACAQ_ERR_CUDA;
+    return (flags | qflags) ? MACAQ_ERR_TIMEOUT : MACAQ_OK;
 }
 
 macaq_status macaq_set_wait_timeout_ns(uint64_t ns)

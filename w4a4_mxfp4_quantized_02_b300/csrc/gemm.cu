@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
     }
     if (GROUPED) {
+        griddep_wait();  // expert offsets may come from the previous kernel
         for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -270,6 +271,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (CLUSTER > 1) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Everything above only touched this CTA's own resources.  The next kernel
+    // may now start its own set-up; this one waits for the previous kernel
+    // (producer of A, reader of Y) before touching global memory.
+    griddep_launch_dependents();
+    griddep_wait();
 
     const int64_t total_units =
         GROUPED ? static_cast<int64_t>(s_pmb[p.E]) * p.num_nb
@@ -669,30 +675,10 @@ __global__ void __launch_bounds__(128, 1) mma_rate_kernel(int bn_mode, int iters
 
 // ------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 bool encode(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base,
             const uint64_t *dims, const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle sw)
 {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    uint32_t es[3] = {1, 1, 1};
-    return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tensor_map(m, dt, rank, base, dims, strides, box, sw);
 }
 
 struct DeviceInfo {
@@ -784,17 +770,48 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
 }
 
 }  // namespace
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+}  // namespace
+
+bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base,
+                       const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                       CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    uint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
 {

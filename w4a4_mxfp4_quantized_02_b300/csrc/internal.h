@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "macaq.h"
@@ -65,7 +66,14 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
+// link), interleave none, 256-byte L2 promotion, zero fill out of bounds.
+bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *base,
+                       const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                       CUtensorMapSwizzle sw);
+
 cudaError_t read_and_clear_device_error(unsigned *flags);
+cudaError_t read_and_clear_quant_error(unsigned *flags);
 cudaError_t set_wait_timeout_ns(uint64_t ns);
 cudaError_t launch_wait_probe(cudaStream_t stream);
 cudaError_t launch_mma_rate(int bn, int iters, unsigned long long *out, const uint8_t *src, int ctas,

@@ -311,5 +311,21 @@ __device__ __forceinline__ void bulk_prefetch(const void *src, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// -------------------------------------------------- programmatic dependent launch
+
+// Allow the next kernel in the stream (launched with programmatic stream
+// serialisation) to start its CTAs once every CTA of this grid has passed here.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel in the stream has completed and its memory
+// operations are visible (a no-op when this kernel was launched normally).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace macaq

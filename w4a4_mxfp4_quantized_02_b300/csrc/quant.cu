@@ -24,9 +24,31 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace macaq {
+
+// Set when a wait in a quantisation kernel runs out (reported through
+// macaq_check_device_error).
+__device__ unsigned int g_quant_error_flags;
+
 namespace {
+
+constexpr uint64_t kQuantWaitNs = 2000000000ull;
+
+// Bounded wait on a TMA barrier; false (and the error flag) after kQuantWaitNs.
+__device__ __forceinline__ bool quant_wait(uint32_t bar, uint32_t parity)
+{
+    if (ptx::mbar_try_wait(bar, parity, 100000)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity, 100000)) return true;
+        if (ptx::globaltimer() - t0 > kQuantWaitNs) {
+            atomicOr(&g_quant_error_flags, 1u);
+            return false;
+        }
+    }
+}
 
 // fp32 nearest to 2^-2.5 = 1/sqrt(32).
 constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
@@ -297,6 +319,10 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
     constexpr int R = 2;  // rows per iteration (loads of all R rows in flight together)
     __shared__ int32_t s_off[kMaxExperts + 1];
     __shared__ int32_t s_poff[kMaxExperts + 1];
+    // launched with programmatic stream serialisation: let the next kernel
+    // start its set-up, and wait for the previous one before touching memory
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     if (MODE == QuantMode::ActGrouped) {
         for (int e = threadIdx.x; e <= a.E; e += blockDim.x) s_off[e] = a.offsets[e];
         __syncthreads();
@@ -388,6 +414,215 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
     }
 }
 
+
+// ------------------------------------------------ TMA-staged dense variant
+
+// The same transform as quant_block with the natural register pairing
+// v[i] = (element 2i, element 2i+1): the stride-1 stage (fed by products, so
+// scalar) pairs the halves of a register, strides 2, 4, 8, 16 pair whole
+// registers i and i + h/2 and run as packed adds; the bf16 words and the
+// output bytes already come in this pairing.
+__device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
+                                                      uint4 &codes)
+{
+    float2 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = __fmul_rn(bf16lo(raw[i]), f[i].x);
+        const float b = __fmul_rn(bf16hi(raw[i]), f[i].y);
+        v[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
+#pragma unroll
+    for (int hh = 1; hh < 16; hh <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & hh) continue;
+            const float2 a = v[i];
+            const float2 b = v[i + hh];
+            // sums of sums: no multiply feeds these adds, so the packed
+            // intrinsics cannot be contracted into an FMA
+            v[i] = __fadd2_rn(a, b);
+            v[i + hh] = __fadd2_rn(a, make_float2(-b.x, -b.y));
+        }
+    }
+    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        m0 = fmaxf(m0, fabsf(v[i].x));
+        m1 = fmaxf(m1, fabsf(v[i].y));
+    }
+    const float vmax = fmaxf(m0, m1);
+    const float amax = __fmul_rn(vmax, kInvSqrt32);
+    const int ef = static_cast<int>(__float_as_uint(amax) >> 23);
+    const uint32_t sbyte = static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
+    const int se = static_cast<int>(sbyte) - 127;
+    if (se >= -124 && se <= 122) {
+        const float g = __int_as_float(__float_as_int(kInvSqrt32) - se * (1 << 23));
+        const float2 g2 = make_float2(g, g);
+        // the scaled values feed only the encoder: no add follows this multiply
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], g2);
+    } else {
+        const float c = kInvSqrt32;
+        const float inv = __uint_as_float((254u - sbyte) << 23);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = __fmul2_rn(v[i], make_float2(c, c));
+            v[i] = __fmul2_rn(v[i], make_float2(inv, inv));
+        }
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t b0 = e2m1x2(v[4 * q].x, v[4 * q].y);
+        const uint32_t b1 = e2m1x2(v[4 * q + 1].x, v[4 * q + 1].y);
+        const uint32_t b2 = e2m1x2(v[4 * q + 2].x, v[4 * q + 2].y);
+        const uint32_t b3 = e2m1x2(v[4 * q + 3].x, v[4 * q + 3].y);
+        w[q] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+    }
+    codes = make_uint4(w[0], w[1], w[2], w[3]);
+    return sbyte;
+}
+
+// Dense rows through a TMA ring.  X is viewed as [rows][blocks][32 values];
+// one box per stage brings RT rows x TB blocks (64 bytes each, 64-byte
+// swizzle so the four 16-byte reads of 8 neighbouring threads hit distinct
+// banks) into shared memory.  Consumer thread c = ty * TB + tx owns block tx
+// of the slab in row ty of every group of RT rows and keeps its 32 balance
+// factors in registers; the last warp only issues the loads, STAGES groups
+// ahead.  Warps run decoupled: each consumer warp waits on a stage's "full"
+// barrier through one lane and releases it on the stage's "empty" barrier.
+template <int STAGES>
+__global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                  QuantArgs a, int32_t groups, int32_t TB,
+                                                                  int32_t RT)
+{
+    extern __shared__ uint8_t qsmem_raw[];
+    const uint32_t raw_base = ptx::smem_u32(qsmem_raw);
+    uint8_t *qsmem = qsmem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_u32(qsmem);
+    const int NC = TB * RT;  // consumer threads
+    const int cwarps = NC / 32;
+    const uint32_t stage_bytes = static_cast<uint32_t>(NC * 64);
+    const uint32_t full0 = sbase + STAGES * stage_bytes;
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(qsmem + STAGES * stage_bytes + 16 * STAGES);
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int32_t slab0 = static_cast<int32_t>(blockIdx.x) * TB;
+
+    if (t == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(empty0 + 8 * s, static_cast<uint32_t>(cwarps));
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // launched with programmatic stream serialisation: let the next kernel
+    // start its set-up, and wait for the previous one (which may produce X or
+    // still read the codes) before touching global memory
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+
+    const int32_t my_groups = blockIdx.y < static_cast<uint32_t>(groups)
+                                  ? (groups - 1 - static_cast<int32_t>(blockIdx.y)) / static_cast<int32_t>(gridDim.y) + 1
+                                  : 0;
+
+    if (t >= NC) {
+        // ------------------------------------------------ producer warp
+        if (lane == 0) {
+            int32_t j = 0;
+            for (; j < my_groups; ++j) {
+                const int s = j % STAGES;
+                if (j >= STAGES && !quant_wait(empty0 + 8 * s, static_cast<uint32_t>(j / STAGES - 1) & 1u)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const int32_t g = static_cast<int32_t>(blockIdx.y) + j * static_cast<int32_t>(gridDim.y);
+                ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(sbase + s * stage_bytes),
+                    "l"(&tmX), "r"(full0 + 8 * s), "r"(0), "r"(slab0), "r"(g * RT)
+                    : "memory");
+            }
+            // every issued copy must land before the CTA exits
+            for (int32_t k = (j > STAGES ? j - STAGES : 0); k < j; ++k)
+                quant_wait(full0 + 8 * (k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int tx = t % TB, ty = t / TB;
+    const int64_t nkb = a.K / 32;
+    const int64_t nka = ((nkb + 7) / 8 * 8) / 4;
+    const int64_t nkb_pad = nka * 4;
+    const int64_t kb = static_cast<int64_t>(slab0) + tx;
+    const bool has_kb = kb < nkb;
+    const bool writes_scale = (lane & 3) == 0 && kb < nkb_pad;
+    float2 f[16];
+    if (has_kb) {
+        const float4 *f4 = reinterpret_cast<const float4 *>(a.f + 32 * kb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 v4 = __ldg(f4 + j);
+            f[2 * j] = make_float2(v4.x, v4.y);
+            f[2 * j + 1] = make_float2(v4.z, v4.w);
+        }
+    }
+    const uint32_t swz = (static_cast<uint32_t>(t) >> 1) & 3u;  // 64-byte row t of a stage
+    const int64_t half_k = a.K / 2;
+
+    for (int32_t j = 0; j < my_groups; ++j) {
+        const int s = j % STAGES;
+        int ok = 1;
+        if (lane == 0) {
+            ok = quant_wait(full0 + 8 * s, static_cast<uint32_t>(j / STAGES) & 1u) ? 1 : 0;
+            if (!ok) *abort_flag = 1;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int32_t g = static_cast<int32_t>(blockIdx.y) + j * static_cast<int32_t>(gridDim.y);
+        const int64_t r = static_cast<int64_t>(g) * RT + ty;  // row (padded space)
+        uint32_t sbyte = 0;
+        if (r < a.rows_valid && has_kb) {
+            uint32_t raw[16];
+            const uint32_t base = sbase + s * stage_bytes + static_cast<uint32_t>(t) * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t x0, x1, x2, x3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                             : "r"(base + 16 * (c ^ swz)));
+                raw[4 * c] = x0;
+                raw[4 * c + 1] = x1;
+                raw[4 * c + 2] = x2;
+                raw[4 * c + 3] = x3;
+            }
+            // the stage is no longer needed by this warp once its reads are done
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
+            uint4 codes;
+            sbyte = quant_block_pairs(raw, f, codes);
+            *reinterpret_cast<uint4 *>(a.codes + r * half_k + 16 * kb) = codes;
+        } else {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
+        }
+        uint32_t word = sbyte << (8 * (lane & 3));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (writes_scale && r < a.rows_out) {
+            const int64_t off = ((r / 128) * nka + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+            *reinterpret_cast<uint32_t *>(a.scales + off) = word;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- balance
 
 __global__ void __launch_bounds__(256) balance_kernel(const uint16_t *xc, int64_t ldxc,
@@ -450,6 +685,68 @@ __global__ void debug_e2m1_kernel(const float *t, int64_t n, uint8_t *codes)
 
 }  // namespace
 
+#define MACAQ_TRY_CUDA(expr)                   \
+    do {                                       \
+        cudaError_t e__ = (expr);              \
+        if (e__ != cudaSuccess) return e__;    \
+    } while (0)
+
+// Launch with programmatic stream serialisation (the kernel itself waits for
+// its predecessor with griddepcontrol.wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t stream, bool *done)
+{
+    *done = false;
+    const int64_t nkb = a.K / 32;
+    const int64_t nkb_pad = pad_scale_cols(a.K);
+    const int64_t slabs = (nkb_pad + tb - 1) / tb;
+    int64_t rt = 512 / tb;  // consumer threads <= 512 (plus one producer warp)
+    rt = rt > 16 ? 16 : (rt < 1 ? 1 : rt);
+    const int64_t stage = tb * rt * 64;
+    const int stages = (6 * stage + 1024 <= 200 * 1024) ? 6 : 4;
+    const int64_t smem = stages * stage + 16 * stages + 16 + 1024;
+    if (smem > 200 * 1024) return cudaSuccess;  // fall through to the register-staged kernel
+    CUtensorMap tm;
+    const uint64_t dims[3] = {32, static_cast<uint64_t>(nkb), static_cast<uint64_t>(a.rows_valid)};
+    const uint64_t strides[2] = {64, static_cast<uint64_t>(a.ld_src) * 2};
+    const uint32_t box[3] = {32, static_cast<uint32_t>(tb), static_cast<uint32_t>(rt)};
+    if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t groups = (a.rows_out + rt - 1) / rt;
+    int64_t ctas_y = sms / slabs;  // one CTA per SM: never a partial second wave
+    ctas_y = ctas_y < 1 ? 1 : ctas_y;
+    ctas_y = ctas_y > groups ? groups : ctas_y;
+    auto kern = stages == 6 ? quant_dense_tma_kernel<6> : quant_dense_tma_kernel<4>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
+    dim3 block(static_cast<unsigned>(tb * rt + 32));
+    MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
+                              static_cast<int32_t>(groups), static_cast<int32_t>(tb), static_cast<int32_t>(rt)));
+    *done = true;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream)
 {
     const int64_t nkb_pad = pad_scale_cols(a.K);
@@ -464,6 +761,11 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
             best_waste = waste;
             best_t = t;
         }
+    }
+    if (mode == QuantMode::Dense && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
+        bool done = false;
+        cudaError_t err = launch_quant_dense_tma(a, best_t, stream, &done);
+        if (err != cudaSuccess || done) return err;
     }
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
@@ -486,9 +788,9 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
     const bool wide = (reinterpret_cast<uintptr_t>(a.src) % 32 == 0) && ((a.ld_src * 2) % 32 == 0);
 #define MACAQ_LAUNCH_QUANT(M)                                                              \
     if (wide)                                                                              \
-        quant_kernel<M, true><<<grid, block, 0, stream>>>(a, rows_per_cta);                \
+        MACAQ_TRY_CUDA(launch_pdl(quant_kernel<M, true>, grid, block, 0, stream, a, rows_per_cta)); \
     else                                                                                   \
-        quant_kernel<M, false><<<grid, block, 0, stream>>>(a, rows_per_cta);
+        MACAQ_TRY_CUDA(launch_pdl(quant_kernel<M, false>, grid, block, 0, stream, a, rows_per_cta));
     switch (mode) {
     case QuantMode::Dense:
         MACAQ_LAUNCH_QUANT(QuantMode::Dense)
@@ -511,6 +813,14 @@ cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_r
     dim3 grid(static_cast<unsigned>((k + 63) / 64));
     balance_kernel<<<grid, 256, 0, stream>>>(xc, ldxc, xc_rows, mc, w, n, k, s, inv_s);
     return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_quant_error(unsigned *flags)
+{
+    cudaError_t err = cudaMemcpyFromSymbol(flags, g_quant_error_flags, sizeof(unsigned));
+    if (err != cudaSuccess) return err;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_quant_error_flags, &zero, sizeof(unsigned));
 }
 
 cudaError_t launch_debug_e2m1(const float *t, int64_t n, uint8_t *codes, cudaStream_t stream)
