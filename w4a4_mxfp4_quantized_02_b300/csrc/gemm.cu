@@ -6,19 +6,27 @@
 // inference mode; routed MoE experts run W4A4).  Y = A . Wq^T with both
 // operands E2M1 codes scaled per 32 elements by E8M0 powers of two.
 //
-// Kernel shape (persistent, one CTA per SM, 320 threads):
+// Two persistent kernels, one CTA per SM, warp-specialised:
+//   gemm_mxf4_pair_kernel   dense Y: CTA pairs (tcgen05 cta_group::2) on
+//                           256 x 256 tiles; see the comment at the kernel.
+//   gemm_mxf4_kernel        grouped (MoE) Y: one CTA per 128 x 256 tile of
+//                           one expert's rows.
+// Common shape (352 threads):
 //   warp 0      TMA producer: per 256-wide K stage, the A tile (128 rows x
-//               128 B), the B tile (BN rows x 128 B), both 128B-swizzled, and
-//               the scale tiles (512-byte atoms) by bulk copy, into a ring of
-//               STAGES shared-memory buffers guarded by mbarriers.
-//   warp 1      MMA issuer (one thread): copies the stage's scale atoms to
-//               tensor memory (tcgen05.cp 32x128b.warpx4) and issues four
-//               tcgen05.mma.kind::mxf4.block_scale (M=128, N=BN, K=64)
-//               accumulating in tensor memory; tcgen05.commit frees the stage.
-//   warps 2..9  epilogue: tcgen05.ld of the 128 x BN fp32 accumulator (each
-//               warp 32 lanes x 128 columns, all in registers), release of
-//               the accumulator, then bf16 rounding and TMA stores of
-//               32 x 16 boxes through a per-warp double buffer.
+//               128 B), the B tile, both 128B-swizzled, and the scale tiles
+//               (512-byte atoms), into a ring of STAGES shared-memory buffers
+//               guarded by mbarriers.
+//   warp 1      MMA issuer (one thread): tcgen05.mma.kind::mxf4.block_scale
+//               (K = 64 per instruction) accumulating in tensor memory;
+//               tcgen05.commit frees the stage.
+//   warp 2      scale copier: tcgen05.cp 32x128b.warpx4 of the stage's scale
+//               atoms into tensor memory, committed to "scales ready".  In
+//               the MMA thread these copies would stall the tensor pipe: a
+//               barrier wait issued after them waits for them to finish.
+//   warps 3..10 epilogue: tcgen05.ld of the fp32 accumulator (each warp 32
+//               lanes x 128 columns, all in registers), release of the
+//               accumulator, then bf16 rounding and TMA stores of 32 x 16
+//               boxes.
 // Every mbarrier wait is bounded in time; a wait that runs out sets a device
 // error flag and the CTA leaves in order (drains its copies and MMAs, frees
 // tensor memory).
@@ -559,6 +567,355 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------ CTA-pair GEMM
+//
+// Dense GEMM on CTA pairs (tcgen05 cta_group::2).  A pair computes a 256 x 256
+// tile of Y: rank r holds rows 128r..128r+127 of the tile's A and the same
+// 128 rows of B (its half of the N = 256 columns); rank 0 issues one
+// M = 256, N = 256, K = 64 MMA per k step, which reads both CTAs' shared
+// memory and accumulates each CTA's 128 x 256 block in its own tensor
+// memory.  Per 256-wide K stage a CTA so loads 32 KB of operands instead of
+// the 48 KB a single-CTA M = 128, N = 256 tile needs, and the scale copies of
+// one stage serve both halves of the tile.
+//
+// Roles (the same warps in both CTAs):
+//   warp 0      TMA producer of this CTA's stage buffers (A rows, B rows,
+//               A's scales, and B's scales for all 256 columns).  Both CTAs'
+//               copies signal rank 0's "full" barrier (TMA .cta_group::2),
+//               so it completes only when both halves of the stage are in.
+//   warp 1      rank 0: MMA issuer.
+//   warp 2      rank 0: scale copier (tcgen05.cp into both CTAs' tensor
+//               memory, each from its own shared memory).
+//   warps 3..10 epilogue, each CTA for its own 128 rows; release of the
+//               accumulator is an arrival on rank 0's barrier.
+template <int STAGES>
+struct PairLayout {
+    static constexpr int BN = 256;           // tile columns (both CTAs)
+    static constexpr int KB = 128;           // operand bytes per row per stage
+    static constexpr int KATOMS = KB / 64;
+    static constexpr int KSTEPS = KB / 32;           // MMAs (K = 64) per stage
+    static constexpr int A_STAGE = BM * KB;          // this CTA's 128 rows of A
+    static constexpr int B_STAGE = (BN / 2) * KB;    // this CTA's 128 rows of B
+    static constexpr int SFA_STAGE = KATOMS * SF_ATOM;
+    static constexpr int SFB_STAGE = (BN / 128) * KATOMS * SF_ATOM;  // all 256 columns
+    static constexpr int SF_COLS = 4 * KATOMS + 4 * KATOMS * (BN / 128);
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
+    // store staging per epilogue warp: double-buffered when it fits
+    static constexpr int EPI_NBUF = STAGES >= 6 ? 1 : 2;
+    static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * EPI_NBUF * EPI_BUF;
+    static constexpr int NUM_BARS = 3 * STAGES + 4;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+    static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
+    static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
+    static_assert(ALLOC <= 232448, "shared memory");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSFA,
+                          const __grid_constant__ CUtensorMap tmSFB, const Params p)
+{
+    using L = PairLayout<STAGES>;
+    constexpr int BN = L::BN;
+    constexpr int KB = L::KB;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_base = sbase + L::OFF_BAR;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto ready_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+    const uint32_t acc_full = bar_base + 8u * (3 * STAGES);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t drain_bar = acc_full + 16u;
+    const uint32_t drain_bar2 = acc_full + 24u;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    MACAQ_TRACE_EDGE(0);
+    const uint64_t wait_ns = g_wait_ns;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t first_unit = blockIdx.x >> 1;
+    const int64_t unit_stride = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            // (rank 0's) stage is full once both CTAs' copies have landed
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);  // one MMA commit, multicast to both CTAs
+            mbar_init(ready_bar(s), 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * NUM_EPI_WARPS);  // every epilogue warp of the pair
+        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar2, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sbase + L::OFF_MISC, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_launch_dependents();
+    griddep_wait();
+
+    const int32_t num_mp = (p.M + 2 * BM - 1) / (2 * BM);
+    const int64_t total_units = static_cast<int64_t>(num_mp) * p.num_nb;
+    const int nks = p.num_kstages;
+    // scale atoms of stage st -> its tensor-memory slot (A: atom `at` at column
+    // 4*at; B: atom `at` of row block r at 4*(2*at + r)), in both CTAs
+    auto copy_scales = [&](uint32_t st) {
+        const uint64_t da = smem_desc(sbase + L::OFF_SFA + st * L::SFA_STAGE, 0, 128, kSwizzleNone);
+        const uint64_t db = smem_desc(sbase + L::OFF_SFB + st * L::SFB_STAGE, 0, 128, kSwizzleNone);
+        const uint32_t sfa_t = tmem + SF_TMEM_BASE + st * L::SF_COLS;
+        const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
+        constexpr uint32_t kAtom = SF_ATOM >> 4;
+#pragma unroll
+        for (int at = 0; at < L::KATOMS; ++at) {
+            tc_cp_pair_32x128b_warpx4(sfa_t + 4 * at, da + at * kAtom);
+#pragma unroll
+            for (int r = 0; r < BN / 128; ++r)
+                tc_cp_pair_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r, db + (r * L::KATOMS + at) * kAtom);
+        }
+    };
+    // unit u: pair m-block u % num_mp (m fastest), n-block u / num_mp
+    auto tile_of = [&](int64_t u, Tile &ti) {
+        const int32_t mp = static_cast<int32_t>(u % num_mp);
+        const int32_t nb = static_cast<int32_t>(u / num_mp);
+        ti.a_row = mp * 2 * BM + static_cast<int32_t>(rank) * BM;
+        ti.n0 = nb * BN;
+        ti.expert = 0;
+        ti.y_row0 = ti.a_row;
+        ti.rows_valid = min(BM, p.M - ti.a_row);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            // Every box is loaded whole (rows or scale blocks past the end of a
+            // tensor are filled with zeros), so each CTA lands the same bytes
+            // per stage.  Rows of A / B past the end are never stored.
+            constexpr uint32_t kStageBytes = L::A_STAGE + L::B_STAGE + L::SFA_STAGE + L::SFB_STAGE;
+            const uint32_t full0 = mapa_shared(full_bar(0), 0);
+            uint32_t it = 0;
+            uint32_t issued = 0;
+            uint32_t last_parity = 0;
+            for (int64_t u = first_unit; u < total_units; u += unit_stride) {
+                Tile ti;
+                tile_of(u, ti);
+                const int32_t a_rb = ti.a_row / BM;
+                const int32_t n_rb0 = ti.n0 / 128;
+                bool ok = true;
+                for (int ks = 0; ks < nks; ++ks, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    MACAQ_TRACE(0, it);
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    MACAQ_TRACE(1, it);
+                    const uint32_t fb = full0 + 8u * s;
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+                    tma_load_2d_pair(sbase + L::OFF_A + s * L::A_STAGE, &tmA, fb, ks * KB, ti.a_row);
+                    tma_load_2d_pair(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * KB,
+                                     ti.n0 + static_cast<int32_t>(rank) * (BN / 2));
+                    // scale blocks: (256 B, 2, k atom, 128-row block) views of the tiled layout
+                    tma_load_4d_pair(sbase + L::OFF_SFA + s * L::SFA_STAGE, &tmSFA, fb, 0, 0,
+                                     L::KATOMS * ks, a_rb);
+                    tma_load_4d_pair(sbase + L::OFF_SFB + s * L::SFB_STAGE, &tmSFB, fb, 0, 0,
+                                     L::KATOMS * ks, n_rb0);
+                    issued |= 1u << s;
+                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
+                }
+                if (!ok) break;
+            }
+            // the copies issued into this CTA must land, and rank 0's MMAs must
+            // have released every stage, before the CTA may leave (a stage is
+            // released only after it landed in both CTAs)
+            for (int s = 0; s < STAGES; ++s) {
+                if (issued & (1u << s)) {
+                    if (leader) wait_fixed(full_bar(s), (last_parity >> s) & 1u);
+                    wait_fixed(empty_bar(s), (last_parity >> s) & 1u);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (rank 0)
+            const uint64_t a_desc0 = smem_desc(sbase + L::OFF_A, 16, 8 * KB, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(sbase + L::OFF_B, 16, 8 * KB, kSwizzle128B);
+            const uint32_t idesc0 = idesc_mxf4(2 * BM, BN, 0, 0);
+            const uint32_t idesc2 = idesc_mxf4(2 * BM, BN, 2, 2);
+            const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
+            constexpr uint32_t kAStep = L::A_STAGE >> 4, kBStep = L::B_STAGE >> 4;
+            uint32_t st = 0, ph = 0, tc = 0;
+            bool ok = true;
+            for (int64_t u = first_unit; u < total_units && ok; u += unit_stride, ++tc) {
+                for (int ks = 0; ks < nks; ++ks) {
+                    MACAQ_TRACE(2, tc * nks + ks);
+                    if (!wait_bounded(ready_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    MACAQ_TRACE(3, tc * nks + ks);
+                    if (ks == 0) {
+                        // both CTAs' epilogues must have drained the previous accumulator
+                        MACAQ_TRACE(4, tc);
+                        if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        MACAQ_TRACE(5, tc);
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = sf_t0 + st * L::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
+                    const uint64_t ad = a_desc0 + st * kAStep;
+                    const uint64_t bd = b_desc0 + st * kBStep;
+#pragma unroll
+                    for (int j = 0; j < L::KSTEPS; ++j)
+                        tc_mma_mxf4_pair(tmem, ad + 2 * j, bd + 2 * j, (j & 1) ? idesc2 : idesc0,
+                                         sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
+                                         (ks > 0 || j > 0) ? 1u : 0u);
+                    // the stage's buffers in both CTAs may be refilled once these MMAs read them
+                    tc_commit_pair_mc(empty_bar(static_cast<int>(st)), 3);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair_mc(acc_full, 3);
+            }
+            tc_commit_pair(drain_bar);
+            wait_fixed(drain_bar, 0);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ scale copier (rank 0)
+            uint32_t st = 0, ph = 0, it = 0;
+            bool ok = true;
+            for (int64_t u = first_unit; u < total_units && ok; u += unit_stride) {
+                for (int ks = 0; ks < nks; ++ks, ++it) {
+                    // both CTAs' data of the stage have landed
+                    MACAQ_TRACE(9, it);
+                    if (!wait_bounded(full_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    MACAQ_TRACE(10, it);
+                    copy_scales(st);
+                    tc_commit_pair(ready_bar(static_cast<int>(st)));
+                    MACAQ_TRACE(11, it);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            tc_commit_pair(drain_bar2);
+            wait_fixed(drain_bar2, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int ew = warp - EPI_WARP0;
+        const int q = warp & 3;
+        const int half = ew >> 2;
+        const uint32_t ebuf = sbase + L::OFF_EPI + ew * L::EPI_NBUF * EPI_BUF;
+        const uint32_t leader_acc_empty = mapa_shared(acc_empty, 0);
+        uint32_t tc = 0, chunk = 0;
+        for (int64_t u = first_unit; u < total_units; u += unit_stride, ++tc) {
+            Tile ti;
+            tile_of(u, ti);
+            if (warp == EPI_WARP0) MACAQ_TRACE(6, tc);
+            if (!warp_wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
+            if (warp == EPI_WARP0) MACAQ_TRACE(7, tc);
+            tc_fence_after();
+            uint32_t acc[4][32];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, acc[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+            if (warp == EPI_WARP0) MACAQ_TRACE(8, tc);
+
+            const int row0 = 32 * q;
+            const bool any_row = row0 < ti.rows_valid;
+            if (!any_row) continue;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int32_t ncol = ti.n0 + half * 128 + 16 * c;
+                if (ncol >= p.N) break;
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
+                    const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                {
+                    // rows past M and columns past N are clipped by the store
+                    const uint32_t buf = ebuf + (chunk % L::EPI_NBUF) * EPI_BUF;
+                    ++chunk;
+                    // the store that last read this buffer must be done with it
+                    if (lane == 0) {
+                        if (L::EPI_NBUF == 2) bulk_wait_read_le1();
+                        else bulk_wait_read_all();
+                    }
+                    __syncwarp();
+                    const uint32_t sw = (lane >> 2) & 1;
+                    const uint32_t r0 = buf + lane * 32 + 16 * (0 ^ sw);
+                    const uint32_t r1 = buf + lane * 32 + 16 * (1 ^ sw);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r0), "r"(packed[0]),
+                                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r1), "r"(packed[4]),
+                                 "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
+                                 : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, buf, ncol, ti.y_row0 + row0);
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    __syncthreads();
+    MACAQ_TRACE_EDGE(1);
+    // neither CTA may leave (or free tensor memory) while its peer can still
+    // touch its shared memory, barriers or tensor memory
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
+}
+
 __global__ void wait_probe_kernel()
 {
     __shared__ alignas(8) uint64_t bar;
@@ -681,6 +1038,13 @@ bool encode(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, const void *b
     return encode_tensor_map(m, dt, rank, base, dims, strides, box, sw);
 }
 
+bool encode_4d(CUtensorMap *m, const void *base, const uint64_t *dims, const uint64_t *strides,
+               const uint32_t *box)
+{
+    return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 struct DeviceInfo {
     int sms = 0;
     bool attr_set[8] = {false, false, false, false, false, false, false, false};
@@ -688,16 +1052,30 @@ struct DeviceInfo {
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 
-template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED>
+template <int BN, int STAGES, int KB, bool PAIR>
+constexpr int smem_alloc()
+{
+    if constexpr (PAIR)
+        return PairLayout<STAGES>::ALLOC;
+    else
+        return Layout<BN, STAGES, KB>::ALLOC;
+}
+
+template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED, bool PAIR = false>
 cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
 {
-    using L = Layout<BN, STAGES, KB>;
+    static_assert(!PAIR || (BN == 256 && KB == 128 && CLUSTER == 2 && !GROUPED), "pair tiles are dense 256 x 256");
+    constexpr int kAlloc = smem_alloc<BN, STAGES, KB, PAIR>();
     constexpr CUtensorMapSwizzle kMapSwizzle = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kern = gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>;
+    const void *kern;
+    if constexpr (PAIR)
+        kern = reinterpret_cast<const void *>(gemm_mxf4_pair_kernel<STAGES>);
+    else
+        kern = reinterpret_cast<const void *>(gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>);
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         DeviceInfo &di = g_dev[dev];
@@ -706,7 +1084,7 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
             if (err != cudaSuccess) return err;
         }
         if (!di.attr_set[slot]) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
             if (err != cudaSuccess) return err;
             di.attr_set[slot] = true;
         }
@@ -744,6 +1122,24 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
             return cudaErrorInvalidValue;
     }
 
+    // Scale blocks for the pair kernel: the tiled layout viewed as
+    // (256 B, 2 halves of a 512-byte atom, k atom, 128-row block).
+    CUtensorMap tmSFA, tmSFB;
+    if (PAIR) {
+        const uint64_t nka = static_cast<uint64_t>(pad_scale_cols(g.K) / 4);
+        uint64_t strides[3] = {256, 512, nka * 512};
+        {
+            uint64_t dims[4] = {256, 2, nka, static_cast<uint64_t>(pad_rows(g.M) / 128)};
+            uint32_t box[4] = {256, 2, 2, 1};
+            if (!encode_4d(&tmSFA, g.a_scales, dims, strides, box)) return cudaErrorInvalidValue;
+        }
+        {
+            uint64_t dims[4] = {256, 2, nka, static_cast<uint64_t>(pad_rows(g.N) / 128)};
+            uint32_t box[4] = {256, 2, 2, 2};
+            if (!encode_4d(&tmSFB, g.w_scales, dims, strides, box)) return cudaErrorInvalidValue;
+        }
+    }
+
     Params p;
     p.sfa = g.a_scales;
     p.sfb = g.w_scales;
@@ -768,7 +1164,7 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.dynamicSmemBytes = kAlloc;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -779,7 +1175,10 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
+    if constexpr (PAIR)
+        return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<STAGES>, tmA, tmB, tmY, tmSFA, tmSFB, p);
+    else
+        return cudaLaunchKernelEx(&cfg, gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>, tmA, tmB, tmY, p);
 }
 
 }  // namespace
@@ -807,7 +1206,7 @@ bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, co
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    uint32_t es[3] = {1, 1, 1};
+    uint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -818,7 +1217,7 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
     // (multicast) the B tile of adjacent m-blocks
     if (g.E > 0) return launch_impl<256, 4, 128, 1, true>(g, stream, 1);
-    return launch_impl<256, 4, 128, 2, false>(g, stream, 2);
+    return launch_impl<256, 6, 128, 2, false, true>(g, stream, 3);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)
