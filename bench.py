@@ -188,8 +188,67 @@ def oracle_linear_rate(d, rows: int, target_s: float):
     return flops / dt / 1e12, n, dt, threads
 
 
+def reference_arm_moe(args, rank: int, world: int):
+    """--impl reference on the MoE workload: each step runs the oracle's gate+up
+    projection (transform, MXFP4, fp64 GEMM) on the rows routed to one expert."""
+    if rank != 0:
+        return 0
+    import workloads
+    import oracle
+
+    d = workloads.make_moe(workloads.MOE if args.config == "moe" else workloads.MOE_SMALL)
+    wl = d["workload"]
+    r, cr = d["routing"], d["calib_routing"]
+    off, coff = r["offsets"].numpy(), cr["offsets"].numpy()
+    prepared = {}
+
+    def prep(e):
+        if e not in prepared:
+            xc = d["X_calib"][cr["row_src"][coff[e]:coff[e + 1]].long()]
+            s, inv = oracle.balance_scales(xc, d["W_gu"][e])
+            cw, sw = oracle.quantize(d["W_gu"][e], s)
+            prepared[e] = (inv, oracle.dequant(cw, sw))
+        return prepared[e]
+
+    n_steps = args.warmup + args.steps
+    for i in range(n_steps):
+        prep(i % wl.E)            # weight preparation: outside the timing
+
+    def step(i):
+        e = i % wl.E
+        inv, deq_w = prep(e)
+        X = d["X"][r["row_src"][off[e]:off[e + 1]].long()]
+        ca, sa = oracle.quantize(X, inv)
+        oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
+        return 2.0 * X.shape[0] * 2 * wl.F * wl.K
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    flops = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    sample = "gate+up projection of the rows routed to one expert per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (fp32 transform)", "data": "synthetic",
+        "config": moe_workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def reference_arm(args, rank: int, world: int):
     """--impl reference: the CPU oracle as it stands, rank 0 only."""
+    if args.config.startswith("moe"):
+        return reference_arm_moe(args, rank, world)
     if rank != 0:
         return 0
     import numpy as np  # noqa: F401
@@ -430,6 +489,231 @@ def gpu_arm(args, rank: int, world: int):
     return 0
 
 
+# ------------------------------------------------------------- MoE GPU arm
+
+def moe_workload_config(wl):
+    return {"workload": f"{wl.name}: {wl.T} tokens x top-{wl.topk} of {wl.E} experts = {wl.rows} rows; "
+                        f"gate+up K={wl.K} N={2 * wl.F}, down K={wl.F} N={wl.K}; bf16 in/out, MXFP4 W4A4",
+            "T": wl.T, "E": wl.E, "topk": wl.topk, "K": wl.K, "F": wl.F, "rows": wl.rows,
+            "l2": "weights (302 MB of codes) exceed L2; no input rotation needed"}
+
+
+def oracle_moe_rate(d, target_s: float):
+    """CPU oracle on the rows of a sample of experts (gate+up projection)."""
+    import numpy as np  # noqa: F401
+    import torch  # noqa: F401
+
+    import oracle
+
+    wl = d["workload"]
+    r, cr = d["routing"], d["calib_routing"]
+    off, coff = r["offsets"].numpy(), cr["offsets"].numpy()
+    done_flops, dt, experts = 0.0, 0.0, 0
+    for e in range(wl.E):
+        xc = d["X_calib"][cr["row_src"][coff[e]:coff[e + 1]].long()]
+        s, inv = oracle.balance_scales(xc, d["W_gu"][e])
+        cw, sw = oracle.quantize(d["W_gu"][e], s)
+        deq_w = oracle.dequant(cw, sw)           # weight preparation: outside the timing
+        X = d["X"][r["row_src"][off[e]:off[e + 1]].long()]
+        t0 = time.perf_counter()
+        ca, sa = oracle.quantize(X, inv)
+        oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
+        dt += time.perf_counter() - t0
+        done_flops += 2.0 * X.shape[0] * 2 * wl.F * wl.K
+        experts += 1
+        if dt > target_s:
+            break
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    return done_flops / dt / 1e12, experts, dt, threads
+
+
+def gpu_arm_moe(args, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    import w4a4_mxfp4_quantized_02_b300 as mq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mq.lib()
+    peaks = load_peaks()
+    d = workloads.make_moe(workloads.MOE if args.config == "moe" else workloads.MOE_SMALL)
+    wl = d["workload"]
+    E, K, F, rows = wl.E, wl.K, wl.F, wl.rows
+    stream = torch.cuda.current_stream()
+
+    # offline preparation (not timed): per-expert calibration and weight quantisation
+    r, cr = d["routing"], d["calib_routing"]
+    coff = cr["offsets"].numpy()
+    Xc = d["X_calib"].to(dev)
+    Xdc = d["Xd_calib"].to(dev)
+    c_rows = cr["row_src"].to(dev)
+    W = d["W_gu"].to(dev)
+    s_gu = torch.empty(E, K, dtype=torch.float32, device=dev)
+    inv_gu = torch.empty_like(s_gu)
+    for e in range(E):
+        s_gu[e], inv_gu[e] = mq.macaq_balance_scales(Xc, W[e], xc_rows=c_rows[coff[e]:coff[e + 1]])
+    wgu_codes, wgu_scales = mq.macaq_quant_weight_grouped(W, s_gu)
+    del W
+    W = d["W_down"].to(dev)
+    s_dn = torch.empty(E, F, dtype=torch.float32, device=dev)
+    inv_dn = torch.empty_like(s_dn)
+    for e in range(E):
+        s_dn[e], inv_dn[e] = mq.macaq_balance_scales(Xdc[coff[e]:coff[e + 1]], W[e])
+    wdn_codes, wdn_scales = mq.macaq_quant_weight_grouped(W, s_dn)
+    del W, Xc, Xdc
+
+    X = d["X"].to(dev)
+    Xd = d["Xd"].to(dev)
+    row_src = r["row_src"].to(dev)
+    ident = torch.arange(rows, dtype=torch.int32, device=dev)
+    offs = r["offsets"].to(dev)
+    P = mq.macaq_grouped_padded_rows(rows, E)
+    a_gu = torch.empty(P, K // 2, dtype=torch.uint8, device=dev)
+    as_gu = torch.empty(mq.macaq_scale_bytes(P, K), dtype=torch.uint8, device=dev)
+    a_dn = torch.empty(P, F // 2, dtype=torch.uint8, device=dev)
+    as_dn = torch.empty(mq.macaq_scale_bytes(P, F), dtype=torch.uint8, device=dev)
+    Ygu = torch.empty(rows, 2 * F, dtype=torch.bfloat16, device=dev)
+    Ydn = torch.empty(rows, K, dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mq.macaq_quant_act_grouped(X, row_src, offs, inv_gu, rows, E, a_gu, as_gu)
+        if ev is not None:
+            ev[1].record(stream)
+        mq.macaq_grouped_w4a4_gemm(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, 2 * F, K, Y=Ygu)
+        if ev is not None:
+            ev[2].record(stream)
+        mq.macaq_quant_act_grouped(Xd, ident, offs, inv_dn, rows, E, a_dn, as_dn)
+        if ev is not None:
+            ev[3].record(stream)
+        mq.macaq_grouped_w4a4_gemm(a_dn, as_dn, wdn_codes, wdn_scales, offs, rows, E, K, F, Y=Ydn)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error during warm-up: {mq.macaq_status_string(status)}")
+
+    every = max(1, args.kernel_events_every)
+    timed = [i for i in range(args.steps) if i % every == 0]
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)] for i in timed}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(pci_bus_id(dev))
+    with sampler:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        h0 = time.perf_counter()
+        for i in range(args.steps):
+            step(evs.get(i))
+        host_enqueue_s = time.perf_counter() - h0
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    avg = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs.values()) for j in range(4)]
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
+
+    flops = wl.flops_gate_up + wl.flops_down
+    value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    # algorithmic bytes: codes + scales of A and W, bf16 Y (the grouped GEMMs are
+    # bound by the weight bytes at this token count)
+    def gemm_bytes(n, k):
+        return rows * (k // 2 + k // 32) + E * n * (k // 2 + k // 32) + rows * n * 2
+    gu_bytes, dn_bytes = gemm_bytes(2 * F, K), gemm_bytes(K, F)
+    q_bytes = [rows * K * 2 + rows * (K // 2 + K // 32), rows * F * 2 + rows * (F // 2 + F // 32)]
+    gu_gbs = gu_bytes / (avg[1] * 1e-3) / 1e9
+    dn_gbs = dn_bytes / (avg[3] * 1e-3) / 1e9
+
+    # end to end through the C ABI: pinned host tokens in, pinned host down output out
+    e2e_steps = max(3, min(args.steps, 20))
+    Xh = d["X"].pin_memory()
+    Yh = torch.empty(rows, K, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        X.copy_(Xh, non_blocking=True)
+        step()
+        Yh.copy_(Ydn, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        X.copy_(Xh, non_blocking=True)
+        step()
+        Yh.copy_(Ydn, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            rate, experts, dt, threads = oracle_moe_rate(d, args.cpu_seconds)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"gate+up projection of the rows of {experts} of {E} experts, {dt:.1f} s; "
+                             "weight prepared outside the timing"}
+        except Exception as e:  # noqa: BLE001 - reported, not fatal
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
+                   "sample": f"failed: {e}"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
+        "data": "synthetic",
+        "config": moe_workload_config(wl),
+        "roofline": {"bound": "hbm", "kernel": "gemm_mxf4_kernel (grouped, gate+up)",
+                     "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gu_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "bytes_per_launch": gu_bytes, "avg_launch_us": avg[1] * 1e3,
+                     "tflops": wl.flops_gate_up / (avg[1] * 1e-3) / 1e12,
+                     "timing": f"CUDA events around the launch in {len(timed)} of the {args.steps} "
+                               "timed steps (includes the launch gap)"},
+        "down_gemm": {"achieved": dn_gbs, "unit": "GB/s", "frac": dn_gbs / peaks["hbm_gbs"],
+                      "bytes_per_launch": dn_bytes, "avg_launch_us": avg[3] * 1e3,
+                      "tflops": wl.flops_down / (avg[3] * 1e-3) / 1e12},
+        "act_quant": {"kernel": "quant_kernel<ActGrouped>",
+                      "achieved": [q_bytes[0] / (avg[0] * 1e-3) / 1e9, q_bytes[1] / (avg[2] * 1e-3) / 1e9],
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s (gate+up input, down input)",
+                      "frac": [q_bytes[0] / (avg[0] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               q_bytes[1] / (avg[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]],
+                      "bytes_per_launch": q_bytes, "avg_launch_us": [avg[0] * 1e3, avg[2] * 1e3]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": wl.T * K * 2, "d2h_bytes_per_step": rows * K * 2,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def kernel_source_sha() -> str:
     """Hash of the GEMM kernel sources: a recorded traffic figure is only used
     while the kernel it was measured on is unchanged."""
@@ -485,6 +769,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     try:
+        if args.config.startswith("moe"):
+            return gpu_arm_moe(args, rank, world)
         return gpu_arm(args, rank, world)
     finally:
         if world > 1:
