@@ -66,6 +66,19 @@ def test_gemm_random_scales(M, N, K, seed):
     check_gemm(bf16_to_np(Y), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
 
 
+@pytest.mark.parametrize("M,N,K,seed", [(8, 136, 32, 5), (17, 1000, 768, 6), (40, 296, 4096, 7),
+                                        (64, 5120, 5120, 8), (1, 520, 9216, 9), (33, 2048, 1280, 10)])
+def test_gemm_few_rows(M, N, K, seed):
+    """Up to 64 rows: weight rows on the MMA's M side, K split over a cluster of
+    CTAs when there are few weight tiles (partials added in rank order)."""
+    ca, sa, cw, sw = _rand_operands(M, N, K, seed, 110, 140)
+    Y = _gpu_gemm(ca, sa, cw, sw, M, N, K)
+    Y2 = _gpu_gemm(ca, sa, cw, sw, M, N, K)
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))  # run to run: same bits
+    da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+    check_gemm(bf16_to_np(Y), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
+
+
 ROWS = {"tiny": None, "decode_m1": None, "decode_m8": None, "decode_m16": None,
         "attn": None, "attn_qkv": 384, "down": 48}
 

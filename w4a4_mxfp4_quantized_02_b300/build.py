@@ -29,7 +29,7 @@ UNITS = {
     "api.cu": [],
     "static_scratch.cu": [],
 }
-HEADERS = ["internal.h", "ptx.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh"]
 
 
 def _mtime(path: str) -> float:

@@ -916,6 +916,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+#include "gemm_skinny.cuh"
+
 __global__ void wait_probe_kernel()
 {
     __shared__ alignas(8) uint64_t bar;
@@ -1212,8 +1214,86 @@ bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, co
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int NT, int STAGES>
+cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
+{
+    using L = skinny::Layout<NT, STAGES>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kern = skinny::gemm_mxf4_skinny_kernel<NT, STAGES>;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        DeviceInfo &di = g_dev[dev];
+        if (di.sms == 0) {
+            err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err != cudaSuccess) return err;
+        }
+        if (!di.attr_set[slot]) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+            if (err != cudaSuccess) return err;
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (err != cudaSuccess) return err;
+            di.attr_set[slot] = true;
+        }
+    }
+    const int sms = g_dev[dev].sms;
+    const uint64_t kb = static_cast<uint64_t>(g.K / 2);
+    CUtensorMap tmW, tmX;
+    {
+        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
+        uint64_t strides[1] = {kb};
+        uint32_t box[2] = {128, 128};
+        if (!encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.M)};
+        uint64_t strides[1] = {kb};
+        uint32_t box[2] = {128, NT};
+        if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    skinny::Params p;
+    p.sfw = g.w_scales;
+    p.sfx = g.a_scales;
+    p.Y = static_cast<uint16_t *>(g.Y);
+    p.ldy = g.ldy;
+    p.M = static_cast<int32_t>(g.M);
+    p.N = static_cast<int32_t>(g.N);
+    p.num_kstages = static_cast<int32_t>((g.K + 255) / 256);
+    p.nka = static_cast<int32_t>(pad_scale_cols(g.K) / 4);
+    // split K over a cluster while there are fewer weight tiles than SMs
+    const int64_t n_tiles = (g.N + 127) / 128;
+    int ks = 1;
+    while (n_tiles * ks < sms && ks < 8 && 2 * ks <= p.num_kstages) ks *= 2;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * ks));
+    cfg.blockDim = dim3(skinny::kThreads);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, p);
+}
+
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
 {
+    // a few token rows: weight rows on the MMA's M side (decode)
+    if (g.E == 0 && g.M <= 16) return launch_skinny<16, 4>(g, stream, 4);
+    if (g.E == 0 && g.M <= 32) return launch_skinny<32, 4>(g, stream, 5);
+    if (g.E == 0 && g.M <= 64) return launch_skinny<64, 4>(g, stream, 6);
     // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
     // (multicast) the B tile of adjacent m-blocks
     if (g.E > 0) return launch_impl<256, 4, 128, 1, true>(g, stream, 1);

@@ -623,6 +623,190 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
     }
 }
 
+// ------------------------------------------- TMA-staged grouped activations
+//
+// The expert-grouped activation transform (MoE): output row p of the
+// expert-padded layout takes token row row_src[offsets[e] + j] (e = the
+// expert whose padded range holds p, j = p - its first padded row) through
+// the transform with that expert's balance factors; padding rows get zero
+// scales and no codes.  The stage layout and the consumer are those of the
+// dense kernel; the producer lands each row of a stage with its own TMA box
+// (one row high), so the rows can come from anywhere in X.  The rows of this
+// CTA are resolved once, up front, into a table in shared memory.
+template <int STAGES>
+__global__ void __launch_bounds__(544, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                    QuantArgs a, int32_t groups, int32_t TB,
+                                                                    int32_t RT, int32_t per_cta)
+{
+    extern __shared__ uint8_t qsmem_raw[];
+    const uint32_t raw_base = ptx::smem_u32(qsmem_raw);
+    uint8_t *qsmem = qsmem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+    const uint32_t sbase = ptx::smem_u32(qsmem);
+    const int NC = TB * RT;
+    const int cwarps = NC / 32;
+    const uint32_t row_bytes = static_cast<uint32_t>(TB * 64);
+    const uint32_t stage_bytes = static_cast<uint32_t>(NC * 64);
+    const uint32_t full0 = sbase + STAGES * stage_bytes;
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    uint8_t *misc = qsmem + STAGES * stage_bytes + 16 * STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
+    int32_t *s_off = reinterpret_cast<int32_t *>(misc + 16);
+    int32_t *s_poff = s_off + (kMaxExperts + 1);
+    int32_t *m_src = s_poff + (kMaxExperts + 1);  // token row, -1 padding, -2 past the end
+    int32_t *m_exp = m_src + per_cta * RT;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int32_t slab0 = static_cast<int32_t>(blockIdx.x) * TB;
+
+    if (t == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(empty0 + 8 * s, static_cast<uint32_t>(cwarps));
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    for (int e = t; e <= a.E; e += blockDim.x) s_off[e] = a.offsets[e];
+    __syncthreads();
+    if (t == 0) {
+        int32_t acc = 0;
+        s_poff[0] = 0;
+        for (int e = 0; e < a.E; ++e) {
+            acc += (s_off[e + 1] - s_off[e] + 127) / 128 * 128;
+            s_poff[e + 1] = acc;
+        }
+    }
+    __syncthreads();
+
+    // a contiguous range of row groups per CTA: consecutive rows mostly share
+    // an expert, so the balance factors are reloaded rarely
+    const int32_t g0 = static_cast<int32_t>(blockIdx.y) * per_cta;
+    const int32_t my_groups = g0 < groups ? min(per_cta, groups - g0) : 0;
+    // row i of local group j is padded row (g0 + j) * RT + i
+    for (int idx = t; idx < my_groups * RT; idx += blockDim.x) {
+        const int j = idx / RT, i = idx - (idx / RT) * RT;
+        const int64_t p = (static_cast<int64_t>(g0) + j) * RT + i;
+        int32_t src = -2, ex = 0;
+        if (p < a.rows_out) {
+            src = -1;
+            if (p < s_poff[a.E]) {
+                int lo = 0, hi = a.E;  // s_poff[lo] <= p < s_poff[hi]
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_poff[mid] <= p) lo = mid; else hi = mid;
+                }
+                const int64_t jj = p - s_poff[lo];
+                ex = lo;
+                if (jj < s_off[lo + 1] - s_off[lo]) src = a.row_src[s_off[lo] + jj];
+            }
+        }
+        m_src[idx] = src;
+        m_exp[idx] = ex;
+    }
+    __syncthreads();
+
+    if (t >= NC) {
+        // ------------------------------------------------ producer warp
+        if (lane == 0) {
+            int32_t j = 0;
+            for (; j < my_groups; ++j) {
+                const int s = j % STAGES;
+                if (j >= STAGES && !quant_wait(empty0 + 8 * s, static_cast<uint32_t>(j / STAGES - 1) & 1u)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                uint32_t nvalid = 0;
+                for (int i = 0; i < RT; ++i) nvalid += m_src[j * RT + i] >= 0 ? 1u : 0u;
+                ptx::mbar_arrive_expect_tx(full0 + 8 * s, nvalid * row_bytes);
+                for (int i = 0; i < RT; ++i) {
+                    const int32_t src = m_src[j * RT + i];
+                    if (src < 0) continue;
+                    asm volatile(
+                        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(sbase + s * stage_bytes + i * row_bytes),
+                        "l"(&tmX), "r"(full0 + 8 * s), "r"(0), "r"(slab0), "r"(src)
+                        : "memory");
+                }
+            }
+            for (int32_t k = (j > STAGES ? j - STAGES : 0); k < j; ++k)
+                quant_wait(full0 + 8 * (k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int tx = t % TB, ty = t / TB;
+    const int64_t nkb = a.K / 32;
+    const int64_t nka = ((nkb + 7) / 8 * 8) / 4;
+    const int64_t nkb_pad = nka * 4;
+    const int64_t kb = static_cast<int64_t>(slab0) + tx;
+    const bool has_kb = kb < nkb;
+    const bool writes_scale = (lane & 3) == 0 && kb < nkb_pad;
+    float2 f[16];
+    int32_t cur_e = -1;
+    const uint32_t swz = (static_cast<uint32_t>(t) >> 1) & 3u;
+    const int64_t half_k = a.K / 2;
+
+    for (int32_t j = 0; j < my_groups; ++j) {
+        const int s = j % STAGES;
+        int ok = 1;
+        if (lane == 0) {
+            ok = quant_wait(full0 + 8 * s, static_cast<uint32_t>(j / STAGES) & 1u) ? 1 : 0;
+            if (!ok) *abort_flag = 1;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int32_t src = m_src[j * RT + ty];
+        const int32_t ex = m_exp[j * RT + ty];
+        const int64_t p = (static_cast<int64_t>(g0) + j) * RT + ty;
+        uint32_t sbyte = 0;
+        const bool valid = src >= 0 && has_kb;
+        uint32_t raw[16];
+        if (valid) {
+            const uint32_t base = sbase + s * stage_bytes + static_cast<uint32_t>(t) * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t x0, x1, x2, x3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                             : "r"(base + 16 * (c ^ swz)));
+                raw[4 * c] = x0;
+                raw[4 * c + 1] = x1;
+                raw[4 * c + 2] = x2;
+                raw[4 * c + 3] = x3;
+            }
+        }
+        // the stage is no longer needed by this warp once its reads are done
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
+        if (valid) {
+            if (ex != cur_e) {
+                cur_e = ex;
+                const float4 *f4 = reinterpret_cast<const float4 *>(a.f + static_cast<int64_t>(ex) * a.K + 32 * kb);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v4 = __ldg(f4 + q);
+                    f[2 * q] = make_float2(v4.x, v4.y);
+                    f[2 * q + 1] = make_float2(v4.z, v4.w);
+                }
+            }
+            uint4 codes;
+            sbyte = quant_block_pairs(raw, f, codes);
+            *reinterpret_cast<uint4 *>(a.codes + p * half_k + 16 * kb) = codes;
+        }
+        uint32_t word = sbyte << (8 * (lane & 3));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (writes_scale && src != -2) {
+            const int64_t off = ((p / 128) * nka + kb / 4) * 512 + (p % 32) * 16 + ((p % 128) / 32) * 4;
+            *reinterpret_cast<uint32_t *>(a.scales + off) = word;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- balance
 
 __global__ void __launch_bounds__(256) balance_kernel(const uint16_t *xc, int64_t ldxc,
@@ -747,6 +931,50 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t 
     return cudaGetLastError();
 }
 
+cudaError_t launch_quant_grouped_tma(const QuantArgs &a, int64_t tb, cudaStream_t stream, bool *done)
+{
+    *done = false;
+    const int64_t nkb = a.K / 32;
+    const int64_t nkb_pad = pad_scale_cols(a.K);
+    const int64_t slabs = (nkb_pad + tb - 1) / tb;
+    int64_t rt = 512 / tb;
+    rt = rt > 16 ? 16 : (rt < 1 ? 1 : rt);
+    const int64_t stage = tb * rt * 64;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t groups = (a.rows_out + rt - 1) / rt;
+    int64_t ctas_y = sms / slabs;
+    ctas_y = ctas_y < 1 ? 1 : ctas_y;
+    ctas_y = ctas_y > groups ? groups : ctas_y;
+    const int64_t per_cta = (groups + ctas_y - 1) / ctas_y;
+    ctas_y = (groups + per_cta - 1) / per_cta;
+    const int64_t max_rows = per_cta * rt;
+    if (max_rows > 4096) return cudaSuccess;  // row table too large: register-staged kernel
+    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 2 * max_rows * 4 + 1024;
+    const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : 4;
+    const int64_t smem = stages * stage + 16 * stages + fixed;
+    if (smem > 200 * 1024) return cudaSuccess;
+    CUtensorMap tm;
+    // the token rows are whatever row_src names (valid by contract): no row bound
+    const uint64_t dims[3] = {32, static_cast<uint64_t>(nkb), 0x7fffffffull};
+    const uint64_t strides[2] = {64, static_cast<uint64_t>(a.ld_src) * 2};
+    const uint32_t box[3] = {32, static_cast<uint32_t>(tb), 1};
+    if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaSuccess;
+    auto kern = stages == 6 ? quant_grouped_tma_kernel<6> : quant_grouped_tma_kernel<4>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
+    dim3 block(static_cast<unsigned>(tb * rt + 32));
+    MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
+                              static_cast<int32_t>(groups), static_cast<int32_t>(tb), static_cast<int32_t>(rt),
+                              static_cast<int32_t>(per_cta)));
+    *done = true;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream)
 {
     const int64_t nkb_pad = pad_scale_cols(a.K);
@@ -765,6 +993,12 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
     if (mode == QuantMode::Dense && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
         bool done = false;
         cudaError_t err = launch_quant_dense_tma(a, best_t, stream, &done);
+        if (err != cudaSuccess || done) return err;
+    }
+    if (mode == QuantMode::ActGrouped && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1 &&
+        best_t % 8 == 0) {
+        bool done = false;
+        cudaError_t err = launch_quant_grouped_tma(a, best_t, stream, &done);
         if (err != cudaSuccess || done) return err;
     }
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
