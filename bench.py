@@ -365,13 +365,10 @@ def gpu_arm(args, rank: int, world: int):
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error during warm-up: {mq.macaq_status_string(status)}")
-
-    # Per-kernel events bracket the two launches of every `every`-th step only:
-    # an event between two kernels stops the second from starting its set-up
-    # while the first finishes (programmatic dependent launch), so bracketing
-    # every step would slow the step being measured.
-    every = max(1, args.kernel_events_every)
-    timed = [i for i in range(args.steps) if i % every == 0]
+    chunk = nsets * max(1, math.ceil(8 / nsets))
+    graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
+    plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
+    timed = plan.event_steps
     evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in timed}
     if world > 1:
         dist.barrier()
@@ -382,7 +379,9 @@ def gpu_arm(args, rank: int, world: int):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         h0 = time.perf_counter()
-        for i in range(args.steps):
+        for _ in range(plan.replays):
+            graph.replay()
+        for i in plan.eager_steps:
             step(i, evs.get(i))
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
@@ -483,6 +482,7 @@ def gpu_arm(args, rank: int, world: int):
                 "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
+        "launch": plan.describe(),
         "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -599,9 +599,10 @@ def gpu_arm_moe(args, rank: int, world: int):
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error during warm-up: {mq.macaq_status_string(status)}")
-
-    every = max(1, args.kernel_events_every)
-    timed = [i for i in range(args.steps) if i % every == 0]
+    chunk = 4
+    graph = None if args.no_graphs else capture_graph(lambda: [step() for _ in range(chunk)])
+    plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
+    timed = plan.event_steps
     evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)] for i in timed}
     if world > 1:
         dist.barrier()
@@ -612,7 +613,9 @@ def gpu_arm_moe(args, rank: int, world: int):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         h0 = time.perf_counter()
-        for i in range(args.steps):
+        for _ in range(plan.replays):
+            graph.replay()
+        for i in plan.eager_steps:
             step(evs.get(i))
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
@@ -708,10 +711,56 @@ def gpu_arm_moe(args, rank: int, world: int):
                 "ms_per_step": e2e_ms},
         "gpu_launches": 4 * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
+        "launch": plan.describe(),
         "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+class StepPlan:
+    """How the timed steps run.  Per-kernel CUDA events bracket the launches of
+    about one step in `every`: an event between two kernels stops the second
+    from starting its set-up while the first finishes (programmatic dependent
+    launch), so they are kept off most steps.  With a captured graph of `chunk`
+    steps, the unbracketed steps run as whole-graph replays (the host's launch
+    cost then does not pace short steps) and the rest, all bracketed, eagerly."""
+
+    def __init__(self, steps: int, every: int, chunk: int):
+        every = max(1, every)
+        n_events = (steps + every - 1) // every
+        if chunk > 0:
+            self.replays = (steps - n_events) // chunk
+            first = self.replays * chunk
+            self.eager_steps = list(range(first, steps))
+            self.event_steps = list(self.eager_steps)
+        else:
+            self.replays = 0
+            self.eager_steps = list(range(steps))
+            self.event_steps = [i for i in range(steps) if i % every == 0]
+        self.chunk = chunk
+
+    def describe(self) -> str:
+        if self.replays:
+            return (f"{self.replays} replays of a CUDA graph of {self.chunk} steps, then "
+                    f"{len(self.eager_steps)} eager steps with per-kernel events")
+        return f"eager launches; per-kernel events on {len(self.event_steps)} steps"
+
+
+def capture_graph(fn):
+    """Capture fn (a run of whole steps: their kernels and the programmatic
+    dependencies between them) into one CUDA graph and check one replay."""
+    import torch
+    import w4a4_mxfp4_quantized_02_b300 as mq
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error in a graph replay: {mq.macaq_status_string(status)}")
+    return g
 
 
 def kernel_source_sha() -> str:
@@ -753,6 +802,8 @@ def main():
     ap.add_argument("--config", default="attn")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch every step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--kernel-events-every", type=int, default=4,
                     help="bracket the kernels of every n-th timed step with CUDA events")
     ap.add_argument("--probe", choices=["mma"], help="print a hardware probe table and exit")

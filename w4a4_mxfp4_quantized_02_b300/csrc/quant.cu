@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -894,6 +895,46 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Per-device facts the launches need, queried once: the SM count, and the
+// dynamic shared memory each TMA kernel variant has been opened up to.
+struct QuantDevice {
+    int sms = 0;
+    int smem_set[4] = {0, 0, 0, 0};
+};
+QuantDevice g_qdev[64];
+std::mutex g_qdev_mu;
+
+cudaError_t quant_device(int *sms)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_qdev_mu);
+    if (g_qdev[dev].sms == 0) {
+        err = cudaDeviceGetAttribute(&g_qdev[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+    }
+    *sms = g_qdev[dev].sms;
+    return cudaSuccess;
+}
+
+template <typename Kern>
+cudaError_t open_smem(Kern kern, int slot, int64_t smem)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_qdev_mu);
+    if (g_qdev[dev].smem_set[slot] < smem) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        g_qdev[dev].smem_set[slot] = static_cast<int>(smem);
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t stream, bool *done)
 {
     *done = false;
@@ -913,16 +954,14 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t 
     if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 148;
+    MACAQ_TRY_CUDA(quant_device(&sms));
     const int64_t groups = (a.rows_out + rt - 1) / rt;
     int64_t ctas_y = sms / slabs;  // one CTA per SM: never a partial second wave
     ctas_y = ctas_y < 1 ? 1 : ctas_y;
     ctas_y = ctas_y > groups ? groups : ctas_y;
     auto kern = stages == 6 ? quant_dense_tma_kernel<6> : quant_dense_tma_kernel<4>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
+    MACAQ_TRY_CUDA(open_smem(kern, stages == 6 ? 0 : 1, smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -940,9 +979,8 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, int64_t tb, cudaStream_
     int64_t rt = 512 / tb;
     rt = rt > 16 ? 16 : (rt < 1 ? 1 : rt);
     const int64_t stage = tb * rt * 64;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 148;
+    MACAQ_TRY_CUDA(quant_device(&sms));
     const int64_t groups = (a.rows_out + rt - 1) / rt;
     int64_t ctas_y = sms / slabs;
     ctas_y = ctas_y < 1 ? 1 : ctas_y;
@@ -964,8 +1002,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, int64_t tb, cudaStream_
                            CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaSuccess;
     auto kern = stages == 6 ? quant_grouped_tma_kernel<6> : quant_grouped_tma_kernel<4>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
+    MACAQ_TRY_CUDA(open_smem(kern, stages == 6 ? 2 : 3, smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -1003,9 +1040,8 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
     }
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 148;
+    MACAQ_TRY_CUDA(quant_device(&sms));
     const int64_t target_ctas = static_cast<int64_t>(sms) * 8;
     int64_t rows_per_cta = (a.rows_out * slabs + target_ctas - 1) / target_ctas;
     rows_per_cta = rows_per_cta < 2 ? 2 : rows_per_cta;
