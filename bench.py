@@ -451,6 +451,27 @@ def gpu_arm(args, rank: int, world: int):
             cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
                    "sample": f"failed: {e}"}
 
+    # the GEMM's bound: FP4 tensor throughput above the ridge intensity, HBM
+    # bytes below it (decode: the weight bytes)
+    gemm_bytes = M * (K // 2 + K // 32) + N * (K // 2 + K // 32) + M * N * 2
+    timing = (f"CUDA events around the launch in {len(timed)} of the {args.steps} timed steps "
+              "(includes the launch gap)")
+    if flops / gemm_bytes >= fp4_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
+        roofline = {"bound": "tensor", "kernel": "gemm_mxf4_pair_kernel",
+                    "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
+                    "frac": gemm_tflops / fp4_peak, "traffic": traffic,
+                    "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x "
+                                 f"{FP4_OVER_BF16:g} (nominal fp4/bf16)",
+                    "avg_launch_us": gemm_avg * 1e3, "timing": timing}
+    else:
+        gbs = gemm_bytes / (gemm_avg * 1e-3) / 1e9
+        roofline = {"bound": "hbm",
+                    "kernel": "gemm_mxf4_skinny_kernel" if M <= 64 else "gemm_mxf4_pair_kernel",
+                    "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": gemm_bytes,
+                    "peak_note": f"{peaks['source']} HBM copy bandwidth",
+                    "tflops": gemm_tflops, "avg_launch_us": gemm_avg * 1e3, "timing": timing}
+
     line = {
         "metric": METRIC,
         "value": value,
@@ -465,14 +486,7 @@ def gpu_arm(args, rank: int, world: int):
         "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
         "data": "synthetic",
         "config": workload_config(wl),
-        "roofline": {"bound": "tensor", "kernel": "gemm_mxf4_pair_kernel",
-                     "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp4_peak, "traffic": traffic,
-                     "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x "
-                                  f"{FP4_OVER_BF16:g} (nominal fp4/bf16)",
-                     "avg_launch_us": gemm_avg * 1e3,
-                     "timing": f"CUDA events around the launch in {len(timed)} of the {args.steps} "
-                               "timed steps (includes the launch gap)"},
+        "roofline": roofline,
         "act_quant": {"kernel": "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
@@ -639,7 +653,9 @@ def gpu_arm_moe(args, rank: int, world: int):
     def gemm_bytes(n, k):
         return rows * (k // 2 + k // 32) + E * n * (k // 2 + k // 32) + rows * n * 2
     gu_bytes, dn_bytes = gemm_bytes(2 * F, K), gemm_bytes(K, F)
-    q_bytes = [rows * K * 2 + rows * (K // 2 + K // 32), rows * F * 2 + rows * (F // 2 + F // 32)]
+    # algorithmic bytes: each token row read once (its eight expert copies are
+    # gathered from L2), every sorted row's codes and scales written once
+    q_bytes = [wl.T * K * 2 + rows * (K // 2 + K // 32), rows * F * 2 + rows * (F // 2 + F // 32)]
     gu_gbs = gu_bytes / (avg[1] * 1e-3) / 1e9
     dn_gbs = dn_bytes / (avg[3] * 1e-3) / 1e9
 
