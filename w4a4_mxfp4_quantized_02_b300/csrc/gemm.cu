@@ -117,6 +117,8 @@ struct Params {
     int32_t num_mb;
     int32_t num_nb;
     int32_t n_rb;
+    int32_t num_full;   // pair kernel: whole 256-column tiles run first ...
+    int32_t num_split;  // ... then the last num_split tiles as two 128-column halves
 };
 
 struct Tile {
@@ -125,6 +127,7 @@ struct Tile {
     int32_t expert;
     int32_t y_row0;     // first output row
     int32_t rows_valid; // rows of this tile that exist in Y
+    int32_t ncols;      // pair kernel: 256, or 128 for half of a split tile
 };
 
 // Wait for the phase of `bar` with parity `parity`.  Each poll lets the
@@ -619,8 +622,9 @@ struct PairLayout {
 template <int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSFA,
-                          const __grid_constant__ CUtensorMap tmSFB, const Params p)
+                          const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmY,
+                          const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                          const Params p)
 {
     using L = PairLayout<STAGES>;
     constexpr int BN = L::BN;
@@ -675,7 +679,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     griddep_wait();
 
     const int32_t num_mp = (p.M + 2 * BM - 1) / (2 * BM);
-    const int64_t total_units = static_cast<int64_t>(num_mp) * p.num_nb;
+    const int64_t total_units = static_cast<int64_t>(p.num_full) + 2 * static_cast<int64_t>(p.num_split);
     const int nks = p.num_kstages;
     // scale atoms of stage st -> its tensor-memory slot (A: atom `at` at column
     // 4*at; B: atom `at` of row block r at 4*(2*at + r)), in both CTAs
@@ -693,12 +697,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_cp_pair_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r, db + (r * L::KATOMS + at) * kAtom);
         }
     };
-    // unit u: pair m-block u % num_mp (m fastest), n-block u / num_mp
+    // Tiles t run over (pair m-block t % num_mp (m fastest), n-block t / num_mp).
+    // Units 0 .. num_full-1 are whole tiles; when the tiles do not fill the
+    // last round of pairs, the remaining num_split tiles run as two units of
+    // 128 columns each, so the last round takes about half as long.
     auto tile_of = [&](int64_t u, Tile &ti) {
-        const int32_t mp = static_cast<int32_t>(u % num_mp);
-        const int32_t nb = static_cast<int32_t>(u / num_mp);
+        int64_t t = u;
+        int32_t half = -1;
+        if (u >= p.num_full) {
+            t = p.num_full + (u - p.num_full) / 2;
+            half = static_cast<int32_t>((u - p.num_full) & 1);
+        }
+        const int32_t mp = static_cast<int32_t>(t % num_mp);
+        const int32_t nb = static_cast<int32_t>(t / num_mp);
         ti.a_row = mp * 2 * BM + static_cast<int32_t>(rank) * BM;
-        ti.n0 = nb * BN;
+        ti.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
+        ti.ncols = half < 0 ? BN : BN / 2;
         ti.expert = 0;
         ti.y_row0 = ti.a_row;
         ti.rows_valid = min(BM, p.M - ti.a_row);
@@ -711,6 +725,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // tensor are filled with zeros), so each CTA lands the same bytes
             // per stage.  Rows of A / B past the end are never stored.
             constexpr uint32_t kStageBytes = L::A_STAGE + L::B_STAGE + L::SFA_STAGE + L::SFB_STAGE;
+            constexpr uint32_t kHalfBytes = kStageBytes - L::B_STAGE / 2;
             const uint32_t full0 = mapa_shared(full_bar(0), 0);
             uint32_t it = 0;
             uint32_t issued = 0;
@@ -720,6 +735,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tile_of(u, ti);
                 const int32_t a_rb = ti.a_row / BM;
                 const int32_t n_rb0 = ti.n0 / 128;
+                const bool whole = ti.ncols == BN;
                 bool ok = true;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     const int s = static_cast<int>(it % STAGES);
@@ -731,10 +747,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     MACAQ_TRACE(1, it);
                     const uint32_t fb = full0 + 8u * s;
-                    if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * kStageBytes);
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * (whole ? kStageBytes : kHalfBytes));
                     tma_load_2d_pair(sbase + L::OFF_A + s * L::A_STAGE, &tmA, fb, ks * KB, ti.a_row);
-                    tma_load_2d_pair(sbase + L::OFF_B + s * L::B_STAGE, &tmB, fb, ks * KB,
-                                     ti.n0 + static_cast<int32_t>(rank) * (BN / 2));
+                    // this CTA's half of the tile's columns (64 of a 128-column unit)
+                    tma_load_2d_pair(sbase + L::OFF_B + s * L::B_STAGE, whole ? &tmB : &tmB64, fb, ks * KB,
+                                     ti.n0 + static_cast<int32_t>(rank) * (ti.ncols / 2));
                     // scale blocks: (256 B, 2, k atom, 128-row block) views of the tiled layout
                     tma_load_4d_pair(sbase + L::OFF_SFA + s * L::SFA_STAGE, &tmSFA, fb, 0, 0,
                                      L::KATOMS * ks, a_rb);
@@ -763,11 +780,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t b_desc0 = smem_desc(sbase + L::OFF_B, 16, 8 * KB, kSwizzle128B);
             const uint32_t idesc0 = idesc_mxf4(2 * BM, BN, 0, 0);
             const uint32_t idesc2 = idesc_mxf4(2 * BM, BN, 2, 2);
+            const uint32_t hdesc0 = idesc_mxf4(2 * BM, BN / 2, 0, 0);
+            const uint32_t hdesc2 = idesc_mxf4(2 * BM, BN / 2, 2, 2);
             const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
             constexpr uint32_t kAStep = L::A_STAGE >> 4, kBStep = L::B_STAGE >> 4;
             uint32_t st = 0, ph = 0, tc = 0;
             bool ok = true;
             for (int64_t u = first_unit; u < total_units && ok; u += unit_stride, ++tc) {
+                const bool whole = u < p.num_full;
+                const uint32_t d0 = whole ? idesc0 : hdesc0, d2 = whole ? idesc2 : hdesc2;
                 for (int ks = 0; ks < nks; ++ks) {
                     MACAQ_TRACE(2, tc * nks + ks);
                     if (!wait_bounded(ready_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) {
@@ -791,7 +812,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint64_t bd = b_desc0 + st * kBStep;
 #pragma unroll
                     for (int j = 0; j < L::KSTEPS; ++j)
-                        tc_mma_mxf4_pair(tmem, ad + 2 * j, bd + 2 * j, (j & 1) ? idesc2 : idesc0,
+                        tc_mma_mxf4_pair(tmem, ad + 2 * j, bd + 2 * j, (j & 1) ? d2 : d0,
                                          sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
                                          (ks > 0 || j > 0) ? 1u : 0u);
                     // the stage's buffers in both CTAs may be refilled once these MMAs read them
@@ -861,7 +882,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
             const int row0 = 32 * q;
             const bool any_row = row0 < ti.rows_valid;
-            if (!any_row) continue;
+            if (!any_row || half * 128 >= ti.ncols) continue;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int32_t ncol = ti.n0 + half * 128 + 16 * c;
@@ -1124,6 +1145,15 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
             return cudaErrorInvalidValue;
     }
 
+    // B boxes of 64 rows for the 128-column halves of split tiles
+    CUtensorMap tmB64;
+    if (PAIR) {
+        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
+        uint64_t strides[1] = {kb};
+        uint32_t box[2] = {KB, 64};
+        if (!encode(&tmB64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box, kMapSwizzle))
+            return cudaErrorInvalidValue;
+    }
     // Scale blocks for the pair kernel: the tiled layout viewed as
     // (256 B, 2 halves of a 512-byte atom, k atom, 128-row block).
     CUtensorMap tmSFA, tmSFB;
@@ -1158,8 +1188,21 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
 
-    const int64_t units = GROUPED ? (g.a_rows / BM) * p.num_nb
-                                  : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
+    int64_t units = GROUPED ? (g.a_rows / BM) * p.num_nb
+                            : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
+    p.num_full = static_cast<int32_t>(units);
+    p.num_split = 0;
+    if (PAIR) {
+        // tiles that would run in a last, partly filled round of pairs run as
+        // two 128-column halves instead (when the halves fit in that round)
+        const int64_t pairs = sms / 2;
+        const int64_t rem = units % pairs;
+        if (rem > 0 && 2 * rem <= pairs) {
+            p.num_full = static_cast<int32_t>(units - rem);
+            p.num_split = static_cast<int32_t>(rem);
+            units += rem;
+        }
+    }
     int64_t clusters = units < sms / CLUSTER ? units : sms / CLUSTER;
     if (clusters < 1) clusters = 1;
 
@@ -1178,7 +1221,7 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if constexpr (PAIR)
-        return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<STAGES>, tmA, tmB, tmY, tmSFA, tmSFB, p);
+        return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<STAGES>, tmA, tmB, tmB64, tmY, tmSFA, tmSFB, p);
     else
         return cudaLaunchKernelEx(&cfg, gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>, tmA, tmB, tmY, p);
 }
