@@ -429,9 +429,10 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
     float2 v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float a = __fmul_rn(bf16lo(raw[i]), f[i].x);
-        const float b = __fmul_rn(bf16hi(raw[i]), f[i].y);
-        v[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+        // one packed multiply for the pair; the stride-1 stage that consumes it
+        // is scalar, so no packed add follows a packed multiply here
+        const float2 ab = __fmul2_rn(make_float2(bf16lo(raw[i]), bf16hi(raw[i])), f[i]);
+        v[i] = make_float2(__fadd_rn(ab.x, ab.y), __fsub_rn(ab.x, ab.y));
     }
 #pragma unroll
     for (int hh = 1; hh < 16; hh <<= 1) {
