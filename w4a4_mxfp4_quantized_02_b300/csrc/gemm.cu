@@ -6,16 +6,16 @@
 // inference mode; routed MoE experts run W4A4).  Y = A . Wq^T with both
 // operands E2M1 codes scaled per 32 elements by E8M0 powers of two.
 //
-// Two persistent kernels, one CTA per SM, warp-specialised:
-//   gemm_mxf4_pair_kernel   dense Y: CTA pairs (tcgen05 cta_group::2) on
-//                           256 x 256 tiles; see the comment at the kernel.
-//   gemm_mxf4_kernel        grouped (MoE) Y: one CTA per 128 x 256 tile of
-//                           one expert's rows.
-// Common shape (352 threads):
-//   warp 0      TMA producer: per 256-wide K stage, the A tile (128 rows x
-//               128 B), the B tile, both 128B-swizzled, and the scale tiles
-//               (512-byte atoms), into a ring of STAGES shared-memory buffers
-//               guarded by mbarriers.
+// Kernels, warp-specialised, one CTA per SM:
+//   gemm_mxf4_pair_kernel   dense and expert-grouped Y: persistent CTA pairs
+//                           (tcgen05 cta_group::2) on 256 x 256 tiles; see the
+//                           comment at the kernel.
+//   gemm_mxf4_skinny_kernel up to 64 token rows (decode): weight rows on the
+//                           MMA's M side; gemm_skinny.cuh.
+// Common shape:
+//   warp 0      TMA producer: per 256-wide K stage, A and B tiles (128-byte
+//               rows, 128B-swizzled) and the scale tiles (512-byte atoms) into
+//               a ring of STAGES shared-memory buffers guarded by mbarriers.
 //   warp 1      MMA issuer (one thread): tcgen05.mma.kind::mxf4.block_scale
 //               (K = 64 per instruction) accumulating in tensor memory;
 //               tcgen05.commit frees the stage.
@@ -23,10 +23,8 @@
 //               atoms into tensor memory, committed to "scales ready".  In
 //               the MMA thread these copies would stall the tensor pipe: a
 //               barrier wait issued after them waits for them to finish.
-//   warps 3..10 epilogue: tcgen05.ld of the fp32 accumulator (each warp 32
-//               lanes x 128 columns, all in registers), release of the
-//               accumulator, then bf16 rounding and TMA stores of 32 x 16
-//               boxes.
+//   epilogue    tcgen05.ld of the fp32 accumulator into registers, release of
+//               the accumulator, bf16 rounding and stores.
 // Every mbarrier wait is bounded in time; a wait that runs out sets a device
 // error flag and the CTA leaves in order (drains its copies and MMAs, frees
 // tensor memory).
@@ -70,55 +68,18 @@ constexpr unsigned kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain
 constexpr uint64_t kDrainNs = 2000000000ull;
 constexpr uint32_t kPollHintNs = 20000;  // longest hardware sleep per poll
 
-// Shared-memory plan of one CTA.  KB = bytes of each operand row per
-// pipeline stage (128: 256 fp4 values, 128-byte swizzle; 64: 128 values,
-// 64-byte swizzle); one stage holds KB/64 scale atoms per 128 rows.
-template <int BN, int STAGES, int KB>
-struct Layout {
-    static_assert(KB == 64 || KB == 128, "stage rows are 64 or 128 bytes");
-    static constexpr int KATOMS = KB / 64;     // 4-scale atoms (128 values) per stage
-    static constexpr int KSTEPS = KB / 32;     // MMAs (K = 64 values) per stage
-    static constexpr int A_STAGE = BM * KB;
-    static constexpr int B_STAGE = BN * KB;
-    static constexpr int SFA_STAGE = KATOMS * SF_ATOM;
-    static constexpr int SFB_STAGE = (BN / 128) * KATOMS * SF_ATOM;
-    static constexpr int SF_COLS = 4 * KATOMS + 4 * KATOMS * (BN / 128);  // tensor-memory columns per stage
-    static constexpr uint32_t SWZ_DESC = KB == 128 ? kSwizzle128B : kSwizzle64B;
-    static constexpr uint32_t SWZ_SBO = 8 * KB;  // bytes between 8-row groups
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
-    static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * 2 * EPI_BUF;
-    static constexpr int NUM_BARS = 3 * STAGES + 4;
-    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int OFF_OFFS = OFF_MISC + 16;
-    static constexpr int BYTES = OFF_OFFS + 2 * (static_cast<int>(kMaxExperts) + 1) * 4;
-    static constexpr int ALLOC = BYTES + 1024;
-    static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
-    static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
-    static_assert(BN <= SF_TMEM_BASE, "accumulator overlaps scale columns");
-    static_assert(ALLOC <= 232448, "shared memory");
-};
-
 struct Params {
-    const uint8_t *sfa;
-    const uint8_t *sfb;
-    size_t sfb_expert_stride;
-    const int32_t *offsets;
+    const int32_t *offsets;  // grouped: expert row offsets [E+1]
     uint16_t *Y;
     int64_t ldy;
     int32_t E;
-    int32_t M;
+    int32_t M;               // rows of Y (grouped: sorted rows)
     int32_t N;
-    int32_t num_kstages;
-    int32_t nka;
-    int32_t num_mb;
-    int32_t num_nb;
-    int32_t n_rb;
-    int32_t num_full;   // pair kernel: whole 256-column tiles run first ...
-    int32_t num_split;  // ... then the last num_split tiles as two 128-column halves
+    int32_t num_kstages;     // 256-wide K stages
+    int32_t num_nb;          // 256-column blocks
+    int32_t n_rb;            // 128-row scale blocks of one weight
+    int32_t num_full;        // whole 256-column tiles run first ...
+    int32_t num_split;       // ... then the last num_split tiles as two 128-column halves
 };
 
 struct Tile {
@@ -127,7 +88,7 @@ struct Tile {
     int32_t expert;
     int32_t y_row0;     // first output row
     int32_t rows_valid; // rows of this tile that exist in Y
-    int32_t ncols;      // pair kernel: 256, or 128 for half of a split tile
+    int32_t ncols;      // 256, or 128 for half of a split tile
 };
 
 // Wait for the phase of `bar` with parity `parity`.  Each poll lets the
@@ -174,402 +135,6 @@ __device__ __forceinline__ bool wait_fixed(uint32_t bar, uint32_t parity)
     }
 }
 
-// Work unit u -> the tile of this CTA.  Dense: units run over (m-group, n)
-// with m fastest; a cluster of CLUSTER CTAs takes one unit and CTA rank r
-// computes m-block CLUSTER*mg + r (the CTAs share the B tile).  Grouped: one
-// CTA per unit over (padded m-block, n), m fastest.
-template <int BN, int CLUSTER, bool GROUPED>
-__device__ __forceinline__ void decode_tile(int64_t u, uint32_t rank, const Params &p,
-                                            const int32_t *s_off, const int32_t *s_pmb, Tile &ti)
-{
-    if (!GROUPED) {
-        const int32_t num_mg = (p.num_mb + CLUSTER - 1) / CLUSTER;
-        const int32_t mg = static_cast<int32_t>(u % num_mg);
-        const int32_t nb = static_cast<int32_t>(u / num_mg);
-        const int32_t mb = mg * CLUSTER + static_cast<int32_t>(rank);
-        ti.a_row = mb * BM;
-        ti.n0 = nb * BN;
-        ti.expert = 0;
-        ti.y_row0 = mb * BM;
-        ti.rows_valid = min(BM, p.M - mb * BM);  // <= 0 for an m-block past the end
-    } else {
-        const int32_t total_mb = s_pmb[p.E];
-        const int32_t mb = static_cast<int32_t>(u % total_mb);
-        const int32_t nb = static_cast<int32_t>(u / total_mb);
-        int lo = 0, hi = p.E;  // s_pmb[lo] <= mb < s_pmb[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_pmb[mid] <= mb) lo = mid; else hi = mid;
-        }
-        const int32_t j = mb - s_pmb[lo];
-        const int32_t cnt = s_off[lo + 1] - s_off[lo];
-        ti.a_row = mb * BM;
-        ti.n0 = nb * BN;
-        ti.expert = lo;
-        ti.y_row0 = s_off[lo] + j * BM;
-        ti.rows_valid = min(BM, cnt - j * BM);
-    }
-}
-
-template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmY, const Params p)
-{
-    static_assert(CLUSTER == 1 || (CLUSTER == 2 && !GROUPED), "clusters pair dense m-blocks");
-    using L = Layout<BN, STAGES, KB>;
-    constexpr int A_STAGE = L::A_STAGE;
-    constexpr int B_PART = L::B_STAGE / CLUSTER;  // bytes of B each CTA loads per stage
-    constexpr uint16_t kAll = (1u << CLUSTER) - 1u;
-    extern __shared__ uint8_t smem_raw[];
-    // 1 KB alignment of the shared-window address (128B-swizzled tiles need it)
-    const uint32_t raw_base = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_base = sbase + L::OFF_BAR;
-    auto full_bar = [&](int s) { return bar_base + 8u * s; };
-    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-    auto ready_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };  // scales in TMEM
-    const uint32_t acc_full = bar_base + 8u * (3 * STAGES);
-    const uint32_t acc_empty = acc_full + 8u;
-    const uint32_t drain_bar = acc_full + 16u;
-    const uint32_t drain_bar2 = acc_full + 24u;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
-    int32_t *s_off = reinterpret_cast<int32_t *>(smem + L::OFF_OFFS);
-    int32_t *s_pmb = s_off + (kMaxExperts + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    MACAQ_TRACE_EDGE(0);
-    const uint64_t wait_ns = g_wait_ns;
-    const uint32_t rank = (CLUSTER > 1) ? cluster_ctarank() : 0u;
-    const int64_t first_unit = blockIdx.x / CLUSTER;
-    const int64_t unit_stride = gridDim.x / CLUSTER;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CLUSTER);  // one MMA commit from every CTA of the cluster
-            mbar_init(ready_bar(s), 1);
-        }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, NUM_EPI_WARPS);
-        mbar_init(drain_bar, 1);
-        mbar_init(drain_bar2, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (GROUPED) {
-        griddep_wait();  // expert offsets may come from the previous kernel
-        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int32_t acc = 0;
-            s_pmb[0] = 0;
-            for (int e = 0; e < p.E; ++e) {
-                acc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
-                s_pmb[e + 1] = acc;
-            }
-        }
-    }
-    if (warp == 1) {
-        tmem_alloc(sbase + L::OFF_MISC, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    // peers may signal our barriers only once they are initialised
-    if (CLUSTER > 1) cluster_sync(); else __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // Everything above only touched this CTA's own resources.  The next kernel
-    // may now start its own set-up; this one waits for the previous kernel
-    // (producer of A, reader of Y) before touching global memory.
-    griddep_launch_dependents();
-    griddep_wait();
-
-    const int64_t total_units =
-        GROUPED ? static_cast<int64_t>(s_pmb[p.E]) * p.num_nb
-                : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
-    const int nks = p.num_kstages;
-    const int64_t my_units =
-        first_unit < total_units ? (total_units - 1 - first_unit) / unit_stride + 1 : 0;
-    const uint32_t total_stages = static_cast<uint32_t>(my_units) * static_cast<uint32_t>(nks);
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            uint32_t it = 0;
-            uint32_t issued = 0;  // bit s: stage s has had a load issued
-            uint32_t last_parity = 0;
-            for (int64_t u = first_unit; u < total_units; u += unit_stride) {
-                Tile ti;
-                decode_tile<BN, CLUSTER, GROUPED>(u, rank, p, s_off, s_pmb, ti);
-                const int32_t n_rb0 = ti.n0 / 128;
-                const int32_t sfb_valid = min(BN / 128, p.n_rb - n_rb0);
-                const bool a_valid = ti.rows_valid > 0;
-                const uint8_t *sfb = p.sfb + static_cast<size_t>(ti.expert) * p.sfb_expert_stride;
-                const uint32_t bytes = A_STAGE + L::B_STAGE + (a_valid ? L::SFA_STAGE : 0) +
-                                       sfb_valid * L::KATOMS * SF_ATOM;
-                bool ok = true;
-                for (int ks = 0; ks < nks; ++ks, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    MACAQ_TRACE(0, it);
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer, wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    MACAQ_TRACE(1, it);
-                    const uint32_t fb = full_bar(s);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(sbase + L::OFF_A + s * A_STAGE, &tmA, fb, ks * KB, ti.a_row);
-                    const uint32_t b_dst = sbase + L::OFF_B + s * L::B_STAGE;
-                    if (GROUPED) {
-                        tma_load_3d(b_dst, &tmB, fb, ks * KB, ti.n0, ti.expert);
-                    } else if (CLUSTER == 1) {
-                        tma_load_2d(b_dst, &tmB, fb, ks * KB, ti.n0);
-                    } else {
-                        // this CTA's share of the B tile, delivered to every CTA of the cluster
-                        tma_load_2d_mc(b_dst + rank * B_PART, &tmB, fb, ks * KB,
-                                       ti.n0 + static_cast<int32_t>(rank) * (BN / CLUSTER), kAll);
-                    }
-                    if (a_valid)
-                        bulk_load(sbase + L::OFF_SFA + s * L::SFA_STAGE,
-                                  p.sfa + (static_cast<size_t>(ti.a_row / BM) * p.nka + L::KATOMS * ks) * SF_ATOM,
-                                  L::SFA_STAGE, fb);
-                    const uint32_t sfb_dst = sbase + L::OFF_SFB + s * L::SFB_STAGE;
-                    if (CLUSTER == 1) {
-                        for (int r = 0; r < sfb_valid; ++r)
-                            bulk_load(sfb_dst + r * L::KATOMS * SF_ATOM,
-                                      sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + L::KATOMS * ks) * SF_ATOM,
-                                      L::KATOMS * SF_ATOM, fb);
-                    } else {
-                        // row atoms of B's scales are split over the cluster the same way
-                        for (int r = static_cast<int>(rank); r < sfb_valid; r += CLUSTER)
-                            bulk_load_mc(sfb_dst + r * L::KATOMS * SF_ATOM,
-                                         sfb + (static_cast<size_t>(n_rb0 + r) * p.nka + L::KATOMS * ks) * SF_ATOM,
-                                         L::KATOMS * SF_ATOM, fb, kAll);
-                    }
-                    issued |= 1u << s;
-                    last_parity = (last_parity & ~(1u << s)) | (ph << s);
-                }
-                if (!ok) break;
-            }
-            // every copy issued into this CTA must land, and every consumer of
-            // each stage (in every CTA of the cluster) must have released it,
-            // before the CTA may leave
-            for (int s = 0; s < STAGES; ++s) {
-                if (issued & (1u << s)) {
-                    wait_fixed(full_bar(s), (last_parity >> s) & 1u);
-                    wait_fixed(empty_bar(s), (last_parity >> s) & 1u);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            // Waits only on "scales ready" (which implies the stage's data has
-            // landed) and the accumulator; issues MMAs and commits.  The scale
-            // copies live in their own warp: a barrier wait issued after
-            // tcgen05.cp in the same thread waits for the copies, which
-            // drains the tensor pipe every stage.  Descriptors are
-            // precomputed and advanced by adds (one thread: its own
-            // instruction latency is on the critical path).
-            const uint64_t a_desc0 = smem_desc(sbase + L::OFF_A, 16, L::SWZ_SBO, L::SWZ_DESC);
-            const uint64_t b_desc0 = smem_desc(sbase + L::OFF_B, 16, L::SWZ_SBO, L::SWZ_DESC);
-            const uint32_t idesc0 = idesc_mxf4(BM, BN, 0, 0);
-            const uint32_t idesc2 = idesc_mxf4(BM, BN, 2, 2);
-            const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
-            constexpr uint32_t kAStep = A_STAGE >> 4, kBStep = L::B_STAGE >> 4;
-            bool ok = true;
-            uint32_t tc = 0, st = 0, ph = 0;
-            int ks = 0;
-            for (uint32_t it = 0; it < total_stages; ++it) {
-                MACAQ_TRACE(2, it);
-                if (!wait_bounded(ready_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                MACAQ_TRACE(3, it);
-                if (ks == 0) {
-                    // the epilogue must have drained the accumulator of the previous tile
-                    MACAQ_TRACE(4, tc);
-                    if (!wait_bounded(acc_empty, (tc & 1u) ^ 1u, abort_flag, kErrMma, wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    MACAQ_TRACE(5, tc);
-                }
-                // order these MMAs after the copies / TMEM reads other threads
-                // completed before the barriers above
-                tc_fence_after();
-                const uint32_t sfa_t = sf_t0 + st * L::SF_COLS;
-                const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
-                const uint64_t ad = a_desc0 + st * kAStep;
-                const uint64_t bd = b_desc0 + st * kBStep;
-#pragma unroll
-                for (int j = 0; j < L::KSTEPS; ++j) {
-                    // k step j: 32 bytes further along the swizzled rows; two
-                    // k steps share one scale atom (bytes 0-1, then 2-3)
-                    tc_mma_mxf4(tmem, ad + 2 * j, bd + 2 * j, (j & 1) ? idesc2 : idesc0,
-                                sfa_t + 4 * (j >> 1), sfb_t + 4 * (BN / 128) * (j >> 1),
-                                (ks > 0 || j > 0) ? 1u : 0u);
-                }
-                // the stage's buffers may be refilled (in every CTA that shares them)
-                // once these MMAs have read them
-                if (CLUSTER == 1) tc_commit(empty_bar(static_cast<int>(st)));
-                else tc_commit_mc(empty_bar(static_cast<int>(st)), kAll);
-                if (++ks == nks) {
-                    ks = 0;
-                    tc_commit(acc_full);
-                    ++tc;
-                }
-                if (++st == STAGES) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-            }
-            (void)ok;
-            // all issued tensor-core work must finish before tensor memory is freed
-            tc_commit(drain_bar);
-            wait_fixed(drain_bar, 0);
-        }
-        __syncwarp();
-    } else if (warp == 2) {
-        if (lane == 0) {
-            // ------------------------------------------------ scale copier
-            // For each stage: wait for its data, copy its scale atoms from
-            // shared memory into the stage's tensor-memory slot, commit to
-            // "scales ready".  Slot reuse is safe: stage it's data (and so
-            // this wait) only arrives after the MMAs of stage it-STAGES have
-            // released the slot.
-            const uint64_t sfa_desc0 = smem_desc(sbase + L::OFF_SFA, 0, 128, kSwizzleNone);
-            const uint64_t sfb_desc0 = smem_desc(sbase + L::OFF_SFB, 0, 128, kSwizzleNone);
-            const uint32_t sf_t0 = tmem + SF_TMEM_BASE;
-            constexpr uint32_t kSfaStep = L::SFA_STAGE >> 4, kSfbStep = L::SFB_STAGE >> 4;
-            constexpr uint32_t kAtom = SF_ATOM >> 4;
-            uint32_t st = 0, ph = 0;
-            for (uint32_t it = 0; it < total_stages; ++it) {
-                MACAQ_TRACE(9, it);
-                if (!wait_bounded(full_bar(static_cast<int>(st)), ph, abort_flag, kErrMma, wait_ns)) break;
-                MACAQ_TRACE(10, it);
-                const uint32_t sfa_t = sf_t0 + st * L::SF_COLS;
-                const uint32_t sfb_t = sfa_t + 4 * L::KATOMS;
-                const uint64_t da = sfa_desc0 + st * kSfaStep;
-                const uint64_t db = sfb_desc0 + st * kSfbStep;
-                // TMEM: atom `at` of A at column 4*at; atom `at` of B row block
-                // r at 4*(at*(BN/128) + r), the order one MMA's scale read expects
-#pragma unroll
-                for (int at = 0; at < L::KATOMS; ++at) {
-                    tc_cp_32x128b_warpx4(sfa_t + 4 * at, da + at * kAtom);
-#pragma unroll
-                    for (int r = 0; r < BN / 128; ++r)
-                        tc_cp_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r,
-                                             db + (r * L::KATOMS + at) * kAtom);
-                }
-                tc_commit(ready_bar(static_cast<int>(st)));
-                MACAQ_TRACE(11, it);
-                if (++st == STAGES) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-            }
-            // its copies must complete before tensor memory is freed
-            tc_commit(drain_bar2);
-            wait_fixed(drain_bar2, 0);
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------- epilogue
-        const int ew = warp - EPI_WARP0;
-        const int q = warp & 3;     // tensor-memory lane quarter this warp may access
-        const int half = ew >> 2;   // which 128 accumulator columns
-        const uint32_t ebuf = sbase + L::OFF_EPI + ew * 2 * EPI_BUF;
-        uint32_t tc = 0, chunk = 0;
-        for (int64_t u = first_unit; u < total_units; u += unit_stride, ++tc) {
-            Tile ti;
-            decode_tile<BN, CLUSTER, GROUPED>(u, rank, p, s_off, s_pmb, ti);
-            if (warp == EPI_WARP0) MACAQ_TRACE(6, tc);
-            if (!warp_wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
-            if (warp == EPI_WARP0) MACAQ_TRACE(7, tc);
-            tc_fence_after();
-            uint32_t acc[4][32];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + 32 * c, acc[c]);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
-            if (warp == EPI_WARP0) MACAQ_TRACE(8, tc);
-
-            const int row0 = 32 * q;  // first tile row of this warp
-            const bool any_row = row0 < ti.rows_valid;
-            const bool all_rows = row0 + 32 <= ti.rows_valid;
-            const bool use_tma = GROUPED ? all_rows : any_row;
-            const bool my_row = row0 + lane < ti.rows_valid;
-            if (!any_row) continue;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int32_t ncol = ti.n0 + half * 128 + 16 * c;
-                if (ncol >= p.N) break;
-                uint32_t packed[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
-                    const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                    packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
-                }
-                if (use_tma) {
-                    const uint32_t buf = ebuf + (chunk & 1u) * EPI_BUF;
-                    ++chunk;
-                    if (lane == 0) bulk_wait_read_le1();
-                    __syncwarp();
-                    const uint32_t sw = (lane >> 2) & 1;
-                    const uint32_t r0 = buf + lane * 32 + 16 * (0 ^ sw);
-                    const uint32_t r1 = buf + lane * 32 + 16 * (1 ^ sw);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r0), "r"(packed[0]),
-                                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r1), "r"(packed[4]),
-                                 "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
-                                 : "memory");
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, buf, ncol, ti.y_row0 + row0);
-                        bulk_commit();
-                    }
-                } else if (my_row) {
-                    uint16_t *dst = p.Y + static_cast<int64_t>(ti.y_row0 + row0 + lane) * p.ldy + ncol;
-                    if (ncol + 16 <= p.N) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-                        d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    } else {
-                        for (int i = 0; i < 16 && ncol + i < p.N; ++i)
-                            dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
-                    }
-                }
-            }
-        }
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
-    }
-
-    __syncthreads();
-    MACAQ_TRACE_EDGE(1);
-    // no CTA of the cluster may leave while a peer can still touch its shared memory
-    if (CLUSTER > 1) cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
-    }
-}
-
 // ------------------------------------------------------------ CTA-pair GEMM
 //
 // Dense GEMM on CTA pairs (tcgen05 cta_group::2).  A pair computes a 256 x 256
@@ -612,14 +177,19 @@ struct PairLayout {
     static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * EPI_NBUF * EPI_BUF;
     static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int OFF_OFFS = OFF_MISC + 16;  // grouped: expert tables
+    static constexpr int BYTES = OFF_OFFS + 3 * (static_cast<int>(kMaxExperts) + 1) * 4;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
     static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
     static_assert(ALLOC <= 232448, "shared memory");
 };
 
-template <int STAGES>
+// GROUPED (MoE): the rows of A are expert-grouped (each expert's rows start on
+// a multiple of 128 of the padded layout, sorted rows in Y), B is [E, N, K/2].
+// A pair tile is two consecutive 128-row blocks of one expert's rows; a rank
+// whose block lies past its expert's rows computes nothing that is stored.
+template <int STAGES, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmY,
@@ -678,8 +248,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     griddep_launch_dependents();
     griddep_wait();
 
-    const int32_t num_mp = (p.M + 2 * BM - 1) / (2 * BM);
-    const int64_t total_units = static_cast<int64_t>(p.num_full) + 2 * static_cast<int64_t>(p.num_split);
+    int32_t *s_off = reinterpret_cast<int32_t *>(smem + L::OFF_OFFS);  // expert row offsets
+    int32_t *s_ppb = s_off + (kMaxExperts + 1);    // pair-tiles before expert e
+    int32_t *s_pst = s_ppb + (kMaxExperts + 1);    // first padded row of expert e
+    int32_t num_mp = (p.M + 2 * BM - 1) / (2 * BM);
+    int32_t num_full = p.num_full, num_split = p.num_split;
+    if (GROUPED) {
+        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t pairs = 0, rows = 0;
+            for (int e = 0; e < p.E; ++e) {
+                const int32_t blocks = (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+                s_ppb[e] = pairs;
+                s_pst[e] = rows;
+                pairs += (blocks + 1) / 2;
+                rows += blocks * BM;
+            }
+            s_ppb[p.E] = pairs;
+            s_pst[p.E] = rows;
+        }
+        __syncthreads();
+        // the same last-round split as the host makes for dense problems
+        num_mp = s_ppb[p.E];
+        const int32_t tiles = num_mp * p.num_nb;
+        const int32_t pairs = static_cast<int32_t>(gridDim.x >> 1);
+        const int32_t rem = tiles % pairs;
+        num_full = tiles;
+        num_split = 0;
+        if (rem > 0 && 2 * rem <= pairs) {
+            num_full = tiles - rem;
+            num_split = rem;
+        }
+    }
+    const int64_t total_units = static_cast<int64_t>(num_full) + 2 * static_cast<int64_t>(num_split);
     const int nks = p.num_kstages;
     // scale atoms of stage st -> its tensor-memory slot (A: atom `at` at column
     // 4*at; B: atom `at` of row block r at 4*(2*at + r)), in both CTAs
@@ -704,18 +306,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto tile_of = [&](int64_t u, Tile &ti) {
         int64_t t = u;
         int32_t half = -1;
-        if (u >= p.num_full) {
-            t = p.num_full + (u - p.num_full) / 2;
-            half = static_cast<int32_t>((u - p.num_full) & 1);
+        if (u >= num_full) {
+            t = num_full + (u - num_full) / 2;
+            half = static_cast<int32_t>((u - num_full) & 1);
         }
         const int32_t mp = static_cast<int32_t>(t % num_mp);
         const int32_t nb = static_cast<int32_t>(t / num_mp);
-        ti.a_row = mp * 2 * BM + static_cast<int32_t>(rank) * BM;
         ti.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
         ti.ncols = half < 0 ? BN : BN / 2;
-        ti.expert = 0;
-        ti.y_row0 = ti.a_row;
-        ti.rows_valid = min(BM, p.M - ti.a_row);
+        if (!GROUPED) {
+            ti.a_row = mp * 2 * BM + static_cast<int32_t>(rank) * BM;
+            ti.expert = 0;
+            ti.y_row0 = ti.a_row;
+            ti.rows_valid = min(BM, p.M - ti.a_row);
+        } else {
+            int lo = 0, hi = p.E;  // s_ppb[lo] <= mp < s_ppb[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_ppb[mid] <= mp) lo = mid; else hi = mid;
+            }
+            const int32_t blk = 2 * (mp - s_ppb[lo]) + static_cast<int32_t>(rank);
+            ti.expert = lo;
+            ti.a_row = s_pst[lo] + blk * BM;
+            ti.y_row0 = s_off[lo] + blk * BM;
+            ti.rows_valid = min(BM, s_off[lo + 1] - s_off[lo] - blk * BM);
+        }
     };
 
     if (warp == 0) {
@@ -734,7 +349,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 Tile ti;
                 tile_of(u, ti);
                 const int32_t a_rb = ti.a_row / BM;
-                const int32_t n_rb0 = ti.n0 / 128;
+                // B's scale row blocks: the experts' tiled arrays follow one another
+                const int32_t n_rb0 = ti.expert * p.n_rb + ti.n0 / 128;
                 const bool whole = ti.ncols == BN;
                 bool ok = true;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
@@ -750,8 +366,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * (whole ? kStageBytes : kHalfBytes));
                     tma_load_2d_pair(sbase + L::OFF_A + s * L::A_STAGE, &tmA, fb, ks * KB, ti.a_row);
                     // this CTA's half of the tile's columns (64 of a 128-column unit)
-                    tma_load_2d_pair(sbase + L::OFF_B + s * L::B_STAGE, whole ? &tmB : &tmB64, fb, ks * KB,
-                                     ti.n0 + static_cast<int32_t>(rank) * (ti.ncols / 2));
+                    const int32_t brow = ti.n0 + static_cast<int32_t>(rank) * (ti.ncols / 2);
+                    if (GROUPED)
+                        tma_load_3d_pair(sbase + L::OFF_B + s * L::B_STAGE, whole ? &tmB : &tmB64, fb, ks * KB,
+                                         brow, ti.expert);
+                    else
+                        tma_load_2d_pair(sbase + L::OFF_B + s * L::B_STAGE, whole ? &tmB : &tmB64, fb, ks * KB,
+                                         brow);
                     // scale blocks: (256 B, 2, k atom, 128-row block) views of the tiled layout
                     tma_load_4d_pair(sbase + L::OFF_SFA + s * L::SFA_STAGE, &tmSFA, fb, 0, 0,
                                      L::KATOMS * ks, a_rb);
@@ -787,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t st = 0, ph = 0, tc = 0;
             bool ok = true;
             for (int64_t u = first_unit; u < total_units && ok; u += unit_stride, ++tc) {
-                const bool whole = u < p.num_full;
+                const bool whole = u < num_full;
                 const uint32_t d0 = whole ? idesc0 : hdesc0, d2 = whole ? idesc2 : hdesc2;
                 for (int ks = 0; ks < nks; ++ks) {
                     MACAQ_TRACE(2, tc * nks + ks);
@@ -883,6 +504,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row0 = 32 * q;
             const bool any_row = row0 < ti.rows_valid;
             if (!any_row || half * 128 >= ti.ncols) continue;
+            // Grouped: rows past an expert's last row belong to the next expert
+            // in Y, so a warp with some of them stores row by row.
+            const bool use_tma = !GROUPED || row0 + 32 <= ti.rows_valid;
+            const bool my_row = row0 + lane < ti.rows_valid;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const int32_t ncol = ti.n0 + half * 128 + 16 * c;
@@ -895,7 +520,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
                     packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
                 }
-                {
+                if (!use_tma) {
+                    if (my_row) {
+                        uint16_t *dst = p.Y + static_cast<int64_t>(ti.y_row0 + row0 + lane) * p.ldy + ncol;
+                        if (ncol + 16 <= p.N) {
+                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                            d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        } else {
+                            for (int i = 0; i < 16 && ncol + i < p.N; ++i)
+                                dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+                        }
+                    }
+                } else {
                     // rows past M and columns past N are clipped by the store
                     const uint32_t buf = ebuf + (chunk % L::EPI_NBUF) * EPI_BUF;
                     ++chunk;
@@ -1075,30 +712,18 @@ struct DeviceInfo {
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 
-template <int BN, int STAGES, int KB, bool PAIR>
-constexpr int smem_alloc()
+// Dense (GROUPED = false) or expert-grouped GEMM on CTA pairs.
+template <int STAGES, bool GROUPED>
+cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
 {
-    if constexpr (PAIR)
-        return PairLayout<STAGES>::ALLOC;
-    else
-        return Layout<BN, STAGES, KB>::ALLOC;
-}
-
-template <int BN, int STAGES, int KB, int CLUSTER, bool GROUPED, bool PAIR = false>
-cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
-{
-    static_assert(!PAIR || (BN == 256 && KB == 128 && CLUSTER == 2 && !GROUPED), "pair tiles are dense 256 x 256");
-    constexpr int kAlloc = smem_alloc<BN, STAGES, KB, PAIR>();
-    constexpr CUtensorMapSwizzle kMapSwizzle = KB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    using L = PairLayout<STAGES>;
+    constexpr int BN = L::BN, KB = L::KB;
+    constexpr CUtensorMapSwizzle kSw = CU_TENSOR_MAP_SWIZZLE_128B;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const void *kern;
-    if constexpr (PAIR)
-        kern = reinterpret_cast<const void *>(gemm_mxf4_pair_kernel<STAGES>);
-    else
-        kern = reinterpret_cast<const void *>(gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>);
+    auto kern = gemm_mxf4_pair_kernel<STAGES, GROUPED>;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         DeviceInfo &di = g_dev[dev];
@@ -1107,7 +732,7 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
             if (err != cudaSuccess) return err;
         }
         if (!di.attr_set[slot]) {
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
             if (err != cudaSuccess) return err;
             di.attr_set[slot] = true;
         }
@@ -1115,26 +740,32 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     const int sms = g_dev[dev].sms;
 
     const uint64_t kb = static_cast<uint64_t>(g.K / 2);
-    CUtensorMap tmA, tmB, tmY;
+    // A: 128-row boxes; B: each CTA's 128 rows (64 for a split tile's halves),
+    // per expert when grouped; Y: 32 x 16 store boxes
+    CUtensorMap tmA, tmB, tmB64, tmY;
     {
         uint64_t dims[2] = {kb, static_cast<uint64_t>(g.a_rows)};
         uint64_t strides[1] = {kb};
         uint32_t box[2] = {KB, BM};
-        if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box, kMapSwizzle))
+        if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.a_codes, dims, strides, box, kSw))
             return cudaErrorInvalidValue;
     }
-    if (GROUPED) {
-        uint64_t dims[3] = {kb, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.E)};
-        uint64_t strides[2] = {kb, kb * static_cast<uint64_t>(g.N)};
-        uint32_t box[3] = {KB, BN, 1};
-        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box, kMapSwizzle))
-            return cudaErrorInvalidValue;
-    } else {
-        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
-        uint64_t strides[1] = {kb};
-        uint32_t box[2] = {KB, BN / CLUSTER};
-        if (!encode(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box, kMapSwizzle))
-            return cudaErrorInvalidValue;
+    for (int which = 0; which < 2; ++which) {
+        CUtensorMap *m = which == 0 ? &tmB : &tmB64;
+        const uint32_t rows = which == 0 ? BN / 2 : BN / 4;
+        if (GROUPED) {
+            uint64_t dims[3] = {kb, static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.E)};
+            uint64_t strides[2] = {kb, kb * static_cast<uint64_t>(g.N)};
+            uint32_t box[3] = {KB, rows, 1};
+            if (!encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_codes, dims, strides, box, kSw))
+                return cudaErrorInvalidValue;
+        } else {
+            uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
+            uint64_t strides[1] = {kb};
+            uint32_t box[2] = {KB, rows};
+            if (!encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box, kSw))
+                return cudaErrorInvalidValue;
+        }
     }
     {
         uint64_t dims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.M)};
@@ -1144,38 +775,23 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
                     CU_TENSOR_MAP_SWIZZLE_32B))
             return cudaErrorInvalidValue;
     }
-
-    // B boxes of 64 rows for the 128-column halves of split tiles
-    CUtensorMap tmB64;
-    if (PAIR) {
-        uint64_t dims[2] = {kb, static_cast<uint64_t>(g.N)};
-        uint64_t strides[1] = {kb};
-        uint32_t box[2] = {KB, 64};
-        if (!encode(&tmB64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box, kMapSwizzle))
-            return cudaErrorInvalidValue;
-    }
-    // Scale blocks for the pair kernel: the tiled layout viewed as
-    // (256 B, 2 halves of a 512-byte atom, k atom, 128-row block).
+    // Scale blocks: the tiled layout viewed as (256 B, 2 halves of a 512-byte
+    // atom, k atom, 128-row block); grouped weights: the experts' tiled arrays
+    // one after another.
     CUtensorMap tmSFA, tmSFB;
-    if (PAIR) {
+    {
         const uint64_t nka = static_cast<uint64_t>(pad_scale_cols(g.K) / 4);
         uint64_t strides[3] = {256, 512, nka * 512};
-        {
-            uint64_t dims[4] = {256, 2, nka, static_cast<uint64_t>(pad_rows(g.M) / 128)};
-            uint32_t box[4] = {256, 2, 2, 1};
-            if (!encode_4d(&tmSFA, g.a_scales, dims, strides, box)) return cudaErrorInvalidValue;
-        }
-        {
-            uint64_t dims[4] = {256, 2, nka, static_cast<uint64_t>(pad_rows(g.N) / 128)};
-            uint32_t box[4] = {256, 2, 2, 2};
-            if (!encode_4d(&tmSFB, g.w_scales, dims, strides, box)) return cudaErrorInvalidValue;
-        }
+        uint64_t dims_a[4] = {256, 2, nka, static_cast<uint64_t>(pad_rows(g.a_rows) / 128)};
+        uint32_t box_a[4] = {256, 2, 2, 1};
+        if (!encode_4d(&tmSFA, g.a_scales, dims_a, strides, box_a)) return cudaErrorInvalidValue;
+        const uint64_t experts = GROUPED ? static_cast<uint64_t>(g.E) : 1;
+        uint64_t dims_b[4] = {256, 2, nka, experts * static_cast<uint64_t>(pad_rows(g.N) / 128)};
+        uint32_t box_b[4] = {256, 2, 2, 2};
+        if (!encode_4d(&tmSFB, g.w_scales, dims_b, strides, box_b)) return cudaErrorInvalidValue;
     }
 
     Params p;
-    p.sfa = g.a_scales;
-    p.sfb = g.w_scales;
-    p.sfb_expert_stride = tiled_scale_bytes(g.N, g.K);
     p.offsets = g.offsets;
     p.Y = static_cast<uint16_t *>(g.Y);
     p.ldy = g.ldy;
@@ -1183,47 +799,48 @@ cudaError_t launch_impl(const GemmArgs &g, cudaStream_t stream, int slot)
     p.M = static_cast<int32_t>(g.M);
     p.N = static_cast<int32_t>(g.N);
     p.num_kstages = static_cast<int32_t>((g.K + 2 * KB - 1) / (2 * KB));
-    p.nka = static_cast<int32_t>(pad_scale_cols(g.K) / 4);
-    p.num_mb = static_cast<int32_t>((g.M + BM - 1) / BM);
     p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
 
-    int64_t units = GROUPED ? (g.a_rows / BM) * p.num_nb
-                            : static_cast<int64_t>((p.num_mb + CLUSTER - 1) / CLUSTER) * p.num_nb;
-    p.num_full = static_cast<int32_t>(units);
-    p.num_split = 0;
-    if (PAIR) {
+    const int64_t pairs_max = sms / 2;
+    int64_t units;
+    if (GROUPED) {
+        // at most (padded blocks / 2 + one odd block per expert) pair tiles per
+        // column block; the kernel counts the exact number and splits its tail
+        units = (g.a_rows / BM / 2 + g.E) * p.num_nb;
+        p.num_full = static_cast<int32_t>(units);
+        p.num_split = 0;
+    } else {
+        units = static_cast<int64_t>((g.M + 2 * BM - 1) / (2 * BM)) * p.num_nb;
+        p.num_full = static_cast<int32_t>(units);
+        p.num_split = 0;
         // tiles that would run in a last, partly filled round of pairs run as
         // two 128-column halves instead (when the halves fit in that round)
-        const int64_t pairs = sms / 2;
-        const int64_t rem = units % pairs;
-        if (rem > 0 && 2 * rem <= pairs) {
+        const int64_t rem = units % pairs_max;
+        if (rem > 0 && 2 * rem <= pairs_max) {
             p.num_full = static_cast<int32_t>(units - rem);
             p.num_split = static_cast<int32_t>(rem);
             units += rem;
         }
     }
-    int64_t clusters = units < sms / CLUSTER ? units : sms / CLUSTER;
-    if (clusters < 1) clusters = 1;
+    int64_t pairs = units < pairs_max ? units : pairs_max;
+    if (pairs < 1) pairs = 1;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = kAlloc;
+    cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if constexpr (PAIR)
-        return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<STAGES>, tmA, tmB, tmB64, tmY, tmSFA, tmSFB, p);
-    else
-        return cudaLaunchKernelEx(&cfg, gemm_mxf4_kernel<BN, STAGES, KB, CLUSTER, GROUPED>, tmA, tmB, tmY, p);
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmY, tmSFA, tmSFB, p);
 }
 
 }  // namespace
@@ -1339,8 +956,8 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     if (g.E == 0 && g.M <= 64) return launch_skinny<64, 4>(g, stream, 6);
     // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
     // (multicast) the B tile of adjacent m-blocks
-    if (g.E > 0) return launch_impl<256, 4, 128, 1, true>(g, stream, 1);
-    return launch_impl<256, 6, 128, 2, false, true>(g, stream, 3);
+    if (g.E > 0) return launch_pair<6, true>(g, stream, 7);
+    return launch_pair<6, false>(g, stream, 3);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)
