@@ -682,16 +682,23 @@ __global__ void __launch_bounds__(544, 1) quant_grouped_tma_kernel(const __grid_
     }
     __syncthreads();
 
-    // a contiguous range of row groups per CTA: consecutive rows mostly share
-    // an expert, so the balance factors are reloaded rarely
-    const int32_t g0 = static_cast<int32_t>(blockIdx.y) * per_cta;
-    const int32_t my_groups = g0 < groups ? min(per_cta, groups - g0) : 0;
+    // A contiguous range of row groups per CTA (consecutive rows mostly share
+    // an expert, so the balance factors are reloaded rarely), dealt over the
+    // rows the experts actually use; the rest of the padded capacity only needs
+    // zero scales, written after the pipeline.
+    const int64_t used = s_poff[a.E];
+    const int32_t groups_used = static_cast<int32_t>((used + RT - 1) / RT);
+    const int32_t per = (groups_used + static_cast<int32_t>(gridDim.y) - 1) / static_cast<int32_t>(gridDim.y);
+    const int32_t g0 = static_cast<int32_t>(blockIdx.y) * per;
+    const int32_t my_groups = g0 < groups_used ? min(per, groups_used - g0) : 0;
+    (void)groups;
+    (void)per_cta;
     // row i of local group j is padded row (g0 + j) * RT + i
     for (int idx = t; idx < my_groups * RT; idx += blockDim.x) {
         const int j = idx / RT, i = idx - (idx / RT) * RT;
         const int64_t p = (static_cast<int64_t>(g0) + j) * RT + i;
         int32_t src = -2, ex = 0;
-        if (p < a.rows_out) {
+        if (p < used) {
             src = -1;
             if (p < s_poff[a.E]) {
                 int lo = 0, hi = a.E;  // s_poff[lo] <= p < s_poff[hi]
@@ -805,6 +812,14 @@ __global__ void __launch_bounds__(544, 1) quant_grouped_tma_kernel(const __grid_
         if (writes_scale && src != -2) {
             const int64_t off = ((p / 128) * nka + kb / 4) * 512 + (p % 32) * 16 + ((p % 128) / 32) * 4;
             *reinterpret_cast<uint32_t *>(a.scales + off) = word;
+        }
+    }
+    // zero scales for the padded capacity past the experts' rows
+    if (writes_scale) {
+        for (int64_t p = used + static_cast<int64_t>(blockIdx.y) * RT + ty; p < a.rows_out;
+             p += static_cast<int64_t>(gridDim.y) * RT) {
+            const int64_t off = ((p / 128) * nka + kb / 4) * 512 + (p % 32) * 16 + ((p % 128) / 32) * 4;
+            *reinterpret_cast<uint32_t *>(a.scales + off) = 0u;
         }
     }
 }
@@ -936,14 +951,44 @@ cudaError_t open_smem(Kern kern, int slot, int64_t smem)
     return cudaSuccess;
 }
 
-cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t stream, bool *done)
+// Stage shape of the TMA kernels: TB blocks of 32 values (a slab of the row)
+// by RT rows, consumer threads TB * RT <= 512 and a whole number of warps
+// (a warp may span rows; TB is a multiple of 8, so every group of four
+// neighbouring blocks sharing a scale word lies in one row), a stage of at
+// most 32 KB, and the fewest idle blocks over the slabs that cover the row.
+bool pick_tma_tile(int64_t nkb_pad, int64_t *tb_out, int64_t *rt_out)
+{
+    int64_t best_waste = -1;
+    const int64_t s0 = (nkb_pad + 255) / 256;
+    for (int64_t slabs = s0; slabs <= s0 + 8; ++slabs) {
+        const int64_t tb = ((nkb_pad + slabs - 1) / slabs + 7) / 8 * 8;
+        if (tb > 256) continue;
+        int64_t rt = 0;
+        for (int64_t r = (512 / tb < 32 ? 512 / tb : 32); r >= 1; --r) {
+            if ((tb * r) % 32 == 0 && tb * r * 64 <= 32768) {
+                rt = r;
+                break;
+            }
+        }
+        if (rt == 0) continue;
+        const int64_t waste = tb * slabs - nkb_pad;
+        if (best_waste < 0 || waste < best_waste) {
+            best_waste = waste;
+            *tb_out = tb;
+            *rt_out = rt;
+        }
+    }
+    return best_waste >= 0;
+}
+
+cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool *done)
 {
     *done = false;
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
+    int64_t tb = 0, rt = 0;
+    if (!pick_tma_tile(nkb_pad, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
-    int64_t rt = 512 / tb;  // consumer threads <= 512 (plus one producer warp)
-    rt = rt > 16 ? 16 : (rt < 1 ? 1 : rt);
     const int64_t stage = tb * rt * 64;
     const int stages = (6 * stage + 1024 <= 200 * 1024) ? 6 : 4;
     const int64_t smem = stages * stage + 16 * stages + 16 + 1024;
@@ -971,14 +1016,14 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, int64_t tb, cudaStream_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_grouped_tma(const QuantArgs &a, int64_t tb, cudaStream_t stream, bool *done)
+cudaError_t launch_quant_grouped_tma(const QuantArgs &a, cudaStream_t stream, bool *done)
 {
     *done = false;
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
+    int64_t tb = 0, rt = 0;
+    if (!pick_tma_tile(nkb_pad, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
-    int64_t rt = 512 / tb;
-    rt = rt > 16 ? 16 : (rt < 1 ? 1 : rt);
     const int64_t stage = tb * rt * 64;
     int sms = 148;
     MACAQ_TRY_CUDA(quant_device(&sms));
@@ -1030,13 +1075,12 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
     }
     if (mode == QuantMode::Dense && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
         bool done = false;
-        cudaError_t err = launch_quant_dense_tma(a, best_t, stream, &done);
+        cudaError_t err = launch_quant_dense_tma(a, stream, &done);
         if (err != cudaSuccess || done) return err;
     }
-    if (mode == QuantMode::ActGrouped && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1 &&
-        best_t % 8 == 0) {
+    if (mode == QuantMode::ActGrouped && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
         bool done = false;
-        cudaError_t err = launch_quant_grouped_tma(a, best_t, stream, &done);
+        cudaError_t err = launch_quant_grouped_tma(a, stream, &done);
         if (err != cudaSuccess || done) return err;
     }
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
