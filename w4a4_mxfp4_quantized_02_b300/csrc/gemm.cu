@@ -951,8 +951,8 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
 {
     // a few token rows: weight rows on the MMA's M side (decode)
-    if (g.E == 0 && g.M <= 16) return launch_skinny<16, 4>(g, stream, 4);
-    if (g.E == 0 && g.M <= 32) return launch_skinny<32, 4>(g, stream, 5);
+    if (g.E == 0 && g.M <= 16) return launch_skinny<16, 5>(g, stream, 4);
+    if (g.E == 0 && g.M <= 32) return launch_skinny<32, 5>(g, stream, 5);
     if (g.E == 0 && g.M <= 64) return launch_skinny<64, 4>(g, stream, 6);
     // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
     // (multicast) the B tile of adjacent m-blocks

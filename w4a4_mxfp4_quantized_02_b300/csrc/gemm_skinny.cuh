@@ -37,9 +37,12 @@ struct Layout {
     static constexpr int OFF_X = OFF_W + STAGES * W_STAGE;
     static constexpr int OFF_SFW = OFF_X + STAGES * X_STAGE;
     static constexpr int OFF_SFX = OFF_SFW + STAGES * SF_STAGE;
-    static constexpr int OFF_PART = OFF_SFX + STAGES * SF_STAGE;  // fp32 [128][NT + 1]
+    // fp32 partial [128][NT + 1] of a K-split cluster: written once every MMA
+    // has completed and every copy has landed, so it reuses the weight stages
+    static constexpr int OFF_PART = OFF_W;
     static constexpr int PART_LD = NT + 1;
-    static constexpr int OFF_BAR = OFF_PART + 128 * PART_LD * 4;
+    static_assert(128 * PART_LD * 4 <= STAGES * W_STAGE, "partial must fit the weight stages");
+    static constexpr int OFF_BAR = OFF_SFX + STAGES * SF_STAGE;
     static constexpr int NUM_BARS = 3 * STAGES + 3;
     static constexpr int OFF_MISC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
     static constexpr int BYTES = OFF_MISC + 16;
