@@ -494,8 +494,17 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
 // factors in registers; the last warp only issues the loads, STAGES groups
 // ahead.  Warps run decoupled: each consumer warp waits on a stage's "full"
 // barrier through one lane and releases it on the stage's "empty" barrier.
+// Consumer threads of a TMA transform CTA (plus one producer warp): 20 warps,
+// 96 registers each, so the warps of the one resident CTA hide more latency.
+constexpr int kTmaConsumersMax = 640;
+constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
+// The grouped kernel keeps its balance factors in registers (they change with
+// the expert): 16 consumer warps.
+constexpr int kGroupedConsumersMax = 512;
+constexpr int kGroupedThreadsMax = kGroupedConsumersMax + 32;
+
 template <int STAGES>
-__global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                   QuantArgs a, int32_t groups, int32_t TB,
                                                                   int32_t RT)
 {
@@ -509,6 +518,9 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
     const uint32_t full0 = sbase + STAGES * stage_bytes;
     const uint32_t empty0 = full0 + 8 * STAGES;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(qsmem + STAGES * stage_bytes + 16 * STAGES);
+    // the slab's balance factors: block tx's 32 floats at 128 * tx, its 16-byte
+    // chunk c stored at position (c + tx) mod 8 (conflict-free reads)
+    const uint32_t ftab = sbase + STAGES * stage_bytes + 16 * STAGES + 16;
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int32_t slab0 = static_cast<int32_t>(blockIdx.x) * TB;
@@ -527,6 +539,16 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
     // still read the codes) before touching global memory
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+
+    for (int idx = t; idx < TB * 8; idx += blockDim.x) {
+        const int bx = idx >> 3, c = idx & 7;
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (slab0 + bx < a.K / 32) v4 = __ldg(reinterpret_cast<const float4 *>(a.f + 32 * (slab0 + bx)) + c);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ftab + 128 * bx + 16 * ((c + bx) & 7)),
+                     "f"(v4.x), "f"(v4.y), "f"(v4.z), "f"(v4.w)
+                     : "memory");
+    }
+    __syncthreads();
 
     const int32_t my_groups = blockIdx.y < static_cast<uint32_t>(groups)
                                   ? (groups - 1 - static_cast<int32_t>(blockIdx.y)) / static_cast<int32_t>(gridDim.y) + 1
@@ -566,16 +588,7 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
     const int64_t kb = static_cast<int64_t>(slab0) + tx;
     const bool has_kb = kb < nkb;
     const bool writes_scale = (lane & 3) == 0 && kb < nkb_pad;
-    float2 f[16];
-    if (has_kb) {
-        const float4 *f4 = reinterpret_cast<const float4 *>(a.f + 32 * kb);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 v4 = __ldg(f4 + j);
-            f[2 * j] = make_float2(v4.x, v4.y);
-            f[2 * j + 1] = make_float2(v4.z, v4.w);
-        }
-    }
+    const uint32_t fbase = ftab + 128 * tx;
     const uint32_t swz = (static_cast<uint32_t>(t) >> 1) & 3u;  // 64-byte row t of a stage
     const int64_t half_k = a.K / 2;
 
@@ -608,6 +621,16 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
             // the stage is no longer needed by this warp once its reads are done
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
+            float2 f[16];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float x0, x1, x2, x3;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+                             : "r"(fbase + 16 * ((c + tx) & 7)));
+                f[2 * c] = make_float2(x0, x1);
+                f[2 * c + 1] = make_float2(x2, x3);
+            }
             uint4 codes;
             sbyte = quant_block_pairs(raw, f, codes);
             *reinterpret_cast<uint4 *>(a.codes + r * half_k + 16 * kb) = codes;
@@ -636,7 +659,7 @@ __global__ void __launch_bounds__(544, 1) quant_dense_tma_kernel(const __grid_co
 // (one row high), so the rows can come from anywhere in X.  The rows of this
 // CTA are resolved once, up front, into a table in shared memory.
 template <int STAGES>
-__global__ void __launch_bounds__(544, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
                                                                     int32_t RT, int32_t per_cta)
 {
@@ -956,7 +979,7 @@ cudaError_t open_smem(Kern kern, int slot, int64_t smem)
 // (a warp may span rows; TB is a multiple of 8, so every group of four
 // neighbouring blocks sharing a scale word lies in one row), a stage of at
 // most 32 KB, and the fewest idle blocks over the slabs that cover the row.
-bool pick_tma_tile(int64_t nkb_pad, int64_t *tb_out, int64_t *rt_out)
+bool pick_tma_tile(int64_t nkb_pad, int64_t max_consumers, int64_t *tb_out, int64_t *rt_out)
 {
     int64_t best_waste = -1;
     const int64_t s0 = (nkb_pad + 255) / 256;
@@ -964,8 +987,8 @@ bool pick_tma_tile(int64_t nkb_pad, int64_t *tb_out, int64_t *rt_out)
         const int64_t tb = ((nkb_pad + slabs - 1) / slabs + 7) / 8 * 8;
         if (tb > 256) continue;
         int64_t rt = 0;
-        for (int64_t r = (512 / tb < 32 ? 512 / tb : 32); r >= 1; --r) {
-            if ((tb * r) % 32 == 0 && tb * r * 64 <= 32768) {
+        for (int64_t r = (max_consumers / tb < 32 ? max_consumers / tb : 32); r >= 1; --r) {
+            if ((tb * r) % 32 == 0 && tb * r * 64 <= 40960) {
                 rt = r;
                 break;
             }
@@ -987,12 +1010,13 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
     int64_t tb = 0, rt = 0;
-    if (!pick_tma_tile(nkb_pad, &tb, &rt)) return cudaSuccess;
+    if (!pick_tma_tile(nkb_pad, kTmaConsumersMax, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
     const int64_t stage = tb * rt * 64;
-    const int stages = (6 * stage + 1024 <= 200 * 1024) ? 6 : 4;
-    const int64_t smem = stages * stage + 16 * stages + 16 + 1024;
-    if (smem > 200 * 1024) return cudaSuccess;  // fall through to the register-staged kernel
+    const int64_t fixed = 16 + tb * 128 + 1024;  // abort flag, balance-factor table, alignment
+    const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : 4;
+    const int64_t smem = stages * stage + 16 * stages + fixed;
+    if (smem > 210 * 1024) return cudaSuccess;  // fall through to the register-staged kernel
     CUtensorMap tm;
     const uint64_t dims[3] = {32, static_cast<uint64_t>(nkb), static_cast<uint64_t>(a.rows_valid)};
     const uint64_t strides[2] = {64, static_cast<uint64_t>(a.ld_src) * 2};
@@ -1022,7 +1046,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, cudaStream_t stream, bo
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
     int64_t tb = 0, rt = 0;
-    if (!pick_tma_tile(nkb_pad, &tb, &rt)) return cudaSuccess;
+    if (!pick_tma_tile(nkb_pad, kGroupedConsumersMax, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
     const int64_t stage = tb * rt * 64;
     int sms = 148;
@@ -1038,7 +1062,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, cudaStream_t stream, bo
     const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 2 * max_rows * 4 + 1024;
     const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : 4;
     const int64_t smem = stages * stage + 16 * stages + fixed;
-    if (smem > 200 * 1024) return cudaSuccess;
+    if (smem > 210 * 1024) return cudaSuccess;
     CUtensorMap tm;
     // the token rows are whatever row_src names (valid by contract): no row bound
     const uint64_t dims[3] = {32, static_cast<uint64_t>(nkb), 0x7fffffffull};
