@@ -507,7 +507,8 @@ def gpu_arm(args, rank: int, world: int):
 
 def moe_workload_config(wl):
     return {"workload": f"{wl.name}: {wl.T} tokens x top-{wl.topk} of {wl.E} experts = {wl.rows} rows; "
-                        f"gate+up K={wl.K} N={2 * wl.F}, down K={wl.F} N={wl.K}; bf16 in/out, MXFP4 W4A4",
+                        f"gate+up K={wl.K} N={2 * wl.F}, SiLU(gate)*up fused into the down input's "
+                        f"transform, down K={wl.F} N={wl.K}; bf16 in/out, MXFP4 W4A4",
             "T": wl.T, "E": wl.E, "topk": wl.topk, "K": wl.K, "F": wl.F, "rows": wl.rows,
             "l2": "weights (302 MB of codes) exceed L2; no input rotation needed"}
 
@@ -579,7 +580,6 @@ def gpu_arm_moe(args, rank: int, world: int):
     del W, Xc, Xdc
 
     X = d["X"].to(dev)
-    Xd = d["Xd"].to(dev)
     row_src = r["row_src"].to(dev)
     ident = torch.arange(rows, dtype=torch.int32, device=dev)
     offs = r["offsets"].to(dev)
@@ -600,7 +600,8 @@ def gpu_arm_moe(args, rank: int, world: int):
         mq.macaq_grouped_w4a4_gemm(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, 2 * F, K, Y=Ygu)
         if ev is not None:
             ev[2].record(stream)
-        mq.macaq_quant_act_grouped(Xd, ident, offs, inv_dn, rows, E, a_dn, as_dn)
+        # the down input is SiLU(gate) * up of the gate+up output, fused into its transform
+        mq.macaq_quant_act_grouped_silu(Ygu, offs, inv_dn, rows, E, a_dn, as_dn)
         if ev is not None:
             ev[3].record(stream)
         mq.macaq_grouped_w4a4_gemm(a_dn, as_dn, wdn_codes, wdn_scales, offs, rows, E, K, F, Y=Ydn)
@@ -655,7 +656,7 @@ def gpu_arm_moe(args, rank: int, world: int):
     gu_bytes, dn_bytes = gemm_bytes(2 * F, K), gemm_bytes(K, F)
     # algorithmic bytes: each token row read once (its eight expert copies are
     # gathered from L2), every sorted row's codes and scales written once
-    q_bytes = [wl.T * K * 2 + rows * (K // 2 + K // 32), rows * F * 2 + rows * (F // 2 + F // 32)]
+    q_bytes = [wl.T * K * 2 + rows * (K // 2 + K // 32), rows * 2 * F * 2 + rows * (F // 2 + F // 32)]
     gu_gbs = gu_bytes / (avg[1] * 1e-3) / 1e9
     dn_gbs = dn_bytes / (avg[3] * 1e-3) / 1e9
 
@@ -715,7 +716,7 @@ def gpu_arm_moe(args, rank: int, world: int):
         "down_gemm": {"achieved": dn_gbs, "unit": "GB/s", "frac": dn_gbs / peaks["hbm_gbs"],
                       "bytes_per_launch": dn_bytes, "avg_launch_us": avg[3] * 1e3,
                       "tflops": wl.flops_down / (avg[3] * 1e-3) / 1e12},
-        "act_quant": {"kernel": "quant_kernel<ActGrouped>",
+        "act_quant": {"kernel": "quant_grouped_tma_kernel (token rows; SwiGLU-fused for the down input)",
                       "achieved": [q_bytes[0] / (avg[0] * 1e-3) / 1e9, q_bytes[1] / (avg[2] * 1e-3) / 1e9],
                       "peak": peaks["hbm_gbs"], "unit": "GB/s (gate+up input, down input)",
                       "frac": [q_bytes[0] / (avg[0] * 1e-3) / 1e9 / peaks["hbm_gbs"],

@@ -189,6 +189,26 @@ macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *
                                      int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
                                      uint8_t *a_scales, macaq_stream_t stream);
 
+/* Grouped activation transform of a gated MLP's down-projection input,
+ * fused with its SwiGLU step.  GU bf16 [rows, ldgu] holds, in sorted row
+ * order, the gate (columns 0..F-1) and up (columns F..2F-1) outputs of the
+ * grouped gate+up GEMM; row r is first turned into
+ *   h_j = bf16_rn( SiLU(g_j) * u_j ),  SiLU(g) = g / (1 + e^-g)
+ * in fp32 (e^x by Cody-Waite range reduction and a degree-8 Taylor
+ * polynomial, every operation rounded to nearest), then transformed exactly as
+ * macaq_quant_act_grouped transforms token rows (balance with inv_s row e,
+ * fp32 [E, F]; 32-point Hadamard; MXFP4) into padded row P_e + r - offsets[e].
+ * The pages state no gated-MLP arithmetic: the SwiGLU form and its fp32 / bf16
+ * rounding are this library's reading (the value an unfused layer would store
+ * in bf16, re-read by the transform).  The routed experts it serves run W4A4
+ * (page "Huawei MACaQ", section "MACaQ Backends").  a_codes [P, F/2],
+ * a_scales tiled for P rows, P = macaq_grouped_padded_rows(rows, E); padding
+ * rows as in macaq_quant_act_grouped.  F % 32 == 0, ldgu >= 2F, ldgu % 8 == 0,
+ * GU 16-byte aligned, E <= 256. */
+macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
+                                          const float *inv_s, int64_t rows, int64_t E, int64_t F,
+                                          uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream);
+
 /* Grouped GEMM: for each expert e and sorted row r of e,
  *   Y[r, n] = bf16_rn( sum_k A(P_e + r - offsets[e], k) * Wq_e(n, k) )
  * with A from macaq_quant_act_grouped and Wq_e from

@@ -60,6 +60,8 @@ def lib():
             "oracle_tile_scales": [P, I, I, P],
             "oracle_e2m1_encode_many": [P, I, P],
             "oracle_scale_exponent_many": [P, I, P],
+            "oracle_silu_mul": [P, I, I, P],
+            "oracle_exp_many": [P, I, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -235,3 +237,23 @@ def quantize_grouped(Xrows, offsets: np.ndarray, inv_s_e: np.ndarray):
         if b > a:
             codes[a:b], scales[a:b] = quantize(x[a:b], inv_s_e[e])
     return codes, scales
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    """The fp32 e^x the SwiGLU step is stated with (range reduction and a
+    degree-8 Taylor polynomial, see macaq_oracle.c)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    lib().oracle_exp_many(_p(x), x.size, _p(y))
+    return y
+
+
+def silu_mul(GU) -> np.ndarray:
+    """h = bf16(SiLU(g) * u) of a [rows, 2F] bf16 gate|up matrix, as bf16 bits
+    (uint16) [rows, F]."""
+    bits = np.ascontiguousarray(bf16_bits(GU))
+    rows, two_f = bits.shape
+    F = two_f // 2
+    h = np.empty((rows, F), dtype=np.uint16)
+    lib().oracle_silu_mul(_p(bits), rows, F, _p(h))
+    return h

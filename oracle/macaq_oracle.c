@@ -26,6 +26,14 @@
  *                    to the even code, saturating at 6.
  *   GEMM reference   Y = deq(A) . deq(W)^T accumulated in fp64.
  *
+ *   SwiGLU input     (extension: the down projection of a gated MLP reads
+ *                    h = SiLU(g) * u of the gate and up outputs g, u.)  Stated
+ *                    in fp32: e^x by range reduction x = n ln2 + r and a
+ *                    degree-8 Taylor polynomial in r, SiLU(g) = g / (1 + e^-g),
+ *                    h rounded once to bf16 (the value an unfused layer would
+ *                    store).  The CUDA path evaluates the same operations in
+ *                    the same order; both are pinned against fp64 exp.
+ *
  * Precision: the transform is stated in fp32 (IEEE, round to nearest, no
  * contraction: build with -ffp-contract=off, no fast-math), because the
  * quantised codes depend on its exact bits.  The fp64 variant exists for the
@@ -337,4 +345,70 @@ void oracle_e2m1_encode_many(const float *t, int64_t n, uint8_t *codes)
 void oracle_scale_exponent_many(const float *amax, int64_t n, int32_t *se)
 {
     for (int64_t i = 0; i < n; ++i) se[i] = oracle_scale_exponent(amax[i]);
+}
+
+/* ------------------------------------------------------------------ SwiGLU */
+
+/* e^x in fp32 (round to nearest at every step, no contraction):
+ *   n = nearest integer to x * log2(e),
+ *   r = (x - n * ln2_hi) - n * ln2_lo      with ln2_hi + ln2_lo = ln 2 and
+ *                                          ln2_hi short enough that n * ln2_hi
+ *                                          is exact for |n| < 256,
+ *   e^r by Horner on the Taylor series to r^8 / 8!  (|r| <= 0.35: the
+ *   truncation is below 2^-30 relative),
+ *   e^x = e^r * 2^n, scaled in two steps where 2^n is not a normal float.
+ * Overflow past ln(FLT_MAX) gives +inf, underflow below the smallest
+ * subnormal gives +0. */
+float oracle_exp_f32(float x)
+{
+    if (x > 88.72283935546875f) return INFINITY;
+    if (x < -103.972084045410156f) return 0.0f;
+    const float t = x * 0x1.715476p+0f;               /* log2(e) */
+    const float fn = rintf(t);
+    const int n = (int)fn;
+    float r = x - fn * 0x1.62e4p-1f;                  /* ln2_hi = 0.693145751953125 */
+    r = r - fn * 0x1.7f7d1cp-20f;                     /* ln2_lo */
+    float p = 0x1.a01a02p-16f;                        /* 1/8! */
+    p = p * r + 0x1.a01a02p-13f;                      /* 1/7! */
+    p = p * r + 0x1.6c16c2p-10f;                      /* 1/6! */
+    p = p * r + 0x1.111112p-7f;                       /* 1/5! */
+    p = p * r + 0x1.555556p-5f;                       /* 1/4! */
+    p = p * r + 0x1.555556p-3f;                       /* 1/3! */
+    p = p * r + 0x1.0p-1f;                            /* 1/2! */
+    p = p * r + 0x1.0p+0f;                            /* 1/1! */
+    p = p * r + 0x1.0p+0f;                            /* 1/0! */
+    if (n > 127) return (p * 0x1.0p+127f) * ldexpf(1.0f, n - 127);
+    if (n < -126) return (p * ldexpf(1.0f, n + 100)) * 0x1.0p-100f;
+    return p * ldexpf(1.0f, n);
+}
+
+static uint16_t f32_to_bf16_rne(float f)
+{
+    const uint32_t u = f32_bits(f);
+    const uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7fffu + lsb) >> 16);
+}
+
+/* h = bf16( SiLU(g) * u ) with SiLU(g) = g / (1 + e^-g), all in fp32. */
+uint16_t oracle_silu_mul_bf16(uint16_t g_bits, uint16_t u_bits)
+{
+    const float g = bf16_bits_to_f32(g_bits);
+    const float u = bf16_bits_to_f32(u_bits);
+    const float e = oracle_exp_f32(-g);
+    const float s = g / (1.0f + e);
+    return f32_to_bf16_rne(s * u);
+}
+
+/* gu: [rows, 2F] bf16 (gate in columns 0..F-1, up in F..2F-1) -> h [rows, F]. */
+void oracle_silu_mul(const uint16_t *gu, int64_t rows, int64_t F, uint16_t *h)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < F; ++j)
+            h[r * F + j] = oracle_silu_mul_bf16(gu[r * 2 * F + j], gu[r * 2 * F + F + j]);
+}
+
+void oracle_exp_many(const float *x, int64_t n, float *y)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_exp_f32(x[i]);
 }

@@ -95,6 +95,12 @@ def test_grouped_rejections(L):
     assert g(p, p, p, p, p, 100, 300, 64, 128, p, 64, None) == UNSUPPORTED
     assert g(p, p, p, p, None, 100, 4, 64, 128, p, 64, None) == INVALID
     assert g(p, p, p, p, p, 0, 4, 64, 128, p, 64, None) == OK
+    z = L.macaq_quant_act_grouped_silu
+    assert z(p, 256, p, p, 100, 0, 128, p, p, None) == INVALID           # E = 0
+    assert z(p, 256, p, p, 100, 4, 100, p, p, None) == INVALID           # F % 32
+    assert z(p, 200, p, p, 100, 4, 128, p, p, None) == INVALID           # ldgu < 2F
+    assert z(p, 260, p, p, 100, 4, 128, p, p, None) == ALIGN             # ldgu % 8 != 0
+
 
 
 def test_balance_rejections(L):

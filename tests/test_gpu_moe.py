@@ -174,3 +174,43 @@ def test_uneven_and_empty_experts(counts):
         cw, sw = oracle.quantize(W[e], s_np[e])
         da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
         check_gemm(bf16_to_np(Y[lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
+
+
+@pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 7, 64, 127))])
+def test_down_fused_swiglu(name, experts):
+    """Down-projection input formed from the gate+up GEMM's own output:
+    h = bf16(SiLU(g) * u) fused with the grouped transform (bit-exact against
+    the oracle's SwiGLU step and transform), then the down GEMM."""
+    d = moe(name)
+    wl = d["workload"]
+    E, F, Kh = wl.E, wl.F, wl.K
+    gu = run_gate_up(d)
+    r = d["routing"]
+    off = r["offsets"].numpy()
+    rows_n = int(off[-1])
+    offs = to_dev(r["offsets"])
+    rng = np.random.default_rng(3)
+    s_np = rng.uniform(0.1, 10.0, (E, F)).astype(np.float32)
+    inv_np = (np.float32(1.0) / s_np).astype(np.float32)
+    W = to_dev(d["W_down"])
+    w_codes, w_scales = mq.macaq_quant_weight_grouped(W, torch.from_numpy(s_np).to(DEV))
+    a_codes, a_scales = mq.macaq_quant_act_grouped_silu(gu["Y"], offs, torch.from_numpy(inv_np).to(DEV),
+                                                        rows_n, E)
+    Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, Kh, F)
+    torch.cuda.synchronize()
+    H = oracle.silu_mul(gu["Y"].cpu())                 # bf16 bits [rows, F]
+    pos = padded_positions(off)
+    P = a_codes.shape[0]
+    sc = untile_scales(u8(a_scales), P, F)
+    used = int(np.sum((np.diff(off) + 127) // 128 * 128))
+    assert not sc[np.setdiff1d(np.arange(used), pos)].any()   # padding rows: zero scales
+    for e in (range(E) if experts is None else experts):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        ca, sa = oracle.quantize(H[lo:hi], inv_np[e])
+        np.testing.assert_array_equal(u8(a_codes)[pos[lo:hi]], ca)
+        np.testing.assert_array_equal(sc[pos[lo:hi]], sa)
+        cw, sw = oracle.quantize(d["W_down"][e], s_np[e])
+        da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+        check_gemm(bf16_to_np(Y[lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), F)

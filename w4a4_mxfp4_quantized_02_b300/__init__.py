@@ -53,6 +53,7 @@ _SIGS = {
     "macaq_linear": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
                      ctypes.c_int),
     "macaq_linear_no_alloc": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_quant_act_grouped_silu": ([_P, _I64, _P, _P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_quant_act_grouped": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P],
                                 ctypes.c_int),
     "macaq_grouped_w4a4_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P],
@@ -242,6 +243,24 @@ def macaq_quant_act_grouped(X, row_src, expert_offsets, inv_s, rows: int, E: int
         a_scales = torch.empty(macaq_scale_bytes(P, K), dtype=torch.uint8, device=X.device)
     _check("macaq_quant_act_grouped", lib().macaq_quant_act_grouped(
         _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
+        _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    return a_codes, a_scales
+
+
+def macaq_quant_act_grouped_silu(GU, expert_offsets, inv_s, rows: int, E: int, a_codes=None,
+                                 a_scales=None, stream=None):
+    """Down-projection input of the grouped experts: h = bf16(SiLU(g) * u) of the
+    gate|up GEMM output GU [rows, 2F] (sorted rows), transformed into the
+    expert-padded MXFP4 layout (see the header)."""
+    _dev(GU, "GU")
+    F = GU.shape[1] // 2
+    P = macaq_grouped_padded_rows(rows, E)
+    if a_codes is None:
+        a_codes = torch.empty(P, F // 2, dtype=torch.uint8, device=GU.device)
+    if a_scales is None:
+        a_scales = torch.empty(macaq_scale_bytes(P, F), dtype=torch.uint8, device=GU.device)
+    _check("macaq_quant_act_grouped_silu", lib().macaq_quant_act_grouped_silu(
+        _ptr(GU), _ld(GU), _ptr(expert_offsets), _ptr(inv_s), rows, E, F,
         _ptr(a_codes), _ptr(a_scales), _stream(stream)))
     return a_codes, a_scales
 

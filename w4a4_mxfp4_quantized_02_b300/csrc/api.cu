@@ -223,6 +223,35 @@ macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *
     return from_cuda(launch_quant(QuantMode::ActGrouped, a, static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
+                                          const float *inv_s, int64_t rows, int64_t E, int64_t F,
+                                          uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(F));
+    MACAQ_TRY(check_rows(rows));
+    if (E <= 0) return MACAQ_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
+    if (grouped_padded_rows(rows, E) > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (!expert_offsets || !inv_s || !a_codes || !a_scales) return MACAQ_ERR_INVALID_ARG;
+    if (rows > 0 && (!GU || ldgu < 2 * F)) return MACAQ_ERR_INVALID_ARG;
+    if ((GU && !aligned16(GU)) || !aligned16(inv_s) || !aligned16(a_codes) || !aligned16(a_scales) ||
+        (GU && ldgu % 8 != 0))
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(GU);
+    a.ld_src = ldgu;
+    a.row_src = nullptr;
+    a.offsets = expert_offsets;
+    a.f = inv_s;
+    a.K = F;
+    a.rows_valid = rows;
+    a.rows_out = grouped_padded_rows(rows, E);
+    a.E = static_cast<int32_t>(E);
+    a.codes = a_codes;
+    a.scales = a_scales;
+    return from_cuda(launch_quant(QuantMode::ActGroupedSilu, a, static_cast<cudaStream_t>(stream)));
+}
+
 macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                                      const uint8_t *w_codes, const uint8_t *w_scales,
                                      const int32_t *expert_offsets, int64_t rows, int64_t E,

@@ -24,7 +24,9 @@ inline int64_t grouped_padded_rows(int64_t rows, int64_t E)
     return pad_rows(rows + (kRowTile - 1) * E);
 }
 
-enum class QuantMode : int { Dense = 0, WeightGrouped = 1, ActGrouped = 2 };
+// ActGroupedSilu: the grouped activation transform of h = SiLU(g) * u read from
+// a [rows, 2F] gate|up matrix in sorted row order (K = F).
+enum class QuantMode : int { Dense = 0, WeightGrouped = 1, ActGrouped = 2, ActGroupedSilu = 3 };
 
 struct QuantArgs {
     const uint16_t *src;      // bf16 bits

@@ -19,6 +19,7 @@
 // Every arithmetic step uses explicitly rounded intrinsics (and the file is
 // built with -fmad=false) so the codes are bit-exact against an fp32 CPU
 // statement of the same steps.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -418,6 +419,55 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
 
 // ------------------------------------------------ TMA-staged dense variant
 
+// ------------------------------------------------------------- SwiGLU step
+//
+// h = bf16( SiLU(g) * u ), SiLU(g) = g / (1 + e^-g), in fp32 with round to
+// nearest at every operation (the file is built with -fmad=false and the
+// operations are explicit).  e^x: Cody-Waite range reduction x = n ln2 + r
+// (ln2 split into a 16-bit head, so n * head is exact, and a tail), the
+// Taylor series of e^r to r^8 / 8! by Horner (|r| <= 0.35, truncation below
+// 2^-30 relative), then the scaling by 2^n, in two steps where 2^n is not a
+// normal float.  Within 1.2 ulp of e^x over the normal range.
+__device__ __forceinline__ float pow2i(int k)  // 2^k, -126 <= k <= 127
+{
+    return __int_as_float((k + 127) << 23);
+}
+
+__device__ __forceinline__ float exp_f32(float x)
+{
+    if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
+    if (x < -103.972084045410156f) return 0.0f;
+    const float fn = rintf(__fmul_rn(x, 0x1.715476p+0f));
+    const int n = static_cast<int>(fn);
+    float r = __fsub_rn(x, __fmul_rn(fn, 0x1.62e4p-1f));
+    r = __fsub_rn(r, __fmul_rn(fn, 0x1.7f7d1cp-20f));
+    float q = 0x1.a01a02p-16f;
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.a01a02p-13f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.6c16c2p-10f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.111112p-7f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.555556p-5f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.555556p-3f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p-1f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p+0f);
+    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p+0f);
+    if (n > 127) return __fmul_rn(__fmul_rn(q, 0x1.0p+127f), pow2i(n - 127));
+    if (n < -126) return __fmul_rn(__fmul_rn(q, pow2i(n + 100)), 0x1.0p-100f);
+    return __fmul_rn(q, pow2i(n));
+}
+
+__device__ __forceinline__ uint32_t silu_mul_bf16(float g, float u)
+{
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, exp_f32(-g)));
+    const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(s, u));
+    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&h));
+}
+
+// Two bf16 words of gate and up values -> the word of the two h values.
+__device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
+{
+    return silu_mul_bf16(bf16lo(gw), bf16lo(uw)) | (silu_mul_bf16(bf16hi(gw), bf16hi(uw)) << 16);
+}
+
 // The same transform as quant_block with the natural register pairing
 // v[i] = (element 2i, element 2i+1): the stride-1 stage (fed by products, so
 // scalar) pairs the halves of a register, strides 2, 4, 8, 16 pair whole
@@ -658,7 +708,10 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 // dense kernel; the producer lands each row of a stage with its own TMA box
 // (one row high), so the rows can come from anywhere in X.  The rows of this
 // CTA are resolved once, up front, into a table in shared memory.
-template <int STAGES>
+// kSilu: the rows are the sorted rows of a [rows, 2F] gate|up matrix; each
+// stage lands the gate and the up slab of every row and the consumer forms
+// h = SiLU(g) * u before the transform.
+template <int STAGES, bool kSilu>
 __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
                                                                     int32_t RT, int32_t per_cta)
@@ -670,7 +723,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     const int NC = TB * RT;
     const int cwarps = NC / 32;
     const uint32_t row_bytes = static_cast<uint32_t>(TB * 64);
-    const uint32_t stage_bytes = static_cast<uint32_t>(NC * 64);
+    const uint32_t stage_bytes = static_cast<uint32_t>(NC * 64) * (kSilu ? 2u : 1u);
     const uint32_t full0 = sbase + STAGES * stage_bytes;
     const uint32_t empty0 = full0 + 8 * STAGES;
     uint8_t *misc = qsmem + STAGES * stage_bytes + 16 * STAGES;
@@ -731,7 +784,8 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                 }
                 const int64_t jj = p - s_poff[lo];
                 ex = lo;
-                if (jj < s_off[lo + 1] - s_off[lo]) src = a.row_src[s_off[lo] + jj];
+                if (jj < s_off[lo + 1] - s_off[lo])
+                    src = kSilu ? static_cast<int32_t>(s_off[lo] + jj) : a.row_src[s_off[lo] + jj];
             }
         }
         m_src[idx] = src;
@@ -752,7 +806,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                 if (*abort_flag) break;
                 uint32_t nvalid = 0;
                 for (int i = 0; i < RT; ++i) nvalid += m_src[j * RT + i] >= 0 ? 1u : 0u;
-                ptx::mbar_arrive_expect_tx(full0 + 8 * s, nvalid * row_bytes);
+                ptx::mbar_arrive_expect_tx(full0 + 8 * s, nvalid * row_bytes * (kSilu ? 2u : 1u));
                 for (int i = 0; i < RT; ++i) {
                     const int32_t src = m_src[j * RT + i];
                     if (src < 0) continue;
@@ -761,6 +815,15 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(sbase + s * stage_bytes + i * row_bytes),
                         "l"(&tmX), "r"(full0 + 8 * s), "r"(0), "r"(slab0), "r"(src)
                         : "memory");
+                    if (kSilu) {
+                        // the up slab: K / 32 blocks further along the row
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(sbase + s * stage_bytes + (RT + i) * row_bytes),
+                            "l"(&tmX), "r"(full0 + 8 * s), "r"(0), "r"(slab0 + static_cast<int32_t>(a.K / 32)),
+                            "r"(src)
+                            : "memory");
+                    }
                 }
             }
             for (int32_t k = (j > STAGES ? j - STAGES : 0); k < j; ++k)
@@ -797,6 +860,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
         uint32_t sbyte = 0;
         const bool valid = src >= 0 && has_kb;
         uint32_t raw[16];
+        uint32_t up[kSilu ? 16 : 1];
         if (valid) {
             const uint32_t base = sbase + s * stage_bytes + static_cast<uint32_t>(t) * 64;
 #pragma unroll
@@ -809,6 +873,21 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                 raw[4 * c + 1] = x1;
                 raw[4 * c + 2] = x2;
                 raw[4 * c + 3] = x3;
+            }
+            if (kSilu) {
+                // the up slab sits NC rows of 64 bytes later (same swizzle phase)
+                const uint32_t ubase = base + static_cast<uint32_t>(NC) * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t x0, x1, x2, x3;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                 : "r"(ubase + 16 * (c ^ swz)));
+                    up[4 * c] = x0;
+                    up[4 * c + 1] = x1;
+                    up[4 * c + 2] = x2;
+                    up[4 * c + 3] = x3;
+                }
             }
         }
         // the stage is no longer needed by this warp once its reads are done
@@ -824,6 +903,10 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                     f[2 * q] = make_float2(v4.x, v4.y);
                     f[2 * q + 1] = make_float2(v4.z, v4.w);
                 }
+            }
+            if (kSilu) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) raw[i] = silu_mul_word(raw[i], up[i]);
             }
             uint4 codes;
             sbyte = quant_block_pairs(raw, f, codes);
@@ -938,7 +1021,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // dynamic shared memory each TMA kernel variant has been opened up to.
 struct QuantDevice {
     int sms = 0;
-    int smem_set[4] = {0, 0, 0, 0};
+    int smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
 QuantDevice g_qdev[64];
 std::mutex g_qdev_mu;
@@ -979,7 +1062,8 @@ cudaError_t open_smem(Kern kern, int slot, int64_t smem)
 // (a warp may span rows; TB is a multiple of 8, so every group of four
 // neighbouring blocks sharing a scale word lies in one row), a stage of at
 // most 32 KB, and the fewest idle blocks over the slabs that cover the row.
-bool pick_tma_tile(int64_t nkb_pad, int64_t max_consumers, int64_t *tb_out, int64_t *rt_out)
+bool pick_tma_tile(int64_t nkb_pad, int64_t max_consumers, int64_t max_slab_bytes, int64_t *tb_out,
+                   int64_t *rt_out)
 {
     int64_t best_waste = -1;
     const int64_t s0 = (nkb_pad + 255) / 256;
@@ -988,7 +1072,7 @@ bool pick_tma_tile(int64_t nkb_pad, int64_t max_consumers, int64_t *tb_out, int6
         if (tb > 256) continue;
         int64_t rt = 0;
         for (int64_t r = (max_consumers / tb < 32 ? max_consumers / tb : 32); r >= 1; --r) {
-            if ((tb * r) % 32 == 0 && tb * r * 64 <= 40960) {
+            if ((tb * r) % 32 == 0 && tb * r * 64 <= max_slab_bytes) {
                 rt = r;
                 break;
             }
@@ -1010,7 +1094,7 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
     int64_t tb = 0, rt = 0;
-    if (!pick_tma_tile(nkb_pad, kTmaConsumersMax, &tb, &rt)) return cudaSuccess;
+    if (!pick_tma_tile(nkb_pad, kTmaConsumersMax, 40960, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
     const int64_t stage = tb * rt * 64;
     const int64_t fixed = 16 + tb * 128 + 1024;  // abort flag, balance-factor table, alignment
@@ -1040,15 +1124,16 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_grouped_tma(const QuantArgs &a, cudaStream_t stream, bool *done)
+cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t stream, bool *done)
 {
     *done = false;
     const int64_t nkb = a.K / 32;
     const int64_t nkb_pad = pad_scale_cols(a.K);
     int64_t tb = 0, rt = 0;
-    if (!pick_tma_tile(nkb_pad, kGroupedConsumersMax, &tb, &rt)) return cudaSuccess;
+    // SwiGLU rows land two slabs (gate and up) per row
+    if (!pick_tma_tile(nkb_pad, kGroupedConsumersMax, 32768, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
-    const int64_t stage = tb * rt * 64;
+    const int64_t stage = tb * rt * 64 * (silu ? 2 : 1);
     int sms = 148;
     MACAQ_TRY_CUDA(quant_device(&sms));
     const int64_t groups = (a.rows_out + rt - 1) / rt;
@@ -1060,19 +1145,23 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, cudaStream_t stream, bo
     const int64_t max_rows = per_cta * rt;
     if (max_rows > 4096) return cudaSuccess;  // row table too large: register-staged kernel
     const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 2 * max_rows * 4 + 1024;
-    const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : 4;
+    const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : (4 * stage + 16 * 4 + fixed <= 210 * 1024) ? 4 : 3;
     const int64_t smem = stages * stage + 16 * stages + fixed;
     if (smem > 210 * 1024) return cudaSuccess;
     CUtensorMap tm;
     // the token rows are whatever row_src names (valid by contract): no row bound
-    const uint64_t dims[3] = {32, static_cast<uint64_t>(nkb), 0x7fffffffull};
+    // (SwiGLU: the gate|up row holds 2 * K / 32 blocks)
+    const uint64_t dims[3] = {32, static_cast<uint64_t>(silu ? 2 * nkb : nkb), 0x7fffffffull};
     const uint64_t strides[2] = {64, static_cast<uint64_t>(a.ld_src) * 2};
     const uint32_t box[3] = {32, static_cast<uint32_t>(tb), 1};
     if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaSuccess;
-    auto kern = stages == 6 ? quant_grouped_tma_kernel<6> : quant_grouped_tma_kernel<4>;
-    MACAQ_TRY_CUDA(open_smem(kern, stages == 6 ? 2 : 3, smem));
+    auto kern = silu ? (stages == 6 ? quant_grouped_tma_kernel<6, true>
+                                    : stages == 4 ? quant_grouped_tma_kernel<4, true> : quant_grouped_tma_kernel<3, true>)
+                     : (stages == 6 ? quant_grouped_tma_kernel<6, false>
+                                    : stages == 4 ? quant_grouped_tma_kernel<4, false> : quant_grouped_tma_kernel<3, false>);
+    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : stages == 4 ? 1 : 2) + (silu ? 3 : 0) + 2, smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -1102,11 +1191,13 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
         cudaError_t err = launch_quant_dense_tma(a, stream, &done);
         if (err != cudaSuccess || done) return err;
     }
-    if (mode == QuantMode::ActGrouped && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
+    if ((mode == QuantMode::ActGrouped || mode == QuantMode::ActGroupedSilu) && (a.ld_src * 2) % 16 == 0 &&
+        a.rows_valid >= 1) {
         bool done = false;
-        cudaError_t err = launch_quant_grouped_tma(a, stream, &done);
+        cudaError_t err = launch_quant_grouped_tma(a, mode == QuantMode::ActGroupedSilu, stream, &done);
         if (err != cudaSuccess || done) return err;
     }
+    if (mode == QuantMode::ActGroupedSilu) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
     int sms = 148;
