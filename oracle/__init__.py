@@ -53,6 +53,8 @@ def lib():
             "oracle_balance_scales": [P, I, P, I, I, P, P],
             "oracle_transform_f32": [P, I, I, P, P],
             "oracle_transform_f64": [P, I, I, P, P],
+            "oracle_transform64_f32": [P, I, I, P, P],
+            "oracle_transform64_f64": [P, I, I, P, P],
             "oracle_quantize_mx": [P, I, I, P, P],
             "oracle_quant": [P, I, I, P, P, P, P],
             "oracle_dequant": [P, P, I, I, P],
@@ -117,22 +119,26 @@ def balance_scales(X_calib, W) -> tuple[np.ndarray, np.ndarray]:
 
 # ------------------------------------------------------------ transform
 
-def transform_f32(X, f: np.ndarray) -> np.ndarray:
+def transform_f32(X, f: np.ndarray, hb: int = 32) -> np.ndarray:
+    """Balance by f and rotate every block of hb (32 or 64) channels, fp32."""
     x = bf16_bits(X)
     rows, K = x.shape
-    assert K % 32 == 0
+    assert hb in (32, 64) and K % hb == 0
     f = np.ascontiguousarray(f, dtype=np.float32)
     y = np.empty((rows, K), np.float32)
-    lib().oracle_transform_f32(_p(x), rows, K, _p(f), _p(y))
+    fn = lib().oracle_transform_f32 if hb == 32 else lib().oracle_transform64_f32
+    fn(_p(x), rows, K, _p(f), _p(y))
     return y
 
 
-def transform_f64(X: np.ndarray, f: np.ndarray) -> np.ndarray:
+def transform_f64(X: np.ndarray, f: np.ndarray, hb: int = 32) -> np.ndarray:
     x = np.ascontiguousarray(X, dtype=np.float64)
     rows, K = x.shape
+    assert hb in (32, 64) and K % hb == 0
     f = np.ascontiguousarray(f, dtype=np.float64)
     y = np.empty((rows, K), np.float64)
-    lib().oracle_transform_f64(_p(x), rows, K, _p(f), _p(y))
+    fn = lib().oracle_transform_f64 if hb == 32 else lib().oracle_transform64_f64
+    fn(_p(x), rows, K, _p(f), _p(y))
     return y
 
 
@@ -148,9 +154,10 @@ def quantize_mx(Y: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
-def quantize(X, f: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    """Balance by f, 32-block Hadamard and MXFP4-encode bf16 rows X [rows,K]."""
-    return quantize_mx(transform_f32(X, f))
+def quantize(X, f: np.ndarray, hb: int = 32) -> tuple[np.ndarray, np.ndarray]:
+    """Balance by f, hb-block Hadamard (32 or 64) and MXFP4-encode bf16 rows X
+    [rows,K] (MX blocks of 32 either way)."""
+    return quantize_mx(transform_f32(X, f, hb))
 
 
 def e2m1_encode(t: np.ndarray) -> np.ndarray:

@@ -19,6 +19,11 @@
  *                    before rounding.  Normalised Sylvester order 32, applied
  *                    as butterflies at strides 1, 2, 4, 8, 16 and one multiply
  *                    by fp32(1/sqrt 32).
+ *   64-wide variant  (page "Huawei MACaQ Is an Open-Source Model Quantizer",
+ *                    section on the llama.cpp recipe: a Hadamard block of 32 or
+ *                    64 channels.)  Sylvester order 64 as butterflies at strides
+ *                    1 .. 32, then one multiply by 1/8; the MX blocks stay 32
+ *                    wide, so one Hadamard block spans two of them.
  *   MXFP4 encode     same page, FAQ "What is W4A4 quantization": 4-bit floats
  *                    in blocks of 32 sharing one scale.  Scale exponent
  *                    floor(log2 amax) - 2 (E8M0), element grid E2M1
@@ -141,6 +146,69 @@ static void fwht32_f64(double v[32])
     }
     const double c = 1.0 / sqrt(32.0);
     for (int i = 0; i < 32; ++i) v[i] = v[i] * c;
+}
+
+/* One 64-channel block: butterflies at strides 1, 2, 4, 8, 16, 32, then the
+ * 1/sqrt(64) = 1/8 normalisation (an exact power of two). */
+static void fwht64_f32(float v[64])
+{
+    for (int h = 1; h < 64; h <<= 1) {
+        for (int i = 0; i < 64; ++i) {
+            if (i & h) continue;
+            float a = v[i];
+            float b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+    for (int i = 0; i < 64; ++i) v[i] = v[i] * 0.125f;
+}
+
+static void fwht64_f64(double v[64])
+{
+    for (int h = 1; h < 64; h <<= 1) {
+        for (int i = 0; i < 64; ++i) {
+            if (i & h) continue;
+            double a = v[i];
+            double b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+    for (int i = 0; i < 64; ++i) v[i] = v[i] * 0.125;
+}
+
+/* The transform with a 64-channel Hadamard block (k % 64 == 0). */
+void oracle_transform64_f32(const uint16_t *x, int64_t rows, int64_t k, const float *f, float *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 64; ++b) {
+            float v[64];
+            for (int i = 0; i < 64; ++i) {
+                int64_t j = 64 * b + i;
+                v[i] = bf16_bits_to_f32(x[r * k + j]) * f[j];
+            }
+            fwht64_f32(v);
+            for (int i = 0; i < 64; ++i) y[r * k + 64 * b + i] = v[i];
+        }
+    }
+}
+
+void oracle_transform64_f64(const double *x, int64_t rows, int64_t k, const double *f, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 64; ++b) {
+            double v[64];
+            for (int i = 0; i < 64; ++i) {
+                int64_t j = 64 * b + i;
+                v[i] = x[r * k + j] * f[j];
+            }
+            fwht64_f64(v);
+            for (int i = 0; i < 64; ++i) y[r * k + 64 * b + i] = v[i];
+        }
+    }
 }
 
 /* y = (x . diag(f)) . (I_{k/32} kron H32), fp32.  x: bf16 bits [rows, k];

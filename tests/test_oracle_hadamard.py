@@ -106,3 +106,50 @@ def test_fp32_route_within_error_bound(orc, name):
     l1 = np.abs(xf).reshape(X.shape[0], K // 32, 32).sum(-1)
     bound = 9 * 2.0 ** -24 / np.sqrt(32.0) * np.repeat(l1, 32, axis=1)
     assert np.all(np.abs(y32 - y64) <= bound)
+
+
+# ------------------------------------------------ 64-channel Hadamard blocks
+# (the recipe's Hadamard block of 64: page "Huawei MACaQ Is an Open-Source
+# Model Quantizer", llama.cpp recipe; the MX blocks stay 32 wide)
+
+def test_h64_unit_vectors_give_scipy_hadamard(orc):
+    H = orc.transform_f64(np.eye(64), np.ones(64), hb=64)
+    ref = scipy.linalg.hadamard(64).astype(np.float64) / 8.0
+    np.testing.assert_allclose(H, ref, rtol=0, atol=1e-16)
+    np.testing.assert_allclose(H.T @ H, np.eye(64), rtol=0, atol=1e-15)
+
+
+def test_h64_is_h2_kron_h32(orc):
+    """Sylvester recursion: H64 = H2 (x) H32 (scaled), i.e. the 64-point output is
+    the sum / difference of the two 32-point outputs of its halves over sqrt 2."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((5, 64))
+    f = rng.uniform(0.5, 2.0, 64)
+    y64 = orc.transform_f64(x, f, hb=64)
+    y32 = orc.transform_f64(x, f, hb=32)
+    lo, hi = y32[:, :32], y32[:, 32:]
+    np.testing.assert_allclose(y64[:, :32], (lo + hi) / np.sqrt(2.0), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(y64[:, 32:], (lo - hi) / np.sqrt(2.0), rtol=0, atol=1e-13)
+
+
+def test_h64_fp32_unit_vectors_are_exact(orc):
+    # with 1/8 exact, e_j through the fp32 route gives exactly +-0.125
+    x = np.zeros((64, 64), np.uint16)
+    x[np.arange(64), np.arange(64)] = 0x3F80
+    y = orc.transform_f32(x, np.ones(64, np.float32), hb=64)
+    np.testing.assert_array_equal(y, scipy.linalg.hadamard(64).astype(np.float32) / 8.0)
+
+
+@pytest.mark.parametrize("name,rows,wrows", [("tiny", None, None), ("attn", 16, 32)])
+def test_h64_fold_identity(orc, name, rows, wrows):
+    """The fold holds for 64-channel blocks too (within 1e-10 normwise, fp64)."""
+    wl = workloads.DENSE[name]
+    d = workloads.make_dense(wl, with_weight=(name == "tiny"))
+    W = d["W"] if "W" in d else workloads.make_weight(wrows, wl.K, seed=8)
+    X = d["X"][:rows] if rows else d["X"]
+    s, _ = orc.balance_scales(d["X_calib"], W)
+    s64 = s.astype(np.float64)
+    x64, w64 = orc.bf16_to_f64(X), orc.bf16_to_f64(W)
+    y_fold = orc.transform_f64(x64, 1.0 / s64, hb=64) @ orc.transform_f64(w64, s64, hb=64).T
+    y = x64 @ w64.T
+    assert np.max(np.abs(y_fold - y)) <= 1e-10 * np.max(np.abs(y))
