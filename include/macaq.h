@@ -112,6 +112,23 @@ macaq_status macaq_quant_act(const void *X, int64_t ldx, const float *inv_s, int
 macaq_status macaq_quant_weight(const void *W, const float *s, int64_t N, int64_t K,
                                 uint8_t *w_codes, uint8_t *w_scales, macaq_stream_t stream);
 
+/* The transform with a Hadamard block of `hadamard_block` channels: 32 (as
+ * macaq_quant_act / macaq_quant_weight) or 64.  The 64-channel block is the
+ * recipe's "--had-block 64" option (page "Huawei MACaQ Is an Open-Source
+ * Model Quantizer", llama.cpp recipe): the normalised Sylvester matrix of order
+ * 64 (butterflies at strides 1 .. 32, then x 1/8 exactly) replaces H32, so one
+ * Hadamard block spans two MX blocks; the MXFP4 encoding (blocks of 32, E8M0
+ * scales, E2M1 codes, the same layouts) and macaq_w4a4_gemm are unchanged.
+ * Activations and weights of one layer must use the same block (the fold).
+ * K % hadamard_block == 0 (else MACAQ_ERR_INVALID_ARG); other arguments,
+ * layouts and errors as macaq_quant_act / macaq_quant_weight. */
+macaq_status macaq_quant_act_hb(const void *X, int64_t ldx, const float *inv_s, int64_t M, int64_t K,
+                                int64_t hadamard_block, uint8_t *a_codes, uint8_t *a_scales,
+                                macaq_stream_t stream);
+macaq_status macaq_quant_weight_hb(const void *W, const float *s, int64_t N, int64_t K,
+                                   int64_t hadamard_block, uint8_t *w_codes, uint8_t *w_scales,
+                                   macaq_stream_t stream);
+
 /* Grouped (per-expert) weight preparation: E experts, W [E, N, K] bf16,
  * s [E, K] fp32 (expert e uses row e); w_codes [E, N, K/2]; w_scales holds E
  * consecutive tiled arrays of macaq_scale_bytes(N, K) bytes each. */

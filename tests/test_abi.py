@@ -103,6 +103,16 @@ def test_grouped_rejections(L):
 
 
 
+def test_hadamard_block_rejections(L):
+    q = L.macaq_quant_act_hb
+    w = L.macaq_quant_weight_hb
+    p = _fake()
+    assert q(p, 128, p, 4, 128, 16, p, p, None) == INVALID      # block neither 32 nor 64
+    assert q(p, 96, p, 4, 96, 64, p, p, None) == INVALID        # K % 64 != 0
+    assert w(p, p, 4, 96, 64, p, p, None) == INVALID
+    assert q(p, 128, p, 0, 128, 64, p, p, None) == OK           # M = 0: nothing to do
+
+
 def test_balance_rejections(L):
     b = L.macaq_balance_scales
     p = _fake()

@@ -117,3 +117,47 @@ def test_e2m1_encoder_matches_oracle():
     t = np.concatenate([t.astype(np.float32), extra, rnd, tiny])
     got = mq.macaq_debug_e2m1(torch.from_numpy(t).to(DEV)).cpu().numpy()
     np.testing.assert_array_equal(got, oracle.e2m1_encode(t))
+
+
+# ------------------------------------------------ 64-channel Hadamard blocks
+
+@pytest.mark.parametrize("M,K,ld_pad", [(1, 64, 0), (5, 192, 8), (130, 320, 0), (300, 1024, 16),
+                                        (64, 5120, 0), (7, 8192, 0)])
+def test_quant_h64_bitexact(M, K, ld_pad):
+    """The 64-channel Hadamard variant (the recipe's Hadamard block of 64):
+    codes and scales bit-exact against the oracle's fwht64 route."""
+    X = workloads.make_matrix(M, K + ld_pad, seed=M * 11 + K, outlier_channels=(1, K // 3, K - 2))
+    f = np.random.default_rng(M + 3 * K).uniform(0.01, 100.0, K).astype(np.float32)
+    codes, scales = mq.macaq_quant_act_hb(to_dev(X)[:, :K], torch.from_numpy(f).to(DEV), 64)
+    torch.cuda.synchronize()
+    c_ref, s_ref = oracle.quantize(X[:, :K].contiguous(), f, hb=64)
+    np.testing.assert_array_equal(u8(codes), c_ref)
+    np.testing.assert_array_equal(u8(scales), oracle.tile_scales(s_ref))
+    # the 32-block entry point through the same API is the default transform
+    c32, s32 = mq.macaq_quant_act_hb(to_dev(X)[:, :K], torch.from_numpy(f).to(DEV), 32)
+    torch.cuda.synchronize()
+    c32_ref, _ = oracle.quantize(X[:, :K].contiguous(), f)
+    np.testing.assert_array_equal(u8(c32), c32_ref)
+
+
+def test_linear_h64_attn_rows():
+    """A 64-block layer end to end: both sides folded with H64, GEMM unchanged."""
+    d = dense("attn")
+    wl = d["workload"]
+    s_ref, inv_ref = oracle.balance_scales(d["X_calib"], d["W"])
+    W = to_dev(d["W"])
+    w_codes, w_scales = mq.macaq_quant_weight_hb(W, torch.from_numpy(s_ref).to(DEV), 64)
+    X = to_dev(d["X"])
+    a_codes, a_scales = mq.macaq_quant_act_hb(X, torch.from_numpy(inv_ref).to(DEV), 64)
+    Y = mq.macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, wl.M, wl.N, wl.K)
+    torch.cuda.synchronize()
+    cw, sw = oracle.quantize(d["W"], s_ref, hb=64)
+    np.testing.assert_array_equal(u8(w_codes), cw)
+    rows = sample_rows(wl.M, 64)
+    ca, sa = oracle.quantize(d["X"][torch.from_numpy(rows)], inv_ref, hb=64)
+    np.testing.assert_array_equal(u8(a_codes)[rows], ca)
+    from helpers import bf16_to_np, check_gemm
+    da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+    frac, _ = check_gemm(bf16_to_np(Y[torch.from_numpy(rows).to(DEV)]), oracle.gemm_ref(da, dw),
+                         oracle.abs_gemm_ref(da, dw), wl.K)
+    assert frac > 0.999

@@ -48,6 +48,8 @@ _SIGS = {
     "macaq_balance_scales": ([_P, _I64, _P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_quant_act": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_quant_weight": ([_P, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_act_hb": ([_P, _I64, _P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_weight_hb": ([_P, _P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_quant_weight_grouped": ([_P, _P, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_w4a4_gemm": ([_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_linear": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
@@ -171,6 +173,37 @@ def macaq_quant_weight(W: torch.Tensor, s: torch.Tensor, w_codes=None, w_scales=
         w_scales = torch.empty(macaq_scale_bytes(N, K), dtype=torch.uint8, device=W.device)
     _check("macaq_quant_weight", lib().macaq_quant_weight(
         _ptr(W), _ptr(s), N, K, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
+    return w_codes, w_scales
+
+
+def macaq_quant_act_hb(X: torch.Tensor, inv_s: torch.Tensor, hadamard_block: int, a_codes=None,
+                       a_scales=None, stream=None):
+    """macaq_quant_act with a Hadamard block of 32 or 64 channels."""
+    _dev(X, "X")
+    M, K = X.shape
+    if a_codes is None:
+        a_codes = torch.empty(M, K // 2, dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty(macaq_scale_bytes(M, K), dtype=torch.uint8, device=X.device)
+    _check("macaq_quant_act_hb", lib().macaq_quant_act_hb(
+        _ptr(X), _ld(X), _ptr(inv_s), M, K, hadamard_block, _ptr(a_codes), _ptr(a_scales),
+        _stream(stream)))
+    return a_codes, a_scales
+
+
+def macaq_quant_weight_hb(W: torch.Tensor, s: torch.Tensor, hadamard_block: int, w_codes=None,
+                          w_scales=None, stream=None):
+    """macaq_quant_weight with a Hadamard block of 32 or 64 channels."""
+    _dev(W, "W")
+    N, K = W.shape
+    if W.stride(0) != K or W.stride(1) != 1:
+        raise ValueError("W must be contiguous [N, K]")
+    if w_codes is None:
+        w_codes = torch.empty(N, K // 2, dtype=torch.uint8, device=W.device)
+    if w_scales is None:
+        w_scales = torch.empty(macaq_scale_bytes(N, K), dtype=torch.uint8, device=W.device)
+    _check("macaq_quant_weight_hb", lib().macaq_quant_weight_hb(
+        _ptr(W), _ptr(s), N, K, hadamard_block, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
     return w_codes, w_scales
 
 

@@ -87,6 +87,40 @@ macaq_status macaq_balance_scales(const void *Xc, int64_t ldxc, const int32_t *x
                                     static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_quant_act_hb(const void *X, int64_t ldx, const float *inv_s, int64_t M, int64_t K,
+                                int64_t hadamard_block, uint8_t *a_codes, uint8_t *a_scales,
+                                macaq_stream_t stream)
+{
+    if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_k(K));
+    if (K % hadamard_block != 0) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_rows(M));
+    if (M == 0) return MACAQ_OK;
+    if (!X || !inv_s || !a_codes || !a_scales || ldx < K) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(inv_s) || !aligned16(a_codes) || !aligned16(a_scales) ||
+        ldx % 8 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(X);
+    a.ld_src = ldx;
+    a.f = inv_s;
+    a.K = K;
+    a.rows_valid = M;
+    a.rows_out = pad_rows(M);
+    a.E = 1;
+    a.codes = a_codes;
+    a.scales = a_scales;
+    a.had = static_cast<int32_t>(hadamard_block);
+    return from_cuda(launch_quant(QuantMode::Dense, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_quant_weight_hb(const void *W, const float *s, int64_t N, int64_t K,
+                                   int64_t hadamard_block, uint8_t *w_codes, uint8_t *w_scales,
+                                   macaq_stream_t stream)
+{
+    return macaq_quant_act_hb(W, K, s, N, K, hadamard_block, w_codes, w_scales, stream);
+}
+
 macaq_status macaq_quant_act(const void *X, int64_t ldx, const float *inv_s, int64_t M, int64_t K,
                              uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
 {

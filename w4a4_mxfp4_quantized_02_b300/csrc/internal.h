@@ -42,6 +42,7 @@ struct QuantArgs {
     uint8_t *codes;
     uint8_t *scales;
     size_t scale_group_stride;  // WeightGrouped: tiled_scale_bytes(N, K)
+    int32_t had = 32;           // Hadamard block: 32, or 64 (Dense only)
 };
 
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream);

@@ -473,6 +473,13 @@ __device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
 // scalar) pairs the halves of a register, strides 2, 4, 8, 16 pair whole
 // registers i and i + h/2 and run as packed adds; the bf16 words and the
 // output bytes already come in this pairing.
+//
+// kH64: the block is one half of a 64-channel Hadamard block whose other half
+// is held by the neighbouring lane (lane ^ 1; the even lane holds the lower
+// half).  After the five 32-point stages the stride-32 stage pairs element i
+// of the two halves through a shuffle, and the normalisation is the exact
+// 1/8; the MX block stays these 32 values.
+template <bool kH64>
 __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
                                                       uint4 &codes)
 {
@@ -497,6 +504,17 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
             v[i + hh] = __fadd2_rn(a, make_float2(-b.x, -b.y));
         }
     }
+    if (kH64) {
+        const unsigned mask = __activemask();
+        const bool upper = (threadIdx.x & 1u) != 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 p = make_float2(__shfl_xor_sync(mask, v[i].x, 1), __shfl_xor_sync(mask, v[i].y, 1));
+            // lower half: a + b; upper half: a - b with a the lower's value
+            v[i] = upper ? __fadd2_rn(p, make_float2(-v[i].x, -v[i].y)) : __fadd2_rn(v[i], p);
+        }
+    }
+    constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
     float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -504,18 +522,18 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
         m1 = fmaxf(m1, fabsf(v[i].y));
     }
     const float vmax = fmaxf(m0, m1);
-    const float amax = __fmul_rn(vmax, kInvSqrt32);
+    const float amax = __fmul_rn(vmax, kNorm);
     const int ef = static_cast<int>(__float_as_uint(amax) >> 23);
     const uint32_t sbyte = static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
     const int se = static_cast<int>(sbyte) - 127;
     if (se >= -124 && se <= 122) {
-        const float g = __int_as_float(__float_as_int(kInvSqrt32) - se * (1 << 23));
+        const float g = __int_as_float(__float_as_int(kNorm) - se * (1 << 23));
         const float2 g2 = make_float2(g, g);
         // the scaled values feed only the encoder: no add follows this multiply
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], g2);
     } else {
-        const float c = kInvSqrt32;
+        const float c = kNorm;
         const float inv = __uint_as_float((254u - sbyte) << 23);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -553,7 +571,7 @@ constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
 constexpr int kGroupedConsumersMax = 512;
 constexpr int kGroupedThreadsMax = kGroupedConsumersMax + 32;
 
-template <int STAGES>
+template <int STAGES, bool kH64>
 __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                   QuantArgs a, int32_t groups, int32_t TB,
                                                                   int32_t RT)
@@ -682,7 +700,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
                 f[2 * c + 1] = make_float2(x2, x3);
             }
             uint4 codes;
-            sbyte = quant_block_pairs(raw, f, codes);
+            sbyte = quant_block_pairs<kH64>(raw, f, codes);
             *reinterpret_cast<uint4 *>(a.codes + r * half_k + 16 * kb) = codes;
         } else {
             __syncwarp();
@@ -909,7 +927,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                 for (int i = 0; i < 16; ++i) raw[i] = silu_mul_word(raw[i], up[i]);
             }
             uint4 codes;
-            sbyte = quant_block_pairs(raw, f, codes);
+            sbyte = quant_block_pairs<false>(raw, f, codes);
             *reinterpret_cast<uint4 *>(a.codes + p * half_k + 16 * kb) = codes;
         }
         uint32_t word = sbyte << (8 * (lane & 3));
@@ -1021,7 +1039,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // dynamic shared memory each TMA kernel variant has been opened up to.
 struct QuantDevice {
     int sms = 0;
-    int smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int smem_set[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 QuantDevice g_qdev[64];
 std::mutex g_qdev_mu;
@@ -1114,8 +1132,9 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     int64_t ctas_y = sms / slabs;  // one CTA per SM: never a partial second wave
     ctas_y = ctas_y < 1 ? 1 : ctas_y;
     ctas_y = ctas_y > groups ? groups : ctas_y;
-    auto kern = stages == 6 ? quant_dense_tma_kernel<6> : quant_dense_tma_kernel<4>;
-    MACAQ_TRY_CUDA(open_smem(kern, stages == 6 ? 0 : 1, smem));
+    auto kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true> : quant_dense_tma_kernel<4, true>)
+                            : (stages == 6 ? quant_dense_tma_kernel<6, false> : quant_dense_tma_kernel<4, false>);
+    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : 1) + (a.had == 64 ? 8 : 0), smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -1198,6 +1217,7 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
         if (err != cudaSuccess || done) return err;
     }
     if (mode == QuantMode::ActGroupedSilu) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
+    if (a.had == 64) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
     int sms = 148;
