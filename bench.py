@@ -330,7 +330,8 @@ def gpu_arm(args, rank: int, world: int):
     Xc = d["X_calib"].to(dev)
     W = d["W"].to(dev)
     s, inv = mq.macaq_balance_scales(Xc, W)
-    w_codes, w_scales = mq.macaq_quant_weight(W, s)
+    hb = args.hadamard_block
+    w_codes, w_scales = mq.macaq_quant_weight_hb(W, s, hb)
     del W, Xc
 
     ws_bytes = mq.macaq_linear_workspace_bytes(M, K)
@@ -352,7 +353,7 @@ def gpu_arm(args, rank: int, world: int):
         b = sets[i % nsets]
         if ev is not None:
             ev[0].record(stream)
-        mq.macaq_quant_act(b["X"], inv, b["a_codes"], b["a_scales"])
+        mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
         if ev is not None:
             ev[1].record(stream)
         mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
@@ -409,13 +410,20 @@ def gpu_arm(args, rank: int, world: int):
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
 
     # end to end through the C ABI: pinned host X in, pinned host Y out
+    def layer(b):
+        if hb == 32:
+            mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+        else:
+            mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
+            mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
+
     e2e_steps = max(3, min(args.steps, 50))
     Xh = d["X"].pin_memory()
     Yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
     b = sets[0]
     for _ in range(2):
         b["X"].copy_(Xh, non_blocking=True)
-        mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+        layer(b)
         Yh.copy_(b["Y"], non_blocking=True)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -423,7 +431,7 @@ def gpu_arm(args, rank: int, world: int):
     e0.record(stream)
     for _ in range(e2e_steps):
         b["X"].copy_(Xh, non_blocking=True)
-        mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+        layer(b)
         Yh.copy_(b["Y"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -485,7 +493,7 @@ def gpu_arm(args, rank: int, world: int):
         "vs_baseline": None,
         "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
         "data": "synthetic",
-        "config": workload_config(wl),
+        "config": dict(workload_config(wl), hadamard_block=hb),
         "roofline": roofline,
         "act_quant": {"kernel": "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -819,6 +827,8 @@ def main():
     ap.add_argument("--config", default="attn")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hadamard-block", type=int, choices=[32, 64], default=32,
+                    help="Hadamard block of the transform (dense workloads)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--kernel-events-every", type=int, default=4,

@@ -506,12 +506,15 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
     }
     if (kH64) {
         const unsigned mask = __activemask();
-        const bool upper = (threadIdx.x & 1u) != 0;
+        // lower half: own + partner; upper half: partner - own.  As p + sgn * v
+        // with sgn = +-1 the product is exact, so one fused multiply-add gives
+        // exactly the rounded sum or difference.
+        const float sgn = (threadIdx.x & 1u) ? -1.0f : 1.0f;
+        const float2 sgn2 = make_float2(sgn, sgn);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float2 p = make_float2(__shfl_xor_sync(mask, v[i].x, 1), __shfl_xor_sync(mask, v[i].y, 1));
-            // lower half: a + b; upper half: a - b with a the lower's value
-            v[i] = upper ? __fadd2_rn(p, make_float2(-v[i].x, -v[i].y)) : __fadd2_rn(v[i], p);
+            v[i] = __ffma2_rn(sgn2, v[i], p);
         }
     }
     constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
