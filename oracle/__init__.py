@@ -264,3 +264,25 @@ def silu_mul(GU) -> np.ndarray:
     h = np.empty((rows, F), dtype=np.uint16)
     lib().oracle_silu_mul(_p(bits), rows, F, _p(h))
     return h
+
+
+def f32_to_bf16_bits(y: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bits, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(y, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    return ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+
+
+def transform_bf16(X, f: np.ndarray, hb: int = 32) -> np.ndarray:
+    """W4A16 activations: the fp32 transform (balance, Hadamard) rounded once
+    to bf16, as bits [rows, K]."""
+    return f32_to_bf16_bits(transform_f32(X, f, hb))
+
+
+def dequant_bf16(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """W4A16 weights: the MXFP4 values as bf16 bits (every E2M1 value times an
+    E8M0 power of two from an fp32 input is exact in bf16)."""
+    d = dequant(codes, scales).astype(np.float32)
+    bits = f32_to_bf16_bits(d)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), d), "not exact in bf16"
+    return bits
