@@ -511,6 +511,203 @@ def gpu_arm(args, rank: int, world: int):
     return 0
 
 
+# ------------------------------------------------------- W4A16 GPU arm
+
+METRIC_W4A16 = "W4A16 linear TFLOP/s (bf16 GEMM on expanded MXFP4 weights)"
+
+
+def oracle_w4a16_rate(d, inv, wd, target_s: float):
+    """Time the CPU oracle of the W4A16 layer (bf16 transform of sampled rows,
+    fp64 GEMM against the expanded weight) and return (TFLOP/s, rows, s, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    wl = d["workload"]
+    w64 = (wd.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    def run(n):
+        t0 = time.perf_counter()
+        xt = oracle.transform_bf16(d["X"][:n], inv)
+        a = (xt.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        torch.from_numpy(oracle.gemm_ref(a, w64)).to(torch.bfloat16)
+        return time.perf_counter() - t0
+
+    run(min(wl.M, 4))
+    n = max(1, min(wl.M, 16))
+    dt = run(n)
+    while dt < target_s * 0.5 and n < wl.M:
+        n = min(wl.M, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+        dt = run(n)
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    return 2.0 * n * wl.N * wl.K / dt / 1e12, n, dt, threads
+
+
+def gpu_arm_w4a16(args, rank: int, world: int):
+    """The W4A16 fallback layer: the bf16 transform (this library's kernel) and
+    a bf16 GEMM against weights expanded once from the MXFP4 checkpoint."""
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    import w4a4_mxfp4_quantized_02_b300 as mq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mq.lib()
+    peaks = load_peaks()
+    d = workloads.make_dense(args.config)
+    wl = d["workload"]
+    M, N, K = wl.M, wl.N, wl.K
+    hb = args.hadamard_block
+    stream = torch.cuda.current_stream()
+
+    Xc = d["X_calib"].to(dev)
+    W = d["W"].to(dev)
+    s, inv = mq.macaq_balance_scales(Xc, W)
+    w_codes, w_scales = mq.macaq_quant_weight_hb(W, s, hb)
+    Wd = mq.macaq_dequant_weight_bf16(w_codes, w_scales, N, K)
+    del W, Xc, w_codes, w_scales
+
+    gemm_ws = torch.empty(32 << 20, dtype=torch.uint8, device=dev)
+    step_bytes = M * K * 4 + N * K * 2 + M * N * 2
+    nsets = max(2, math.ceil(2.5 * L2_BYTES / step_bytes) + 1)
+    X0 = d["X"].to(dev)
+    sets = [{"X": X0.clone() if i else X0, "Wd": Wd.clone() if i else Wd,
+             "Xt": torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+             "Y": torch.empty(M, N, dtype=torch.bfloat16, device=dev)} for i in range(nsets)]
+
+    def step(i, ev=None):
+        b = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        mq.macaq_transform_act_bf16(b["X"], inv, hb, Xt=b["Xt"])
+        if ev is not None:
+            ev[1].record(stream)
+        mq.macaq_w4a16_gemm(b["Xt"], b["Wd"], Y=b["Y"], workspace=gemm_ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    chunk = nsets * max(1, math.ceil(8 / nsets))
+    graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
+    plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in plan.event_steps}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(pci_bus_id(dev))
+    with sampler:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(plan.replays):
+            graph.replay()
+        for i in plan.eager_steps:
+            step(i, evs.get(i))
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
+    g_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
+    status = mq.macaq_check_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
+    flops = 2.0 * M * N * K
+    value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    gemm_tflops = flops / (g_ms * 1e-3) / 1e12
+    gemm_bytes = M * K * 2 + N * K * 2 + M * N * 2
+    t_bytes = M * K * 4
+    t_gbs = t_bytes / (q_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI (pinned host X in, Y out)
+    work = torch.empty(mq.macaq_w4a16_linear_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    Xh = d["X"].pin_memory()
+    Yh = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    b = sets[0]
+
+    def layer():
+        b["X"].copy_(Xh, non_blocking=True)
+        mq.macaq_w4a16_linear(b["X"], inv, b["Wd"], hb, Y=b["Y"], workspace=work)
+        Yh.copy_(b["Y"], non_blocking=True)
+
+    for _ in range(2):
+        layer()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        layer()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            wd = sets[0]["Wd"].cpu().view(torch.int16).numpy().view("uint16")
+            import numpy as np
+            rate, rows, dt, threads = oracle_w4a16_rate(d, inv.cpu().numpy().astype(np.float32), wd,
+                                                        args.cpu_seconds)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{rows} of {M} rows (full N={N}, K={K}), {dt:.1f} s; "
+                             "weight expansion outside the timing"}
+        except Exception as e:  # noqa: BLE001 - reported, not fatal
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
+                   "sample": f"failed: {e}"}
+    bf16_peak = peaks["bf16_tflops"]
+    timing = (f"CUDA events around the launch in {len(evs)} of the {args.steps} timed steps "
+              "(includes the launch gap)")
+    if flops / gemm_bytes >= bf16_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
+        roofline = {"bound": "tensor", "kernel": "cuBLASLt bf16 GEMM (library)",
+                    "achieved": gemm_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": gemm_tflops / bf16_peak, "traffic": None,
+                    "peak_note": f"{peaks['source']} bf16 burst", "avg_launch_us": g_ms * 1e3,
+                    "timing": timing}
+    else:
+        gbs = gemm_bytes / (g_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "cuBLASLt bf16 GEMM (library)", "achieved": gbs,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                    "traffic": None, "bytes_per_launch": gemm_bytes,
+                    "peak_note": f"{peaks['source']} HBM copy bandwidth", "tflops": gemm_tflops,
+                    "avg_launch_us": g_ms * 1e3, "timing": timing}
+    line = {
+        "metric": METRIC_W4A16, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp32 transform rounded to bf16; MXFP4 weights expanded to bf16; fp32 accumulate)",
+        "data": "synthetic",
+        "config": dict(workload_config(wl), hadamard_block=hb, precision="w4a16"),
+        "roofline": roofline,
+        "act_transform": {"kernel": "quant_dense_tma_kernel (bf16 output)", "achieved": t_gbs,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": t_gbs / peaks["hbm_gbs"],
+                          "bytes_per_launch": t_bytes, "avg_launch_us": q_ms * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "library_launches_per_step": "1 (cuBLASLt GEMM; may use more than one kernel)",
+        "launch": plan.describe(),
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------- MoE GPU arm
 
 def moe_workload_config(wl):
@@ -829,6 +1026,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--hadamard-block", type=int, choices=[32, 64], default=32,
                     help="Hadamard block of the transform (dense workloads)")
+    ap.add_argument("--precision", choices=["w4a4", "w4a16"], default="w4a4",
+                    help="w4a16: the weight-only fallback (dense workloads)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--kernel-events-every", type=int, default=4,
@@ -849,6 +1048,8 @@ def main():
     try:
         if args.config.startswith("moe"):
             return gpu_arm_moe(args, rank, world)
+        if args.precision == "w4a16":
+            return gpu_arm_w4a16(args, rank, world)
         return gpu_arm(args, rank, world)
     finally:
         if world > 1:

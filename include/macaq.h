@@ -237,6 +237,58 @@ macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_sc
                                      int64_t N, int64_t K, void *Y, int64_t ldy,
                                      macaq_stream_t stream);
 
+/* ------------------------------------------------ W4A16 fallback */
+
+/* The weight-only fallback (page "Huawei MACaQ: Choosing GGUF or vLLM and
+ * Avoiding Setup Mistakes", section "vLLM checkpoints have different
+ * constraints": the W4A16 mode expands the weights for a BF16 matrix
+ * multiplication and is slower than W4A4).  The weights are the same MXFP4
+ * checkpoint (macaq_quant_weight / _hb); the activations keep the online
+ * transform but are not quantised: the fp32 transform is rounded once to
+ * bf16 (this library's reading; the pages state no W4A16 arithmetic).
+ *
+ * macaq_transform_act_bf16: Xt[m, k] = bf16_rn(y) with y the normalised
+ * transform of macaq_quant_act (hadamard_block 32) or macaq_quant_act_hb
+ * (64).  X bf16 [M, ldx]; inv_s fp32 [K]; Xt bf16 [M, ldxt], ldxt >= K, a
+ * multiple of 8; only the first K columns of each row are written.  Errors as
+ * macaq_quant_act_hb. */
+macaq_status macaq_transform_act_bf16(const void *X, int64_t ldx, const float *inv_s, int64_t M,
+                                      int64_t K, int64_t hadamard_block, void *Xt, int64_t ldxt,
+                                      macaq_stream_t stream);
+
+/* Weight expansion: Wd[n, k] = the MXFP4 value (E2M1 code times 2^(scale -
+ * 127)) as bf16, exact for every scale an fp32 input can produce.  w_codes
+ * [N, K/2] and tiled w_scales as macaq_quant_weight writes them; Wd bf16
+ * [N, K] (row pitch K), 16-byte aligned. */
+macaq_status macaq_dequant_weight_bf16(const uint8_t *w_codes, const uint8_t *w_scales, int64_t N,
+                                       int64_t K, void *Wd, macaq_stream_t stream);
+
+/* The W4A16 GEMM alone: Y[m, n] = bf16_rn( sum_k Xt(m, k) * Wd(n, k) ), fp32
+ * accumulation, a plain bf16 library GEMM (cuBLASLt; its algorithm is chosen
+ * once per shape and workspace size and cached).  Xt bf16 [M, ldxt]; Wd bf16
+ * [N, K] row pitch K; Y bf16 [M, ldy]; ldxt and ldy multiples of 8.
+ * workspace: device scratch of ws_bytes bytes (256-byte aligned; may be
+ * NULL with ws_bytes 0).  MACAQ_ERR_UNSUPPORTED if the library offers no
+ * algorithm for the shape within ws_bytes. */
+macaq_status macaq_w4a16_gemm(const void *Xt, int64_t ldxt, const void *Wd, int64_t M, int64_t N,
+                              int64_t K, void *Y, int64_t ldy, void *workspace, size_t ws_bytes,
+                              macaq_stream_t stream);
+
+/* Workspace bytes macaq_w4a16_linear needs for M rows of K channels: the bf16
+ * transform plus the GEMM's scratch. */
+size_t macaq_w4a16_linear_workspace_bytes(int64_t M, int64_t K);
+
+/* The W4A16 layer: macaq_transform_act_bf16 into `workspace`, then
+ *   Y[m, n] = bf16_rn( sum_k Xt(m, k) * Wd(n, k) )  (fp32 accumulation)
+ * with macaq_w4a16_gemm, both on `stream`.  Wd bf16 [N, K] from
+ * macaq_dequant_weight_bf16 (the same hadamard_block as the weights were
+ * prepared with); Y bf16 [M, ldy], ldy >= N, a multiple of 8; workspace as
+ * macaq_linear (256-byte aligned, ws_bytes >=
+ * macaq_w4a16_linear_workspace_bytes(M, K)); errors as macaq_w4a16_gemm. */
+macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, const void *Wd,
+                                int64_t M, int64_t N, int64_t K, int64_t hadamard_block, void *Y,
+                                int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream);
+
 /* --------------------------------------------------- device errors */
 
 /* Every device-side wait of the GEMM kernels is bounded in time.  A wait that

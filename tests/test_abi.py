@@ -113,6 +113,28 @@ def test_hadamard_block_rejections(L):
     assert q(p, 128, p, 0, 128, 64, p, p, None) == OK           # M = 0: nothing to do
 
 
+def test_w4a16_rejections(L):
+    t = L.macaq_transform_act_bf16
+    d = L.macaq_dequant_weight_bf16
+    f = L.macaq_w4a16_linear
+    p = _fake()
+    assert t(p, 128, p, 4, 128, 16, p, 128, None) == INVALID      # block neither 32 nor 64
+    assert t(p, 128, p, 4, 128, 32, p, 64, None) == INVALID       # ldxt < K
+    assert t(p, 128, p, 4, 128, 32, p, 132, None) == ALIGN        # ldxt % 8
+    assert t(p, 128, p, 4, 128, 32, None, 128, None) == INVALID
+    assert t(p, 128, p, 0, 128, 32, p, 128, None) == OK           # M = 0
+    assert d(p, p, 4, 100, p, None) == INVALID                    # K % 32
+    assert d(p, p, 4, 128, _fake(0x10008), None) == ALIGN
+    assert d(p, p, 0, 128, p, None) == OK
+    need = mq.macaq_w4a16_linear_workspace_bytes(16, 128)
+    assert need == 16 * 128 * 2 + (32 << 20)
+    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, None, need, None) == WORKSPACE
+    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, p, need - 1, None) == WORKSPACE
+    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, _fake(0x10010), need, None) == ALIGN
+    assert f(p, 128, p, p, 16, 64, 128, 32, p, 32, p, need, None) == INVALID   # ldy < N
+    assert f(p, 96, p, p, 16, 64, 96, 64, p, 64, p, need, None) == INVALID     # K % 64
+
+
 def test_balance_rejections(L):
     b = L.macaq_balance_scales
     p = _fake()

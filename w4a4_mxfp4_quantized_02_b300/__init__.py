@@ -60,6 +60,12 @@ _SIGS = {
                                 ctypes.c_int),
     "macaq_grouped_w4a4_gemm": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P],
                                 ctypes.c_int),
+    "macaq_transform_act_bf16": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_dequant_weight_bf16": ([_P, _P, _I64, _I64, _P, _P], ctypes.c_int),
+    "macaq_w4a16_linear_workspace_bytes": ([_I64, _I64], _SZ),
+    "macaq_w4a16_gemm": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], ctypes.c_int),
+    "macaq_w4a16_linear": ([_P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
+                           ctypes.c_int),
     "macaq_check_device_error": ([_P], ctypes.c_int),
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
@@ -260,6 +266,70 @@ def macaq_linear_no_alloc(X: torch.Tensor, inv_s, w_codes, w_scales, N: int, Y=N
     _check("macaq_linear_no_alloc", lib().macaq_linear_no_alloc(
         _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
         _stream(stream)))
+    return Y
+
+
+# --------------------------------------------------------- W4A16 fallback
+
+def macaq_transform_act_bf16(X: torch.Tensor, inv_s: torch.Tensor, hadamard_block: int = 32,
+                             Xt=None, stream=None):
+    """The online transform rounded once to bf16 (the W4A16 activation)."""
+    _dev(X, "X")
+    M, K = X.shape
+    if Xt is None:
+        Xt = torch.empty(M, K, dtype=torch.bfloat16, device=X.device)
+    _check("macaq_transform_act_bf16", lib().macaq_transform_act_bf16(
+        _ptr(X), _ld(X), _ptr(inv_s), M, K, hadamard_block, _ptr(Xt), _ld(Xt), _stream(stream)))
+    return Xt
+
+
+def macaq_dequant_weight_bf16(w_codes: torch.Tensor, w_scales: torch.Tensor, N: int, K: int,
+                              Wd=None, stream=None):
+    """MXFP4 weights expanded to bf16 [N, K]."""
+    _dev(w_codes, "w_codes")
+    if Wd is None:
+        Wd = torch.empty(N, K, dtype=torch.bfloat16, device=w_codes.device)
+    _check("macaq_dequant_weight_bf16", lib().macaq_dequant_weight_bf16(
+        _ptr(w_codes), _ptr(w_scales), N, K, _ptr(Wd), _stream(stream)))
+    return Wd
+
+
+def macaq_w4a16_gemm(Xt: torch.Tensor, Wd: torch.Tensor, Y=None, workspace=None, stream=None):
+    """Y = Xt . Wd^T in bf16 (fp32 accumulation): the W4A16 GEMM alone."""
+    _dev(Xt, "Xt")
+    M, K = Xt.shape
+    N = Wd.shape[0]
+    if Wd.shape[1] != K or not Wd.is_contiguous():
+        raise ValueError("Wd must be contiguous [N, K]")
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=Xt.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("macaq_w4a16_gemm", lib().macaq_w4a16_gemm(
+        _ptr(Xt), _ld(Xt), _ptr(Wd), M, N, K, _ptr(Y), _ld(Y), _ptr(workspace), nbytes,
+        _stream(stream)))
+    return Y
+
+
+def macaq_w4a16_linear_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().macaq_w4a16_linear_workspace_bytes(M, K))
+
+
+def macaq_w4a16_linear(X: torch.Tensor, inv_s, Wd: torch.Tensor, hadamard_block: int = 32, Y=None,
+                       workspace=None, stream=None):
+    """W4A16 layer: bf16 transform of X, then Y = Xt . Wd^T (bf16 GEMM)."""
+    _dev(X, "X")
+    M, K = X.shape
+    N = Wd.shape[0]
+    if Wd.shape[1] != K or not Wd.is_contiguous():
+        raise ValueError("Wd must be contiguous [N, K]")
+    if Y is None:
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = torch.empty(max(macaq_w4a16_linear_workspace_bytes(M, K), 1), dtype=torch.uint8,
+                                device=X.device)
+    _check("macaq_w4a16_linear", lib().macaq_w4a16_linear(
+        _ptr(X), _ld(X), _ptr(inv_s), _ptr(Wd), M, N, K, hadamard_block, _ptr(Y), _ld(Y),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return Y
 
 

@@ -5,7 +5,8 @@ only; the quantisation kernels additionally with ``-fmad=false`` (their
 arithmetic must not be contracted into FMAs).  The CUDA runtime is linked
 statically and the driver API is reached through the runtime's entry-point
 query, so the library loads on machines without a GPU driver (for symbol and
-argument checks) and needs no JIT cache at run time.
+argument checks) and needs no JIT cache at run time.  cuBLASLt (the plain bf16
+GEMM of the W4A16 fallback) is the one shared library it links.
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ UNITS = {
     "gemm.cu": [],
     "api.cu": [],
     "static_scratch.cu": [],
+    "w4a16.cu": [],
 }
 HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh"]
 
@@ -52,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             subprocess.check_call(cmd)
     if force or _mtime(LIB) < max(_mtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, *objs]
+        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, *objs, "-lcublasLt"]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.check_call(cmd)

@@ -43,9 +43,18 @@ struct QuantArgs {
     uint8_t *scales;
     size_t scale_group_stride;  // WeightGrouped: tiled_scale_bytes(N, K)
     int32_t had = 32;           // Hadamard block: 32, or 64 (Dense only)
+    bool out_bf16 = false;      // Dense only: bf16 transform into codes viewed as bf16 [rows, ld_out]
+    int64_t ld_out = 0;
 };
 
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream);
+cudaError_t launch_dequant_bf16(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t K,
+                                uint16_t *out, cudaStream_t stream);
+// W4A16: Y[M, N] = Xt[M, K] . Wd[N, K]^T in bf16 with fp32 accumulation
+// (a plain library GEMM; ws is its scratch).
+cudaError_t launch_bf16_gemm_nt(const uint16_t *Xt, int64_t ldx, const uint16_t *Wd, int64_t M, int64_t N,
+                                int64_t K, uint16_t *Y, int64_t ldy, void *ws, size_t ws_bytes,
+                                cudaStream_t stream);
 
 cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_rows, int64_t mc,
                            const uint16_t *w, int64_t n, int64_t k, float *s, float *inv_s,

@@ -480,10 +480,9 @@ __device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
 // of the two halves through a shuffle, and the normalisation is the exact
 // 1/8; the MX block stays these 32 values.
 template <bool kH64>
-__device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
-                                                      uint4 &codes)
+__device__ __forceinline__ void hadamard_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
+                                                     float2 (&v)[16])
 {
-    float2 v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         // one packed multiply for the pair; the stride-1 stage that consumes it
@@ -517,7 +516,32 @@ __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16],
             v[i] = __ffma2_rn(sgn2, v[i], p);
         }
     }
+}
+
+// The W4A16 activation: the normalised transform rounded once to bf16
+// (element 2i in the low half of word i).
+template <bool kH64>
+__device__ __forceinline__ void bf16_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
+                                                 uint32_t (&out)[16])
+{
     constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
+    float2 v[16];
+    hadamard_block_pairs<kH64>(raw, f, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 y = __fmul2_rn(v[i], make_float2(kNorm, kNorm));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(y.x, y.y);
+        out[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+}
+
+template <bool kH64>
+__device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
+                                                      uint4 &codes)
+{
+    constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
+    float2 v[16];
+    hadamard_block_pairs<kH64>(raw, f, v);
     float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -574,7 +598,9 @@ constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
 constexpr int kGroupedConsumersMax = 512;
 constexpr int kGroupedThreadsMax = kGroupedConsumersMax + 32;
 
-template <int STAGES, bool kH64>
+// kBf16: write the normalised transform as bf16 (the W4A16 activation) to
+// a.codes viewed as bf16 [rows, ld_out] instead of MXFP4 codes and scales.
+template <int STAGES, bool kH64, bool kBf16>
 __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                   QuantArgs a, int32_t groups, int32_t TB,
                                                                   int32_t RT)
@@ -702,13 +728,23 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
                 f[2 * c] = make_float2(x0, x1);
                 f[2 * c + 1] = make_float2(x2, x3);
             }
-            uint4 codes;
-            sbyte = quant_block_pairs<kH64>(raw, f, codes);
-            *reinterpret_cast<uint4 *>(a.codes + r * half_k + 16 * kb) = codes;
+            if (kBf16) {
+                // W4A16: the bf16 transform, 64 bytes of row r at block kb
+                uint32_t w[16];
+                bf16_block_pairs<kH64>(raw, f, w);
+                uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (r * a.ld_out + 32 * kb) * 2);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            } else {
+                uint4 codes;
+                sbyte = quant_block_pairs<kH64>(raw, f, codes);
+                *reinterpret_cast<uint4 *>(a.codes + r * half_k + 16 * kb) = codes;
+            }
         } else {
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
         }
+        if (kBf16) continue;
         uint32_t word = sbyte << (8 * (lane & 3));
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
@@ -951,6 +987,49 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     }
 }
 
+// ------------------------------------------------------------ W4A16 weights
+
+// MXFP4 codes and tiled scales -> bf16 values (each E2M1 value times its
+// E8M0 power of two; exact in bf16 for scales an fp32 input can produce).
+// One thread per block of 32 values: 16 code bytes in, 64 bytes out.
+__global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t *codes, const uint8_t *scales,
+                                                           int64_t rows, int64_t K, uint16_t *out)
+{
+    const int64_t nkb = K / 32;
+    const int64_t nka = ((nkb + 7) / 8 * 8) / 4;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= rows * nkb) return;
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    const int64_t r = idx / nkb, kb = idx - (idx / nkb) * nkb;
+    const uint8_t sb = scales[((r / 128) * nka + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4)];
+    // 2^se with se = sb - 127 (sb = 0 gives 2^-127, a subnormal)
+    const float p2 = sb > 0 ? __int_as_float(static_cast<int>(sb) << 23) : __int_as_float(1 << 22);
+    const uint4 c4 = *reinterpret_cast<const uint4 *>(codes + r * (K / 2) + 16 * kb);
+    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t byte = (cw[i >> 2] >> (8 * (i & 3))) & 0xffu;
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t c = (byte >> (4 * h)) & 0xfu;
+            const uint32_t m = c & 7u;
+            // E2M1 magnitude m: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+            const float mag = m < 2 ? 0.5f * static_cast<float>(m)
+                                    : __int_as_float(static_cast<int>(((m >> 1) + 126) << 23) | static_cast<int>((m & 1u) << 22));
+            v[h] = __fmul_rn((c & 8u) ? -mag : mag, p2);
+        }
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[0], v[1]);
+        w[i] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(out + r * K + 32 * kb);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+
 // ---------------------------------------------------------------- balance
 
 __global__ void __launch_bounds__(256) balance_kernel(const uint16_t *xc, int64_t ldxc,
@@ -1042,7 +1121,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // dynamic shared memory each TMA kernel variant has been opened up to.
 struct QuantDevice {
     int sms = 0;
-    int smem_set[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    int smem_set[20] = {};
 };
 QuantDevice g_qdev[64];
 std::mutex g_qdev_mu;
@@ -1135,9 +1214,14 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     int64_t ctas_y = sms / slabs;  // one CTA per SM: never a partial second wave
     ctas_y = ctas_y < 1 ? 1 : ctas_y;
     ctas_y = ctas_y > groups ? groups : ctas_y;
-    auto kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true> : quant_dense_tma_kernel<4, true>)
-                            : (stages == 6 ? quant_dense_tma_kernel<6, false> : quant_dense_tma_kernel<4, false>);
-    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : 1) + (a.had == 64 ? 8 : 0), smem));
+    void (*kern)(CUtensorMap, QuantArgs, int32_t, int32_t, int32_t);
+    if (a.out_bf16)
+        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, true> : quant_dense_tma_kernel<4, true, true>)
+                           : (stages == 6 ? quant_dense_tma_kernel<6, false, true> : quant_dense_tma_kernel<4, false, true>);
+    else
+        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, false> : quant_dense_tma_kernel<4, true, false>)
+                           : (stages == 6 ? quant_dense_tma_kernel<6, false, false> : quant_dense_tma_kernel<4, false, false>);
+    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : 1) + (a.had == 64 ? 8 : 0) + (a.out_bf16 ? 10 : 0), smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -1220,7 +1304,7 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
         if (err != cudaSuccess || done) return err;
     }
     if (mode == QuantMode::ActGroupedSilu) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
-    if (a.had == 64) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
+    if (a.had == 64 || a.out_bf16) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
     int sms = 148;
@@ -1280,6 +1364,16 @@ cudaError_t launch_debug_e2m1(const float *t, int64_t n, uint8_t *codes, cudaStr
 {
     const int64_t blocks = (n + 255) / 256;
     debug_e2m1_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(t, n, codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_bf16(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t K,
+                                uint16_t *out, cudaStream_t stream)
+{
+    const int64_t n = rows * (K / 32);
+    const int64_t blocks = (n + 255) / 256;
+    MACAQ_TRY_CUDA(launch_pdl(dequant_bf16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                              codes, scales, rows, K, out));
     return cudaGetLastError();
 }
 
