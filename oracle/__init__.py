@@ -14,6 +14,9 @@ Passages followed (MACaQ page "What is MACaQ quantization"):
     folded into the weights) -> ``transform_f32`` / ``transform_f64``
   * FAQ "What is W4A4 quantization" (4-bit floats, blocks of 32 sharing one
     scale) -> ``quantize``, ``dequant``
+  * section "How MACaQ works", "Flip Refinement" (Hessian-aware coordinate
+    descent moving single 4-bit codes to an adjacent value when the layer's
+    calibration error falls) -> ``flip_hessian``, ``flip_refine``
 """
 from __future__ import annotations
 
@@ -64,6 +67,8 @@ def lib():
             "oracle_scale_exponent_many": [P, I, P],
             "oracle_silu_mul": [P, I, I, P],
             "oracle_exp_many": [P, I, P],
+            "oracle_flip_hessian": [P, I, I, ctypes.c_float, P],
+            "oracle_flip_refine": [P, P, I, I, ctypes.c_int32, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -286,3 +291,38 @@ def dequant_bf16(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     bits = f32_to_bf16_bits(d)
     assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), d), "not exact in bf16"
     return bits
+
+
+# ------------------------------------------------------- Flip Refinement
+
+def flip_hessian(A: np.ndarray, damp: float = 0.0) -> np.ndarray:
+    """H = A^T A of fp32 calibration rows A [m, k] (each entry a sequential
+    fp32 fused multiply-add over the rows), plus ``damp`` on the diagonal."""
+    a = np.ascontiguousarray(A, dtype=np.float32)
+    m, k = a.shape
+    h = np.empty((k, k), np.float32)
+    lib().oracle_flip_hessian(_p(a), m, k, ctypes.c_float(damp), _p(h))
+    return h
+
+
+def flip_refine(Wt: np.ndarray, H: np.ndarray, codes: np.ndarray, scales: np.ndarray,
+                sweeps: int = 2):
+    """Flip Refinement of round-to-nearest codes [n, k/2] (row-major scales
+    [n, k/32] unchanged) for fp32 transformed weight rows Wt [n, k] against
+    the Hessian H [k, k].  Returns (codes, moves per row)."""
+    wt = np.ascontiguousarray(Wt, dtype=np.float32)
+    h = np.ascontiguousarray(H, dtype=np.float32)
+    n, k = wt.shape
+    assert h.shape == (k, k)
+    c = np.array(codes, dtype=np.uint8, copy=True, order="C")
+    sc = np.ascontiguousarray(scales, dtype=np.uint8)
+    assert c.shape == (n, k // 2) and sc.shape == (n, k // 32)
+    flips = np.zeros(n, np.int32)
+    lib().oracle_flip_refine(_p(wt), _p(h), n, k, int(sweeps), _p(c), _p(sc), _p(flips))
+    return c, flips
+
+
+def flip_error(Wt: np.ndarray, H: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """E = (Wt - q)^T H (Wt - q) per row in fp64 (q the exact dequantised codes)."""
+    r = np.asarray(Wt, np.float64) - dequant(codes, scales)
+    return np.einsum("nk,nk->n", r @ np.asarray(H, np.float64), r)

@@ -39,6 +39,26 @@
  *                    store).  The CUDA path evaluates the same operations in
  *                    the same order; both are pinned against fp64 exp.
  *
+ *   Flip Refinement  (page "What is MACaQ quantization", section "How MACaQ
+ *                    works", step "Flip Refinement": instead of plain round to
+ *                    nearest, a Hessian-aware coordinate descent moves single
+ *                    4-bit weight codes to an adjacent value when that lowers
+ *                    the layer's error on calibration data.)  Stated in the
+ *                    rotated space, where the layer output is A . Wt^T (A the
+ *                    calibration rows through the activation transform, Wt the
+ *                    weight rows through the weight transform, both fp32):
+ *                    H = A^T A (+ damp on the diagonal), and for one weight row
+ *                    the error E(q) = (Wt - q)^T H (Wt - q) of its dequantised
+ *                    codes q.  With r = Wt - q and g = H r, moving q_k by D
+ *                    changes E by D (D H_kk - 2 g_k); coordinates are visited
+ *                    in order k = 0 .. K-1, `sweeps` times; the adjacent grid
+ *                    value (one step down or up the signed E2M1 grid, scale
+ *                    unchanged) with the larger strict decrease is taken (ties
+ *                    to the lower one) and g absorbs the move, g -= D H[k, :].
+ *                    All of it in fp32 with explicit fused multiply-adds in
+ *                    the sums (sequential order) and single roundings
+ *                    elsewhere: the codes depend on every bit of g.
+ *
  * Precision: the transform is stated in fp32 (IEEE, round to nearest, no
  * contraction: build with -ffp-contract=off, no fast-math), because the
  * quantised codes depend on its exact bits.  The fp64 variant exists for the
@@ -50,6 +70,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifdef _OPENMP
@@ -479,4 +500,113 @@ void oracle_silu_mul(const uint16_t *gu, int64_t rows, int64_t F, uint16_t *h)
 void oracle_exp_many(const float *x, int64_t n, float *y)
 {
     for (int64_t i = 0; i < n; ++i) y[i] = oracle_exp_f32(x[i]);
+}
+
+/* ------------------------------------------------------ Flip Refinement */
+
+/* H = A^T A for calibration rows A [m, k] (fp32), each entry a sequential
+ * fused multiply-add over the rows r = 0 .. m-1 starting from +0; `damp` is
+ * then added (one fp32 add) to every diagonal entry. */
+void oracle_flip_hessian(const float *a, int64_t m, int64_t k, float damp, float *h)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < k; ++i) {
+        for (int64_t j = 0; j < k; ++j) {
+            float acc = 0.0f;
+            for (int64_t r = 0; r < m; ++r) acc = fmaf(a[r * k + i], a[r * k + j], acc);
+            if (i == j) acc = acc + damp;
+            h[i * k + j] = acc;
+        }
+    }
+}
+
+/* Magnitudes of the E2M1 grid, by magnitude code 0 .. 7. */
+static float e2m1_magnitude(int mag)
+{
+    return (float)oracle_e2m1_value((uint8_t)mag);
+}
+
+/* Signed grid position of a code: -7 .. 7, both zeros at 0. */
+static int e2m1_position(uint8_t code)
+{
+    int mag = code & 7;
+    return (code & 8) ? -mag : mag;
+}
+
+/* Code of a signed grid position; position 0 gets the sign of the value the
+ * move came from (from_negative), so a zero keeps the side it was reached from. */
+static uint8_t e2m1_code_at(int pos, int from_negative)
+{
+    if (pos > 0) return (uint8_t)pos;
+    if (pos < 0) return (uint8_t)(8 | -pos);
+    return from_negative ? 0x8 : 0x0;
+}
+
+static float e2m1_position_value(int pos)
+{
+    return pos < 0 ? -e2m1_magnitude(-pos) : e2m1_magnitude(pos);
+}
+
+/* Flip Refinement of weight rows wt [n, k] (the fp32 weight transform) whose
+ * round-to-nearest codes [n, k/2] (in/out) and row-major scales [n, k/32] the
+ * MXFP4 step produced, against the Hessian h [k, k] (symmetric).  flips[row]
+ * (if not NULL) receives the number of moves taken. */
+void oracle_flip_refine(const float *wt, const float *h, int64_t n, int64_t k, int32_t sweeps,
+                        uint8_t *codes, const uint8_t *scales, int32_t *flips)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t row = 0; row < n; ++row) {
+        uint8_t *c = codes + row * (k / 2);
+        const uint8_t *sc = scales + row * (k / 32);
+        float *r = (float *)malloc(sizeof(float) * (size_t)k);
+        float *g = (float *)malloc(sizeof(float) * (size_t)k);
+        /* residual of the round-to-nearest codes */
+        for (int64_t j = 0; j < k; ++j) {
+            uint8_t code = (j & 1) ? (c[j / 2] >> 4) : (c[j / 2] & 0xf);
+            float q = ldexpf(e2m1_position_value(e2m1_position(code)), (int)sc[j / 32] - 127);
+            r[j] = wt[row * k + j] - q;
+        }
+        /* g = H r, each entry a sequential fused multiply-add over l */
+        for (int64_t j = 0; j < k; ++j) {
+            float acc = 0.0f;
+            for (int64_t l = 0; l < k; ++l) acc = fmaf(h[j * k + l], r[l], acc);
+            g[j] = acc;
+        }
+        int32_t moves = 0;
+        for (int32_t sw = 0; sw < sweeps; ++sw) {
+            for (int64_t j = 0; j < k; ++j) {
+                uint8_t code = (j & 1) ? (c[j / 2] >> 4) : (c[j / 2] & 0xf);
+                int pos = e2m1_position(code);
+                int se = (int)sc[j / 32] - 127;
+                float t = e2m1_position_value(pos);
+                float hjj = h[j * k + j];
+                float two_g = 2.0f * g[j];
+                int best = 0;          /* 0: stay, -1: down, +1: up */
+                float best_de = 0.0f;
+                float best_d = 0.0f;
+                for (int dir = -1; dir <= 1; dir += 2) {
+                    int np = pos + dir;
+                    if (np < -7 || np > 7) continue;
+                    float d = ldexpf(e2m1_position_value(np) - t, se);
+                    float de = d * (d * hjj - two_g);
+                    if (de < 0.0f && (best == 0 || de < best_de)) {
+                        best = dir;
+                        best_de = de;
+                        best_d = d;
+                    }
+                }
+                if (best == 0) continue;
+                uint8_t nc = e2m1_code_at(pos + best, pos < 0);
+                if (j & 1)
+                    c[j / 2] = (uint8_t)((c[j / 2] & 0x0f) | (nc << 4));
+                else
+                    c[j / 2] = (uint8_t)((c[j / 2] & 0xf0) | nc);
+                for (int64_t l = 0; l < k; ++l) g[l] = fmaf(-best_d, h[j * k + l], g[l]);
+                ++moves;
+            }
+        }
+        if (flips) flips[row] = moves;
+        free(r);
+        free(g);
+    }
 }
