@@ -708,6 +708,155 @@ def gpu_arm_w4a16(args, rank: int, world: int):
     return 0
 
 
+# ------------------------------------------------- Flip Refinement GPU arm
+
+METRIC_FLIP = "offline weight preparation with Flip Refinement: weight rows per second"
+FP32_LANES_PER_SM = 128        # fp32 FMA lanes per SM (B300)
+
+
+def oracle_flip_rate(d, rows: int, sweeps: int):
+    """Time the CPU oracle: the Hessian of the calibration rows, then the
+    transform, round to nearest and refinement of `rows` weight rows.
+    Returns (rows/s with the Hessian's time charged pro rata, detail)."""
+    import oracle
+
+    wl = d["workload"]
+    t0 = time.perf_counter()
+    s, inv = oracle.balance_scales(d["X_calib"], d["W"])
+    A = oracle.transform_f32(d["X_calib"], inv)
+    H = oracle.flip_hessian(A)
+    t_h = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    W = d["W"][:rows].contiguous()
+    wt = oracle.transform_f32(W, s)
+    c, sc = oracle.quantize(W, s)
+    oracle.flip_refine(wt, H, c, sc, sweeps)
+    t_r = time.perf_counter() - t0
+    rate = rows / (t_r + t_h * rows / wl.N)
+    threads = max(oracle.num_threads(), os.cpu_count() or 1)
+    return rate, t_h, t_r, threads
+
+
+def gpu_arm_flip(args, rank: int, world: int):
+    """One layer's offline preparation: balance scales, the fp32 transforms of
+    the calibration rows and the weight, the Hessian, round-to-nearest MXFP4,
+    and Flip Refinement of every weight row."""
+    import torch
+
+    import workloads
+    import w4a4_mxfp4_quantized_02_b300 as mq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mq.lib()
+    peaks = load_peaks()
+    d = workloads.make_dense(args.config)
+    wl = d["workload"]
+    N, K, Mc = wl.N, wl.K, wl.calib_rows
+    hb = args.hadamard_block
+    sweeps = args.sweeps
+    stream = torch.cuda.current_stream()
+    Xc = d["X_calib"].to(dev)
+    W = d["W"].to(dev)
+    A = torch.empty(Mc, K, dtype=torch.float32, device=dev)
+    Wt = torch.empty(N, K, dtype=torch.float32, device=dev)
+    H = torch.empty(K, K, dtype=torch.float32, device=dev)
+    codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(mq.macaq_scale_bytes(N, K), dtype=torch.uint8, device=dev)
+    flips = torch.empty(N, dtype=torch.int32, device=dev)
+    work = torch.empty(mq.macaq_flip_refine_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    stages = ["balance+transforms", "hessian", "rtn", "prepare", "sweeps"]
+
+    def step(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        s, inv = mq.macaq_balance_scales(Xc, W)
+        mq.macaq_transform_f32(Xc, inv, hb, Y=A)
+        mq.macaq_transform_f32(W, s, hb, Y=Wt)
+        rec(1)
+        mq.macaq_flip_hessian(A, args.damp, H=H)
+        rec(2)
+        mq.macaq_quant_weight_hb(W, s, hb, codes, scales)
+        rec(3)
+        mq.macaq_flip_prepare(Wt, H, codes, scales, work)
+        rec(4)
+        mq.macaq_flip_sweeps(H, N, K, codes, scales, work, sweeps, flips=flips)
+        rec(5)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if mq.macaq_check_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(pci_bus_id(dev))
+    torch.cuda.synchronize()
+    with sampler:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    elapsed_ms = t0.elapsed_time(t1)
+    if mq.macaq_check_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    parts = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, name in enumerate(stages)}
+    moves = flips.cpu().numpy()
+    ms = elapsed_ms / args.steps
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        try:
+            rate, t_h, t_r, threads = oracle_flip_rate(d, args.cpu_rows, sweeps)
+            cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                   "sample": f"Hessian of {Mc} x {K} calibration rows ({t_h:.1f} s, charged pro rata) "
+                             f"and {args.cpu_rows} of {N} weight rows refined ({t_r:.1f} s)"}
+        except Exception as e:  # noqa: BLE001 - reported, not fatal
+            cpu = {"value": None, "unit": "rows/s", "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+    # the dominant kernel is the descent: per move it streams one row of H
+    # (K fp32) into the row's g; per row it also reads g and writes codes
+    total_moves = float(moves.sum())
+    sweep_bytes = total_moves * K * 4 + N * K * 4 + N * K
+    sweep_gbs = sweep_bytes / (parts["sweeps"] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "flip_sweep_kernel", "achieved": sweep_gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": sweep_gbs / peaks["hbm_gbs"],
+                "traffic": None, "bytes_per_launch": sweep_bytes,
+                "peak_note": f"{peaks['source']} HBM copy bandwidth (H of {K * K * 4 / 1e6:.0f} MB "
+                             f"{'fits' if K * K * 4 < L2_BYTES else 'exceeds'} L2)",
+                "avg_launch_us": parts["sweeps"] * 1e3}
+    # the Hessian and g = R H are fp32 FMA chains on the CUDA cores (no tensor
+    # path keeps the definition's order): their bound is the fp32 FMA rate
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk = sampler.summary().get("sm_mhz") or 2032.0
+    fp32_peak = 2.0 * sm * FP32_LANES_PER_SM * clk * 1e6 / 1e12
+    fma_chains = {
+        "kernel": "sgemm_seq_kernel", "unit": "TFLOP/s", "peak": fp32_peak, "bound": "alu",
+        "peak_note": f"fp32 FMA: {sm} SMs x {FP32_LANES_PER_SM} lanes x 2 x {clk:.0f} MHz (derived)",
+        "hessian": 2.0 * K * K * Mc / (parts["hessian"] * 1e-3) / 1e12,
+        "prepare_g": 2.0 * N * K * K / (parts["prepare"] * 1e-3) / 1e12,
+    }
+    line = {
+        "metric": METRIC_FLIP, "value": N / (ms * 1e-3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (fp32 transform, Hessian and descent; MXFP4 codes)", "data": "synthetic",
+        "config": dict(workload_config(wl), hadamard_block=hb, sweeps=sweeps, damp=args.damp,
+                       stage="flip refinement (offline)"),
+        "stages_ms": parts,
+        "moves_per_row": {"mean": float(moves.mean()), "max": int(moves.max()), "min": int(moves.min())},
+        "roofline": roofline,
+        "fma_chains": fma_chains,
+        "cpu_baseline": cpu,
+        "e2e": None,
+        "gpu_launches": 8 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------- MoE GPU arm
 
 def moe_workload_config(wl):
@@ -1028,6 +1177,11 @@ def main():
                     help="Hadamard block of the transform (dense workloads)")
     ap.add_argument("--precision", choices=["w4a4", "w4a16"], default="w4a4",
                     help="w4a16: the weight-only fallback (dense workloads)")
+    ap.add_argument("--stage", choices=["layer", "flip"], default="layer",
+                    help="flip: time the offline weight preparation with Flip Refinement")
+    ap.add_argument("--sweeps", type=int, default=2, help="Flip Refinement passes")
+    ap.add_argument("--damp", type=float, default=0.0, help="Flip Refinement diagonal damping")
+    ap.add_argument("--cpu-rows", type=int, default=64, help="weight rows the oracle refines")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--kernel-events-every", type=int, default=4,
@@ -1048,6 +1202,8 @@ def main():
     try:
         if args.config.startswith("moe"):
             return gpu_arm_moe(args, rank, world)
+        if args.stage == "flip":
+            return gpu_arm_flip(args, rank, world)
         if args.precision == "w4a16":
             return gpu_arm_w4a16(args, rank, world)
         return gpu_arm(args, rank, world)

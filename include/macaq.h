@@ -289,6 +289,71 @@ macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, 
                                 int64_t M, int64_t N, int64_t K, int64_t hadamard_block, void *Y,
                                 int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream);
 
+/* --------------------------------------------- Flip Refinement (offline) */
+
+/* The fp32 transform itself (no rounding to MXFP4): Y[m, k] = the normalised
+ * transform y of macaq_quant_act (hadamard_block 32) / macaq_quant_act_hb (64)
+ * of X with factor f (1/s for activations, s for weights).  X bf16 [M, ldx];
+ * Y fp32 [M, ldy], ldy >= K, a multiple of 4; only the first K columns of each
+ * row are written.  The rotated rows Flip Refinement works on. */
+macaq_status macaq_transform_f32(const void *X, int64_t ldx, const float *f, int64_t M, int64_t K,
+                                 int64_t hadamard_block, float *Y, int64_t ldy, macaq_stream_t stream);
+
+/* Flip Refinement (page "What is MACaQ quantization", section "How MACaQ
+ * works", step "Flip Refinement": instead of plain round to nearest, a
+ * Hessian-aware coordinate descent moves single 4-bit weight codes to an
+ * adjacent value when that lowers the layer's error on calibration data).
+ * Reading: in the rotated space the layer output is A . Wt^T, with A the
+ * calibration rows through the activation transform and Wt the weight rows
+ * through the weight transform (macaq_transform_f32 with 1/s and s); the
+ * error of one weight row with dequantised codes q is
+ *   E(q) = (Wt - q)^T H (Wt - q),  H = A^T A (+ damp on the diagonal).
+ *
+ * macaq_flip_hessian: H[i, j] = fp32 fused multiply-add chain over the
+ * calibration rows r = 0 .. Mc-1 of A[r, i] * A[r, j] (from +0), then + damp
+ * (one fp32 add) where i == j.  A fp32 [Mc, K] row pitch K; H fp32 [K, K]
+ * (symmetric bit for bit), 4 K^2 bytes, caller-owned. */
+macaq_status macaq_flip_hessian(const float *A, int64_t Mc, int64_t K, float damp, float *H,
+                                macaq_stream_t stream);
+
+/* Workspace bytes macaq_flip_refine needs for N rows of K channels. */
+size_t macaq_flip_refine_workspace_bytes(int64_t N, int64_t K);
+
+/* The descent, per weight row: r = Wt - q, g = H r (a fused multiply-add
+ * chain over k); `sweeps` passes over k = 0 .. K-1; at each k the two
+ * neighbours of q_k on the signed E2M1 grid (-6 .. -0.5, 0, 0.5 .. 6 times the
+ * block's scale, which never changes) are scored dE = D (D H_kk - 2 g_k)
+ * (fp32, one rounding per operation; D the move), the lower strictly negative
+ * score is taken (ties to the lower value), and g -= D H[k, :].  A move onto
+ * zero keeps the sign of the side it came from (code 0x8 from below).  The
+ * pages do not fix the number of passes; the recipe's --vq-sweeps default of 2
+ * is the natural choice.
+ * Wt fp32 [N, K] row pitch K; H from macaq_flip_hessian; w_codes [N, K/2]
+ * (in: round-to-nearest codes from macaq_quant_weight / _hb, out: refined)
+ * and tiled w_scales (read only) for the same Wt; flips: int32 [N] moves per
+ * row, or NULL.  workspace: device, >= macaq_flip_refine_workspace_bytes(N, K),
+ * 256-byte aligned.  K above 48736 is MACAQ_ERR_UNSUPPORTED (a row's state
+ * lives in shared memory).  A row whose warps fail to meet within 2 s stops
+ * without writing its codes and macaq_check_device_error reports
+ * MACAQ_ERR_TIMEOUT. */
+macaq_status macaq_flip_refine(const float *Wt, const float *H, int64_t N, int64_t K, int32_t sweeps,
+                               uint8_t *w_codes, const uint8_t *w_scales, int32_t *flips,
+                               void *workspace, size_t ws_bytes, macaq_stream_t stream);
+
+/* macaq_flip_refine in its two launches.  macaq_flip_prepare: r = Wt - q of
+ * the current codes and g = H r (fused multiply-add chain over k) into
+ * `workspace`.  macaq_flip_sweeps: the passes, starting from the g that
+ * macaq_flip_prepare left in the same workspace (it does not write g back:
+ * more passes later start with a new macaq_flip_prepare, whose g is computed
+ * afresh and so may differ in its last bits from a continued descent).
+ * Arguments and errors as macaq_flip_refine. */
+macaq_status macaq_flip_prepare(const float *Wt, const float *H, int64_t N, int64_t K,
+                                const uint8_t *w_codes, const uint8_t *w_scales, void *workspace,
+                                size_t ws_bytes, macaq_stream_t stream);
+macaq_status macaq_flip_sweeps(const float *H, int64_t N, int64_t K, int32_t sweeps, uint8_t *w_codes,
+                               const uint8_t *w_scales, int32_t *flips, void *workspace, size_t ws_bytes,
+                               macaq_stream_t stream);
+
 /* --------------------------------------------------- device errors */
 
 /* Every device-side wait of the GEMM kernels is bounded in time.  A wait that

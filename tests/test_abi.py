@@ -135,6 +135,25 @@ def test_w4a16_rejections(L):
     assert f(p, 96, p, p, 16, 64, 96, 64, p, 64, p, need, None) == INVALID     # K % 64
 
 
+def test_flip_rejections(L):
+    t = L.macaq_transform_f32
+    h = L.macaq_flip_hessian
+    f = L.macaq_flip_refine
+    p = _fake()
+    assert t(p, 128, p, 4, 128, 16, p, 128, None) == INVALID        # block neither 32 nor 64
+    assert t(p, 128, p, 4, 128, 32, p, 130, None) == ALIGN          # ldy % 4
+    assert t(p, 128, p, 4, 128, 32, p, 64, None) == INVALID         # ldy < K
+    assert h(p, 16, 100, ctypes.c_float(0.0), p, None) == INVALID   # K % 32
+    assert h(p, 16, 128, ctypes.c_float(0.0), None, None) == INVALID
+    need = mq.macaq_flip_refine_workspace_bytes(16, 128)
+    assert need == 2 * 16 * 128 * 4
+    assert f(p, p, 16, 128, -1, p, p, None, p, need, None) == INVALID   # negative sweeps
+    assert f(p, p, 16, 128, 2, p, p, None, None, need, None) == WORKSPACE
+    assert f(p, p, 16, 128, 2, p, p, None, p, need - 1, None) == WORKSPACE
+    assert f(p, p, 16, 48768, 2, p, p, None, p, 1 << 40, None) == UNSUPPORTED  # row state too large
+    assert f(p, p, 0, 128, 2, p, p, None, p, need, None) == OK
+
+
 def test_balance_rejections(L):
     b = L.macaq_balance_scales
     p = _fake()

@@ -66,6 +66,12 @@ _SIGS = {
     "macaq_w4a16_gemm": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], ctypes.c_int),
     "macaq_w4a16_linear": ([_P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
                            ctypes.c_int),
+    "macaq_transform_f32": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_flip_hessian": ([_P, _I64, _I64, ctypes.c_float, _P, _P], ctypes.c_int),
+    "macaq_flip_refine_workspace_bytes": ([_I64, _I64], _SZ),
+    "macaq_flip_refine": ([_P, _P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
+    "macaq_flip_prepare": ([_P, _P, _I64, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
+    "macaq_flip_sweeps": ([_P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_check_device_error": ([_P], ctypes.c_int),
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
@@ -331,6 +337,76 @@ def macaq_w4a16_linear(X: torch.Tensor, inv_s, Wd: torch.Tensor, hadamard_block:
         _ptr(X), _ld(X), _ptr(inv_s), _ptr(Wd), M, N, K, hadamard_block, _ptr(Y), _ld(Y),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return Y
+
+
+# ------------------------------------------------- Flip Refinement (offline)
+
+def macaq_transform_f32(X: torch.Tensor, f: torch.Tensor, hadamard_block: int = 32, Y=None,
+                        stream=None):
+    """The fp32 transform (balance by f, block Hadamard, normalisation)."""
+    _dev(X, "X")
+    M, K = X.shape
+    if Y is None:
+        Y = torch.empty(M, K, dtype=torch.float32, device=X.device)
+    _check("macaq_transform_f32", lib().macaq_transform_f32(
+        _ptr(X), _ld(X), _ptr(f), M, K, hadamard_block, _ptr(Y), _ld(Y), _stream(stream)))
+    return Y
+
+
+def macaq_flip_hessian(A: torch.Tensor, damp: float = 0.0, H=None, stream=None):
+    """H = A^T A (+ damp on the diagonal) of fp32 rows A [Mc, K]."""
+    _dev(A, "A")
+    Mc, K = A.shape
+    if not A.is_contiguous():
+        raise ValueError("A must be contiguous [Mc, K]")
+    if H is None:
+        H = torch.empty(K, K, dtype=torch.float32, device=A.device)
+    _check("macaq_flip_hessian", lib().macaq_flip_hessian(
+        _ptr(A), Mc, K, ctypes.c_float(damp), _ptr(H), _stream(stream)))
+    return H
+
+
+def macaq_flip_refine_workspace_bytes(N: int, K: int) -> int:
+    return int(lib().macaq_flip_refine_workspace_bytes(N, K))
+
+
+def macaq_flip_refine(Wt: torch.Tensor, H: torch.Tensor, w_codes: torch.Tensor, w_scales: torch.Tensor,
+                      sweeps: int = 2, flips=None, workspace=None, stream=None):
+    """Refine round-to-nearest codes in place; returns the moves per row."""
+    _dev(Wt, "Wt")
+    N, K = Wt.shape
+    if not Wt.is_contiguous() or not H.is_contiguous():
+        raise ValueError("Wt and H must be contiguous")
+    if flips is None:
+        flips = torch.empty(N, dtype=torch.int32, device=Wt.device)
+    if workspace is None:
+        workspace = torch.empty(max(macaq_flip_refine_workspace_bytes(N, K), 1), dtype=torch.uint8,
+                                device=Wt.device)
+    _check("macaq_flip_refine", lib().macaq_flip_refine(
+        _ptr(Wt), _ptr(H), N, K, int(sweeps), _ptr(w_codes), _ptr(w_scales), _ptr(flips),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return flips
+
+
+def macaq_flip_prepare(Wt: torch.Tensor, H: torch.Tensor, w_codes, w_scales, workspace, stream=None):
+    """r = Wt - q and g = H r of the current codes into ``workspace``."""
+    _dev(Wt, "Wt")
+    N, K = Wt.shape
+    _check("macaq_flip_prepare", lib().macaq_flip_prepare(
+        _ptr(Wt), _ptr(H), N, K, _ptr(w_codes), _ptr(w_scales), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def macaq_flip_sweeps(H: torch.Tensor, N: int, K: int, w_codes, w_scales, workspace, sweeps: int = 2,
+                      flips=None, stream=None):
+    """The passes of Flip Refinement from the g macaq_flip_prepare left."""
+    _dev(H, "H")
+    if flips is None:
+        flips = torch.empty(N, dtype=torch.int32, device=H.device)
+    _check("macaq_flip_sweeps", lib().macaq_flip_sweeps(
+        _ptr(H), N, K, int(sweeps), _ptr(w_codes), _ptr(w_scales), _ptr(flips), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return flips
 
 
 # ----------------------------------------------------------- grouped (MoE)

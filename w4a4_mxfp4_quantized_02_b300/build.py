@@ -30,6 +30,7 @@ UNITS = {
     "api.cu": [],
     "static_scratch.cu": [],
     "w4a16.cu": [],
+    "flip.cu": ["-fmad=false"],
 }
 HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh"]
 

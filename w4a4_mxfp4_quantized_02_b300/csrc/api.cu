@@ -253,7 +253,7 @@ macaq_status macaq_transform_act_bf16(const void *X, int64_t ldx, const float *i
     a.codes = static_cast<uint8_t *>(Xt);
     a.scales = nullptr;
     a.had = static_cast<int32_t>(hadamard_block);
-    a.out_bf16 = true;
+    a.out_kind = kOutBf16;
     a.ld_out = ldxt;
     return from_cuda(launch_quant(QuantMode::Dense, a, static_cast<cudaStream_t>(stream)));
 }
@@ -316,6 +316,107 @@ macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, 
     const size_t xt_bytes = align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
     MACAQ_TRY(macaq_transform_act_bf16(X, ldx, inv_s, M, K, hadamard_block, xt, K, stream));
     return macaq_w4a16_gemm(xt, K, Wd, M, N, K, Y, ldy, xt + xt_bytes, kW4A16GemmWorkspace, stream);
+}
+
+macaq_status macaq_transform_f32(const void *X, int64_t ldx, const float *f, int64_t M, int64_t K,
+                                 int64_t hadamard_block, float *Y, int64_t ldy, macaq_stream_t stream)
+{
+    if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_k(K));
+    if (K % hadamard_block != 0) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_rows(M));
+    if (M == 0) return MACAQ_OK;
+    if (!X || !f || !Y || ldx < K || ldy < K) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(f) || !aligned16(Y) || ldx % 8 != 0 || ldy % 4 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(X);
+    a.ld_src = ldx;
+    a.f = f;
+    a.K = K;
+    a.rows_valid = M;
+    a.rows_out = M;
+    a.E = 1;
+    a.codes = reinterpret_cast<uint8_t *>(Y);
+    a.scales = nullptr;
+    a.had = static_cast<int32_t>(hadamard_block);
+    a.out_kind = kOutF32;
+    a.ld_out = ldy;
+    return from_cuda(launch_quant(QuantMode::Dense, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_flip_hessian(const float *A, int64_t Mc, int64_t K, float damp, float *H,
+                                macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(Mc));
+    if (!H || (Mc > 0 && !A)) return MACAQ_ERR_INVALID_ARG;
+    if ((A && !aligned16(A)) || !aligned16(H)) return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_flip_hessian(A, Mc, K, damp, H, static_cast<cudaStream_t>(stream)));
+}
+
+size_t macaq_flip_refine_workspace_bytes(int64_t N, int64_t K)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0) return 0;
+    return 2 * align256(static_cast<size_t>(N) * static_cast<size_t>(K) * 4);
+}
+
+namespace {
+
+macaq_status check_flip(const float *H, int64_t N, int64_t K, const uint8_t *w_codes, const uint8_t *w_scales,
+                        void *workspace, size_t ws_bytes)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(N));
+    if (flip_rows_per_cta(K) < 1) return MACAQ_ERR_UNSUPPORTED;
+    if (N == 0) return MACAQ_OK;
+    if (!H || !w_codes || !w_scales) return MACAQ_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < macaq_flip_refine_workspace_bytes(N, K)) return MACAQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || !aligned16(H) || !aligned16(w_codes) ||
+        !aligned16(w_scales))
+        return MACAQ_ERR_ALIGNMENT;
+    return MACAQ_OK;
+}
+
+float *flip_g(void *workspace, int64_t N, int64_t K)
+{
+    return reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                     align256(static_cast<size_t>(N) * static_cast<size_t>(K) * 4));
+}
+
+}  // namespace
+
+macaq_status macaq_flip_prepare(const float *Wt, const float *H, int64_t N, int64_t K,
+                                const uint8_t *w_codes, const uint8_t *w_scales, void *workspace,
+                                size_t ws_bytes, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_flip(H, N, K, w_codes, w_scales, workspace, ws_bytes));
+    if (N == 0) return MACAQ_OK;
+    if (!Wt) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(Wt)) return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_flip_prepare(Wt, H, N, K, w_codes, w_scales, static_cast<float *>(workspace),
+                                         flip_g(workspace, N, K), static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_flip_sweeps(const float *H, int64_t N, int64_t K, int32_t sweeps, uint8_t *w_codes,
+                               const uint8_t *w_scales, int32_t *flips, void *workspace, size_t ws_bytes,
+                               macaq_stream_t stream)
+{
+    if (sweeps < 0) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_flip(H, N, K, w_codes, w_scales, workspace, ws_bytes));
+    if (N == 0) return MACAQ_OK;
+    if (flips && (reinterpret_cast<uintptr_t>(flips) & 3u)) return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_flip_sweeps(H, flip_g(workspace, N, K), N, K, sweeps, w_codes, w_scales, flips,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_flip_refine(const float *Wt, const float *H, int64_t N, int64_t K, int32_t sweeps,
+                               uint8_t *w_codes, const uint8_t *w_scales, int32_t *flips,
+                               void *workspace, size_t ws_bytes, macaq_stream_t stream)
+{
+    if (sweeps < 0) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(macaq_flip_prepare(Wt, H, N, K, w_codes, w_scales, workspace, ws_bytes, stream));
+    return macaq_flip_sweeps(H, N, K, sweeps, w_codes, w_scales, flips, workspace, ws_bytes, stream);
 }
 
 macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *row_src,
@@ -415,10 +516,11 @@ macaq_status macaq_check_device_error(macaq_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MACAQ_ERR_CUDA;
-    unsigned flags = 0, qflags = 0;
+    unsigned flags = 0, qflags = 0, fflags = 0;
     if (read_and_clear_device_error(&flags) != cudaSuccess) return MACAQ_ERR_CUDA;
     if (read_and_clear_quant_error(&qflags) != cudaSuccess) return MACAQ_ERR_CUDA;
-    return (flags | qflags) ? MACAQ_ERR_TIMEOUT : MACAQ_OK;
+    if (read_and_clear_flip_error(&fflags) != cudaSuccess) return MACAQ_ERR_CUDA;
+    return (flags | qflags | fflags) ? MACAQ_ERR_TIMEOUT : MACAQ_OK;
 }
 
 macaq_status macaq_set_wait_timeout_ns(uint64_t ns)

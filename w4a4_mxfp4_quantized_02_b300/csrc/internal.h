@@ -26,6 +26,8 @@ inline int64_t grouped_padded_rows(int64_t rows, int64_t E)
 
 // ActGroupedSilu: the grouped activation transform of h = SiLU(g) * u read from
 // a [rows, 2F] gate|up matrix in sorted row order (K = F).
+constexpr int32_t kOutMx = 0, kOutBf16 = 1, kOutF32 = 2;
+
 enum class QuantMode : int { Dense = 0, WeightGrouped = 1, ActGrouped = 2, ActGroupedSilu = 3 };
 
 struct QuantArgs {
@@ -43,8 +45,8 @@ struct QuantArgs {
     uint8_t *scales;
     size_t scale_group_stride;  // WeightGrouped: tiled_scale_bytes(N, K)
     int32_t had = 32;           // Hadamard block: 32, or 64 (Dense only)
-    bool out_bf16 = false;      // Dense only: bf16 transform into codes viewed as bf16 [rows, ld_out]
-    int64_t ld_out = 0;
+    int32_t out_kind = 0;       // Dense only: kOutMx, or kOutBf16 / kOutF32 (the transform into
+    int64_t ld_out = 0;         //   codes viewed as bf16 / float [rows, ld_out])
 };
 
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream);
@@ -55,6 +57,18 @@ cudaError_t launch_dequant_bf16(const uint8_t *codes, const uint8_t *scales, int
 cudaError_t launch_bf16_gemm_nt(const uint16_t *Xt, int64_t ldx, const uint16_t *Wd, int64_t M, int64_t N,
                                 int64_t K, uint16_t *Y, int64_t ldy, void *ws, size_t ws_bytes,
                                 cudaStream_t stream);
+
+// Flip Refinement: H = A^T A (+ damp on the diagonal) of fp32 calibration rows
+// a [m, k]; the descent over rows wt [n, k] of round-to-nearest codes (in/out)
+// with tiled scales: prepare writes r = wt - q and g = r H ([n, k] fp32
+// each), the sweeps read g.
+int64_t flip_rows_per_cta(int64_t k);
+cudaError_t launch_flip_hessian(const float *a, int64_t m, int64_t k, float damp, float *h, cudaStream_t stream);
+cudaError_t launch_flip_prepare(const float *wt, const float *h, int64_t n, int64_t k, const uint8_t *codes,
+                               const uint8_t *scales, float *r, float *g, cudaStream_t stream);
+cudaError_t launch_flip_sweeps(const float *h, const float *g, int64_t n, int64_t k, int32_t sweeps,
+                               uint8_t *codes, const uint8_t *scales, int32_t *flips, cudaStream_t stream);
+cudaError_t read_and_clear_flip_error(unsigned *flags);
 
 cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_rows, int64_t mc,
                            const uint16_t *w, int64_t n, int64_t k, float *s, float *inv_s,

@@ -598,9 +598,11 @@ constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
 constexpr int kGroupedConsumersMax = 512;
 constexpr int kGroupedThreadsMax = kGroupedConsumersMax + 32;
 
-// kBf16: write the normalised transform as bf16 (the W4A16 activation) to
-// a.codes viewed as bf16 [rows, ld_out] instead of MXFP4 codes and scales.
-template <int STAGES, bool kH64, bool kBf16>
+// kOut: kOutMx writes MXFP4 codes and scales; kOutBf16 the normalised
+// transform as bf16 (the W4A16 activation) to a.codes viewed as bf16
+// [rows, ld_out]; kOutF32 the same values in fp32 (the rotated rows Flip
+// Refinement works on) to a.codes viewed as float [rows, ld_out].
+template <int STAGES, bool kH64, int kOut>
 __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                   QuantArgs a, int32_t groups, int32_t TB,
                                                                   int32_t RT)
@@ -728,13 +730,25 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
                 f[2 * c] = make_float2(x0, x1);
                 f[2 * c + 1] = make_float2(x2, x3);
             }
-            if (kBf16) {
+            if (kOut == kOutBf16) {
                 // W4A16: the bf16 transform, 64 bytes of row r at block kb
                 uint32_t w[16];
                 bf16_block_pairs<kH64>(raw, f, w);
                 uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (r * a.ld_out + 32 * kb) * 2);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            } else if (kOut == kOutF32) {
+                // the fp32 transform, 128 bytes of row r at block kb
+                constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
+                float2 v[16];
+                hadamard_block_pairs<kH64>(raw, f, v);
+                float4 *dst = reinterpret_cast<float4 *>(a.codes + (r * a.ld_out + 32 * kb) * 4);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float2 y0 = __fmul2_rn(v[2 * q], make_float2(kNorm, kNorm));
+                    const float2 y1 = __fmul2_rn(v[2 * q + 1], make_float2(kNorm, kNorm));
+                    dst[q] = make_float4(y0.x, y0.y, y1.x, y1.y);
+                }
             } else {
                 uint4 codes;
                 sbyte = quant_block_pairs<kH64>(raw, f, codes);
@@ -744,7 +758,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
         }
-        if (kBf16) continue;
+        if (kOut != kOutMx) continue;
         uint32_t word = sbyte << (8 * (lane & 3));
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
@@ -1121,7 +1135,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // dynamic shared memory each TMA kernel variant has been opened up to.
 struct QuantDevice {
     int sms = 0;
-    int smem_set[20] = {};
+    int smem_set[30] = {};
 };
 QuantDevice g_qdev[64];
 std::mutex g_qdev_mu;
@@ -1215,13 +1229,16 @@ cudaError_t launch_quant_dense_tma(const QuantArgs &a, cudaStream_t stream, bool
     ctas_y = ctas_y < 1 ? 1 : ctas_y;
     ctas_y = ctas_y > groups ? groups : ctas_y;
     void (*kern)(CUtensorMap, QuantArgs, int32_t, int32_t, int32_t);
-    if (a.out_bf16)
-        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, true> : quant_dense_tma_kernel<4, true, true>)
-                           : (stages == 6 ? quant_dense_tma_kernel<6, false, true> : quant_dense_tma_kernel<4, false, true>);
+    if (a.out_kind == kOutBf16)
+        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, kOutBf16> : quant_dense_tma_kernel<4, true, kOutBf16>)
+                           : (stages == 6 ? quant_dense_tma_kernel<6, false, kOutBf16> : quant_dense_tma_kernel<4, false, kOutBf16>);
+    else if (a.out_kind == kOutF32)
+        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, kOutF32> : quant_dense_tma_kernel<4, true, kOutF32>)
+                           : (stages == 6 ? quant_dense_tma_kernel<6, false, kOutF32> : quant_dense_tma_kernel<4, false, kOutF32>);
     else
-        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, false> : quant_dense_tma_kernel<4, true, false>)
-                           : (stages == 6 ? quant_dense_tma_kernel<6, false, false> : quant_dense_tma_kernel<4, false, false>);
-    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : 1) + (a.had == 64 ? 8 : 0) + (a.out_bf16 ? 10 : 0), smem));
+        kern = a.had == 64 ? (stages == 6 ? quant_dense_tma_kernel<6, true, kOutMx> : quant_dense_tma_kernel<4, true, kOutMx>)
+                           : (stages == 6 ? quant_dense_tma_kernel<6, false, kOutMx> : quant_dense_tma_kernel<4, false, kOutMx>);
+    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : 1) + (a.had == 64 ? 8 : 0) + 10 * a.out_kind, smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
@@ -1304,7 +1321,7 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
         if (err != cudaSuccess || done) return err;
     }
     if (mode == QuantMode::ActGroupedSilu) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
-    if (a.had == 64 || a.out_bf16) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
+    if (a.had == 64 || a.out_kind != kOutMx) return a.rows_valid >= 1 ? cudaErrorNotSupported : cudaSuccess;
     const int64_t slabs = (nkb_pad + best_t - 1) / best_t;
     // rows per CTA: aim for about 8 resident-CTA waves worth of work items
     int sms = 148;
