@@ -102,16 +102,21 @@ constexpr int kSgBM = 128, kSgBN = 128, kSgBK = 8, kSgThreads = 256;
 
 // C[i, j] = fma-chain over l = 0 .. L-1 of A(i, l) * B(l, j), starting at +0,
 // then + diag_add where i == j (one fp32 add; only when add_diag).
-// A(i, l) = a[i * a_si + l * a_sl], B(l, j) = b[l * ldb + j], C[i * ldc + j].
-// Each thread owns an 8 x 8 block of C and walks l in order, so each output's
-// FMA chain is the definition's regardless of the tiling.
-__global__ void __launch_bounds__(kSgThreads) sgemm_seq_kernel(const float *a, int64_t a_si, int64_t a_sl,
-                                                                const float *b, int64_t ldb, float *c, int64_t ldc,
-                                                                int64_t M, int64_t N, int64_t L, bool add_diag,
-                                                                float diag_add)
+// A(i, l) = a[l * lda + i] (kAT) or a[i * lda + l]; B(l, j) = b[l * ldb + j];
+// C[i * ldc + j].  M, N, L multiples of 4 where they index a contiguous
+// dimension; all pitches multiples of 4, pointers 16-byte aligned.
+// Each thread owns an 8 x 8 block of C (rows 4ty.. and 64+4ty.., columns
+// 4tx.. and 64+4tx..) and walks l in order, so each output's FMA chain is the
+// definition's whatever the tiling; the next 8-deep slab of A and B is
+// fetched into registers while the current one is consumed (two shared
+// buffers, one barrier per slab).
+template <bool kAT>
+__global__ void __launch_bounds__(kSgThreads) sgemm_seq_kernel(const float *a, int64_t lda, const float *b,
+                                                                int64_t ldb, float *c, int64_t ldc, int64_t M,
+                                                                int64_t N, int64_t L, bool add_diag, float diag_add)
 {
-    __shared__ float As[kSgBK][kSgBM];
-    __shared__ float Bs[kSgBK][kSgBN];
+    __shared__ __align__(16) float As[2][kSgBK][kSgBM];
+    __shared__ __align__(16) float Bs[2][kSgBK][kSgBN];
     const int t = threadIdx.x;
     const int tx = t % 16, ty = t / 16;
     const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kSgBM;
@@ -122,52 +127,79 @@ __global__ void __launch_bounds__(kSgThreads) sgemm_seq_kernel(const float *a, i
 #pragma unroll
         for (int v = 0; v < 8; ++v) acc[u][v] = 0.0f;
 
+    // one float4 of A and one of B per thread and slab
+    const int a_l = kAT ? t / 32 : (t % 2) * 4;   // slab row (kAT) or first of 4 l
+    const int a_i = kAT ? (t % 32) * 4 : t / 2;   // first of 4 i (kAT) or the i
+    const int b_l = t / 32, b_j = (t % 32) * 4;
+    auto fetch = [&](int64_t l0, float4 &ra, float4 &rb) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kAT) {
+            const int64_t gl = l0 + a_l, gi = i0 + a_i;
+            ra = (gl < L && gi < M) ? *reinterpret_cast<const float4 *>(a + gl * lda + gi) : z;
+        } else {
+            const int64_t gl = l0 + a_l, gi = i0 + a_i;
+            ra = (gl < L && gi < M) ? *reinterpret_cast<const float4 *>(a + gi * lda + gl) : z;
+        }
+        const int64_t gl = l0 + b_l, gj = j0 + b_j;
+        rb = (gl < L && gj < N) ? *reinterpret_cast<const float4 *>(b + gl * ldb + gj) : z;
+    };
+    auto stash = [&](int buf, const float4 &ra, const float4 &rb) {
+        if (kAT) {
+            *reinterpret_cast<float4 *>(&As[buf][a_l][a_i]) = ra;
+        } else {
+            As[buf][a_l][a_i] = ra.x;
+            As[buf][a_l + 1][a_i] = ra.y;
+            As[buf][a_l + 2][a_i] = ra.z;
+            As[buf][a_l + 3][a_i] = ra.w;
+        }
+        *reinterpret_cast<float4 *>(&Bs[buf][b_l][b_j]) = rb;
+    };
+
+    float4 ra, rb;
+    fetch(0, ra, rb);
+    stash(0, ra, rb);
+    __syncthreads();
+    int buf = 0;
     for (int64_t l0 = 0; l0 < L; l0 += kSgBK) {
-        // stage A[i0 .. +128, l0 .. +8] and B[l0 .. +8, j0 .. +128] (zeros
-        // outside; those never enter a chain: the inner loop stops at L)
-        for (int e = t; e < kSgBK * kSgBM; e += kSgThreads) {
-            int ii, ll;
-            if (a_si == 1) {  // A contiguous along i: coalesce over i
-                ii = e % kSgBM;
-                ll = e / kSgBM;
-            } else {          // contiguous along l
-                ll = e % kSgBK;
-                ii = e / kSgBK;
-            }
-            const int64_t gi = i0 + ii, gl = l0 + ll;
-            As[ll][ii] = (gi < M && gl < L) ? a[gi * a_si + gl * a_sl] : 0.0f;
-        }
-        for (int e = t; e < kSgBK * kSgBN; e += kSgThreads) {
-            const int jj = e % kSgBN, ll = e / kSgBN;
-            const int64_t gj = j0 + jj, gl = l0 + ll;
-            Bs[ll][jj] = (gj < N && gl < L) ? b[gl * ldb + gj] : 0.0f;
-        }
-        __syncthreads();
-        const int lmax = L - l0 < kSgBK ? static_cast<int>(L - l0) : kSgBK;
-        for (int ll = 0; ll < lmax; ++ll) {
-            float av[8], bv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) av[u] = As[ll][ty + 16 * u];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) bv[v] = Bs[ll][tx + 16 * v];
+        const bool more = l0 + kSgBK < L;
+        if (more) fetch(l0 + kSgBK, ra, rb);
+        auto step = [&](int ll) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][ll][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][ll][64 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][ll][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][ll][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int v = 0; v < 8; ++v) acc[u][v] = __fmaf_rn(av[u], bv[v], acc[u][v]);
+        };
+        if (L - l0 >= kSgBK) {
+#pragma unroll
+            for (int ll = 0; ll < kSgBK; ++ll) step(ll);
+        } else {
+            for (int ll = 0; ll < static_cast<int>(L - l0); ++ll) step(ll);
         }
-        __syncthreads();
+        if (more) {
+            stash(buf ^ 1, ra, rb);
+            __syncthreads();
+            buf ^= 1;
+        }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const int64_t gi = i0 + ty + 16 * u;
+        const int64_t gi = i0 + (u < 4 ? 4 * ty + u : 64 + 4 * ty + u - 4);
         if (gi >= M) continue;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const int64_t gj = j0 + tx + 16 * v;
+        for (int h = 0; h < 2; ++h) {
+            const int64_t gj = j0 + 64 * h + 4 * tx;
             if (gj >= N) continue;
-            float x = acc[u][v];
-            if (add_diag && gi == gj) x = __fadd_rn(x, diag_add);
-            c[gi * ldc + gj] = x;
+            float x[4] = {acc[u][4 * h], acc[u][4 * h + 1], acc[u][4 * h + 2], acc[u][4 * h + 3]};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (add_diag && gi == gj + q) x[q] = __fadd_rn(x[q], diag_add);
+            *reinterpret_cast<float4 *>(c + gi * ldc + gj) = make_float4(x[0], x[1], x[2], x[3]);
         }
     }
 }
@@ -407,7 +439,7 @@ cudaError_t launch_flip_hessian(const float *a, int64_t m, int64_t k, float damp
 {
     dim3 grid(static_cast<unsigned>((k + kSgBN - 1) / kSgBN), static_cast<unsigned>((k + kSgBM - 1) / kSgBM));
     // A(i, l) = a[l, i]: rows of H are channels, the inner index the calibration row
-    sgemm_seq_kernel<<<grid, kSgThreads, 0, stream>>>(a, 1, k, a, k, h, k, k, k, m, true, damp);
+    sgemm_seq_kernel<true><<<grid, kSgThreads, 0, stream>>>(a, k, a, k, h, k, k, k, m, true, damp);
     return cudaGetLastError();
 }
 
@@ -420,7 +452,7 @@ cudaError_t launch_flip_prepare(const float *wt, const float *h, int64_t n, int6
     if (err != cudaSuccess) return err;
     // G = R . H: g of every row, each entry a chain over the coordinates
     dim3 grid(static_cast<unsigned>((k + kSgBN - 1) / kSgBN), static_cast<unsigned>((n + kSgBM - 1) / kSgBM));
-    sgemm_seq_kernel<<<grid, kSgThreads, 0, stream>>>(r, k, 1, h, k, g, k, n, k, k, false, 0.0f);
+    sgemm_seq_kernel<false><<<grid, kSgThreads, 0, stream>>>(r, k, h, k, g, k, n, k, k, false, 0.0f);
     return cudaGetLastError();
 }
 
