@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kSgThreads) sgemm_seq_kernel(const float *a, i
 // ------------------------------------------------------------------ descent
 
 constexpr int kFlipThreads = 512;
+constexpr int kFlushRB = 8;  // float4 of g per thread per pass of the block update
 constexpr uint64_t kFlipWaitNs = 2000000000ull;  // a row barrier gives up after 2 s
 constexpr int64_t kFlipSmemMax = 220 * 1024;
 
@@ -376,18 +377,40 @@ __global__ void __launch_bounds__(kFlipThreads, 1) flip_sweep_kernel(const float
             const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
             if (writer && (lane & 1) == 0) cs[(c0 + lane) >> 1] = static_cast<uint8_t>(code | (hi << 4));
             if (cnt > 0) {
+                // kFlushRB float4 of g per thread in registers; for each move
+                // (in order) their kFlushRB rows-of-H loads are independent
                 float4 *g4 = reinterpret_cast<float4 *>(g);
-                for (int64_t j = gt; j < k / 4; j += threads) {
-                    float4 x = g4[j];
+                const int64_t k4 = k / 4;
+                for (int64_t j0 = gt; j0 < k4; j0 += kFlushRB * threads) {
+                    float4 x[kFlushRB];
+#pragma unroll
+                    for (int q = 0; q < kFlushRB; ++q) {
+                        const int64_t j = j0 + q * threads;
+                        if (j < k4) x[q] = g4[j];
+                    }
+#pragma unroll 2
                     for (int m = 0; m < cnt; ++m) {
                         const float nd = -mv_d[m];
-                        const float4 h = __ldg(reinterpret_cast<const float4 *>(H + (c0 + mv_k[m]) * k) + j);
-                        x.x = __fmaf_rn(nd, h.x, x.x);
-                        x.y = __fmaf_rn(nd, h.y, x.y);
-                        x.z = __fmaf_rn(nd, h.z, x.z);
-                        x.w = __fmaf_rn(nd, h.w, x.w);
+                        const float4 *hrow = reinterpret_cast<const float4 *>(H + (c0 + mv_k[m]) * k);
+                        float4 h[kFlushRB];
+#pragma unroll
+                        for (int q = 0; q < kFlushRB; ++q) {
+                            const int64_t j = j0 + q * threads;
+                            if (j < k4) h[q] = __ldg(hrow + j);
+                        }
+#pragma unroll
+                        for (int q = 0; q < kFlushRB; ++q) {
+                            x[q].x = __fmaf_rn(nd, h[q].x, x[q].x);
+                            x[q].y = __fmaf_rn(nd, h[q].y, x[q].y);
+                            x[q].z = __fmaf_rn(nd, h[q].z, x[q].z);
+                            x[q].w = __fmaf_rn(nd, h[q].w, x[q].w);
+                        }
                     }
-                    g4[j] = x;
+#pragma unroll
+                    for (int q = 0; q < kFlushRB; ++q) {
+                        const int64_t j = j0 + q * threads;
+                        if (j < k4) g4[j] = x[q];
+                    }
                 }
             }
             // the diagonal piece of the next block (wrapping to block 0)
