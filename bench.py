@@ -173,8 +173,10 @@ def oracle_linear_rate(d, rows: int, target_s: float):
     deq_w = oracle.dequant(cw, sw)          # weight preparation: outside the timing
 
     def run(n):
-        X = d["X"][:n]
+        X = d["X"][:n] if "X" in d else d["GU"][:n].contiguous()
         t0 = time.perf_counter()
+        if "X" not in d:            # gated input: the SwiGLU step first
+            X = oracle.silu_mul(X)
         ca, sa = oracle.quantize(X, inv)
         Y = oracle.gemm_ref(oracle.dequant(ca, sa), deq_w)
         torch.from_numpy(Y).to(torch.bfloat16)
@@ -324,10 +326,14 @@ def gpu_arm(args, rank: int, world: int):
     torch.cuda.set_device(dev)
     mq.lib()
     peaks = load_peaks()
-    d = workloads.make_dense(args.config)
+    fused = args.fused_swiglu
+    if fused and (workloads.DENSE[args.config].act != "swiglu" or args.hadamard_block != 32):
+        raise SystemExit("--fused-swiglu needs a SwiGLU-input workload (down) and --hadamard-block 32")
+    d = workloads.make_dense_gated(args.config) if fused else workloads.make_dense(args.config)
     wl = d["workload"]
     M, N, K = wl.M, wl.N, wl.K
     stream = torch.cuda.current_stream()
+    xcols = 2 * K if fused else K   # the step's input: the gate|up matrix when fused
 
     # offline preparation (not timed): calibration, fold, weight quantisation
     Xc = d["X_calib"].to(dev)
@@ -338,9 +344,9 @@ def gpu_arm(args, rank: int, world: int):
     del W, Xc
 
     ws_bytes = mq.macaq_linear_workspace_bytes(M, K)
-    step_bytes = M * K * 2 + ws_bytes * 2 + w_codes.numel() + w_scales.numel() + M * N * 2
+    step_bytes = M * xcols * 2 + ws_bytes * 2 + w_codes.numel() + w_scales.numel() + M * N * 2
     nsets = max(2, math.ceil(2.5 * L2_BYTES / step_bytes) + 1)
-    X0 = d["X"].to(dev)
+    X0 = (d["GU"] if fused else d["X"]).to(dev)
     sets = []
     for i in range(nsets):
         sets.append({
@@ -356,7 +362,10 @@ def gpu_arm(args, rank: int, world: int):
         b = sets[i % nsets]
         if ev is not None:
             ev[0].record(stream)
-        mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
+        if fused:
+            mq.macaq_quant_act_silu(b["X"], inv, b["a_codes"], b["a_scales"])
+        else:
+            mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
         if ev is not None:
             ev[1].record(stream)
         mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
@@ -408,20 +417,23 @@ def gpu_arm(args, rank: int, world: int):
     gemm_avg = statistics.mean(g_ms)
     quant_avg = statistics.mean(q_ms)
     gemm_tflops = flops / (gemm_avg * 1e-3) / 1e12
-    quant_bytes = M * K * 2 + M * K // 2 + M * K // 32
+    quant_bytes = M * xcols * 2 + M * K // 2 + M * K // 32
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
 
     # end to end through the C ABI: pinned host X in, pinned host Y out
     def layer(b):
-        if hb == 32:
+        if fused:
+            mq.macaq_quant_act_silu(b["X"], inv, b["a_codes"], b["a_scales"])
+            mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
+        elif hb == 32:
             mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
         else:
             mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
             mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
 
     e2e_steps = max(3, min(args.steps, 50))
-    Xh = d["X"].pin_memory()
+    Xh = (d["GU"] if fused else d["X"]).pin_memory()
     nslot = min(3, nsets)
     Yh = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(nslot)]
     b = sets[0]
@@ -501,14 +513,17 @@ def gpu_arm(args, rank: int, world: int):
         "vs_baseline": None,
         "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
         "data": "synthetic",
-        "config": dict(workload_config(wl), hadamard_block=hb),
+        "config": dict(workload_config(wl), hadamard_block=hb,
+                       **({"input": "gate|up [M, 2K]; SiLU(gate) * up fused into the transform"}
+                          if fused else {})),
         "roofline": roofline,
-        "act_quant": {"kernel": "quant_dense_tma_kernel", "achieved": quant_gbs,
+        "act_quant": {"kernel": "quant_grouped_tma_kernel<.., true> (SwiGLU, one group)" if fused
+                      else "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
                       "avg_launch_us": quant_avg * 1e3},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * K * 2,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * xcols * 2,
                 "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
                 "copies": f"overlapped across steps ({nslot} buffer slots, separate copy streams)",
                 "serial_ms_per_step": e2e_serial_ms},
@@ -1229,6 +1244,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--hadamard-block", type=int, choices=[32, 64], default=32,
                     help="Hadamard block of the transform (dense workloads)")
+    ap.add_argument("--fused-swiglu", action="store_true",
+                    help="down: feed the gate|up matrix and fuse SiLU(gate) * up into the transform")
     ap.add_argument("--precision", choices=["w4a4", "w4a16"], default="w4a4",
                     help="w4a16: the weight-only fallback (dense workloads)")
     ap.add_argument("--stage", choices=["layer", "flip"], default="layer",

@@ -226,6 +226,15 @@ macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const in
                                           const float *inv_s, int64_t rows, int64_t E, int64_t F,
                                           uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream);
 
+/* The same fused SwiGLU transform for a dense gated MLP (the down
+ * projection's input h = bf16(SiLU(g) * u), SiLU and rounding as
+ * macaq_quant_act_grouped_silu): GU bf16 [M, ldgu] holds gate columns
+ * 0 .. F-1 and up columns F .. 2F-1 of each row; inv_s fp32 [F]; output as
+ * macaq_quant_act of h (a_codes [M, F/2], a_scales macaq_scale_bytes(M, F)
+ * bytes).  Equals macaq_quant_act of the bf16 h, without writing h. */
+macaq_status macaq_quant_act_silu(const void *GU, int64_t ldgu, const float *inv_s, int64_t M, int64_t F,
+                                  uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream);
+
 /* Grouped GEMM: for each expert e and sorted row r of e,
  *   Y[r, n] = bf16_rn( sum_k A(P_e + r - offsets[e], k) * Wq_e(n, k) )
  * with A from macaq_quant_act_grouped and Wq_e from

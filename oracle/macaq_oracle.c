@@ -34,7 +34,8 @@
  *   SwiGLU input     (extension: the down projection of a gated MLP reads
  *                    h = SiLU(g) * u of the gate and up outputs g, u.)  Stated
  *                    in fp32: e^x by range reduction x = n ln2 + r and a
- *                    degree-8 Taylor polynomial in r, SiLU(g) = g / (1 + e^-g),
+ *                    degree-8 Taylor polynomial in r (both as fused
+ *                    multiply-adds), SiLU(g) = g / (1 + e^-g),
  *                    h rounded once to bf16 (the value an unfused layer would
  *                    store).  The CUDA path evaluates the same operations in
  *                    the same order; both are pinned against fp64 exp.
@@ -455,17 +456,17 @@ float oracle_exp_f32(float x)
     const float t = x * 0x1.715476p+0f;               /* log2(e) */
     const float fn = rintf(t);
     const int n = (int)fn;
-    float r = x - fn * 0x1.62e4p-1f;                  /* ln2_hi = 0.693145751953125 */
-    r = r - fn * 0x1.7f7d1cp-20f;                     /* ln2_lo */
+    float r = fmaf(-fn, 0x1.62e4p-1f, x);             /* ln2_hi = 0.693145751953125 */
+    r = fmaf(-fn, 0x1.7f7d1cp-20f, r);                /* ln2_lo */
     float p = 0x1.a01a02p-16f;                        /* 1/8! */
-    p = p * r + 0x1.a01a02p-13f;                      /* 1/7! */
-    p = p * r + 0x1.6c16c2p-10f;                      /* 1/6! */
-    p = p * r + 0x1.111112p-7f;                       /* 1/5! */
-    p = p * r + 0x1.555556p-5f;                       /* 1/4! */
-    p = p * r + 0x1.555556p-3f;                       /* 1/3! */
-    p = p * r + 0x1.0p-1f;                            /* 1/2! */
-    p = p * r + 0x1.0p+0f;                            /* 1/1! */
-    p = p * r + 0x1.0p+0f;                            /* 1/0! */
+    p = fmaf(p, r, 0x1.a01a02p-13f);                  /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);                  /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);                   /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);                   /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);                   /* 1/3! */
+    p = fmaf(p, r, 0x1.0p-1f);                        /* 1/2! */
+    p = fmaf(p, r, 0x1.0p+0f);                        /* 1/1! */
+    p = fmaf(p, r, 0x1.0p+0f);                        /* 1/0! */
     if (n > 127) return (p * 0x1.0p+127f) * ldexpf(1.0f, n - 127);
     if (n < -126) return (p * ldexpf(1.0f, n + 100)) * 0x1.0p-100f;
     return p * ldexpf(1.0f, n);

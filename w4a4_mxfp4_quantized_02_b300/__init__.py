@@ -72,6 +72,7 @@ _SIGS = {
     "macaq_flip_refine": ([_P, _P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_flip_prepare": ([_P, _P, _I64, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_flip_sweeps": ([_P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
+    "macaq_quant_act_silu": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_check_device_error": ([_P], ctypes.c_int),
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
@@ -423,6 +424,21 @@ def macaq_quant_act_grouped(X, row_src, expert_offsets, inv_s, rows: int, E: int
     _check("macaq_quant_act_grouped", lib().macaq_quant_act_grouped(
         _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
         _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    return a_codes, a_scales
+
+
+def macaq_quant_act_silu(GU: torch.Tensor, inv_s: torch.Tensor, a_codes=None, a_scales=None, stream=None):
+    """Dense fused SwiGLU transform: MXFP4 of h = bf16(SiLU(gate) * up) for a
+    [M, 2F] gate|up matrix."""
+    _dev(GU, "GU")
+    M, F2 = GU.shape
+    F = F2 // 2
+    if a_codes is None:
+        a_codes = torch.empty(M, F // 2, dtype=torch.uint8, device=GU.device)
+    if a_scales is None:
+        a_scales = torch.empty(macaq_scale_bytes(M, F), dtype=torch.uint8, device=GU.device)
+    _check("macaq_quant_act_silu", lib().macaq_quant_act_silu(
+        _ptr(GU), _ld(GU), _ptr(inv_s), M, F, _ptr(a_codes), _ptr(a_scales), _stream(stream)))
     return a_codes, a_scales
 
 

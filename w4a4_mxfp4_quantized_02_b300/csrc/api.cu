@@ -478,6 +478,30 @@ macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const in
     return from_cuda(launch_quant(QuantMode::ActGroupedSilu, a, static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_quant_act_silu(const void *GU, int64_t ldgu, const float *inv_s, int64_t M, int64_t F,
+                                  uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(F));
+    MACAQ_TRY(check_rows(M));
+    if (M == 0) return MACAQ_OK;
+    if (!GU || !inv_s || !a_codes || !a_scales || ldgu < 2 * F) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(GU) || !aligned16(inv_s) || !aligned16(a_codes) || !aligned16(a_scales) || ldgu % 8 != 0)
+        return MACAQ_ERR_ALIGNMENT;
+    QuantArgs a{};
+    a.src = static_cast<const uint16_t *>(GU);
+    a.ld_src = ldgu;
+    a.row_src = nullptr;
+    a.offsets = nullptr;  // one group: all M rows
+    a.f = inv_s;
+    a.K = F;
+    a.rows_valid = M;
+    a.rows_out = pad_rows(M);
+    a.E = 1;
+    a.codes = a_codes;
+    a.scales = a_scales;
+    return from_cuda(launch_quant(QuantMode::ActGroupedSilu, a, static_cast<cudaStream_t>(stream)));
+}
+
 macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                                      const uint8_t *w_codes, const uint8_t *w_scales,
                                      const int32_t *expert_offsets, int64_t rows, int64_t E,

@@ -421,51 +421,64 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
 
 // ------------------------------------------------------------- SwiGLU step
 //
-// h = bf16( SiLU(g) * u ), SiLU(g) = g / (1 + e^-g), in fp32 with round to
-// nearest at every operation (the file is built with -fmad=false and the
-// operations are explicit).  e^x: Cody-Waite range reduction x = n ln2 + r
-// (ln2 split into a 16-bit head, so n * head is exact, and a tail), the
-// Taylor series of e^r to r^8 / 8! by Horner (|r| <= 0.35, truncation below
-// 2^-30 relative), then the scaling by 2^n, in two steps where 2^n is not a
-// normal float.  Within 1.2 ulp of e^x over the normal range.
+// h = bf16( SiLU(g) * u ), SiLU(g) = g / (1 + e^-g), in fp32 with one round
+// to nearest per operation (the file is built with -fmad=false and every
+// fused multiply-add is explicit).  e^x: Cody-Waite range reduction
+// x = n ln2 + r (ln2 split into a 16-bit head, so n * head is exact, and a
+// tail; both steps fused multiply-adds), the Taylor series of e^r to r^8 / 8!
+// by Horner with fused multiply-adds (|r| <= 0.35, truncation below 2^-30
+// relative), then the scaling by 2^n, in two steps where 2^n is not a normal
+// float.  The two elements of a bf16 word go through the polynomial as one
+// packed pair.
 __device__ __forceinline__ float pow2i(int k)  // 2^k, -126 <= k <= 127
 {
     return __int_as_float((k + 127) << 23);
 }
 
-__device__ __forceinline__ float exp_f32(float x)
+// e^x of one element from its reduced-range polynomial value q and n: the
+// case analysis (inf above the largest argument, 0 below the smallest, the
+// scaling by 2^n in two steps outside the normal range) with selects instead
+// of branches, so that independent elements interleave
+__device__ __forceinline__ float exp_finish(float x, float q, int n)
 {
-    if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
-    if (x < -103.972084045410156f) return 0.0f;
-    const float fn = rintf(__fmul_rn(x, 0x1.715476p+0f));
-    const int n = static_cast<int>(fn);
-    float r = __fsub_rn(x, __fmul_rn(fn, 0x1.62e4p-1f));
-    r = __fsub_rn(r, __fmul_rn(fn, 0x1.7f7d1cp-20f));
-    float q = 0x1.a01a02p-16f;
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.a01a02p-13f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.6c16c2p-10f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.111112p-7f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.555556p-5f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.555556p-3f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p-1f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p+0f);
-    q = __fadd_rn(__fmul_rn(q, r), 0x1.0p+0f);
-    if (n > 127) return __fmul_rn(__fmul_rn(q, 0x1.0p+127f), pow2i(n - 127));
-    if (n < -126) return __fmul_rn(__fmul_rn(q, pow2i(n + 100)), 0x1.0p-100f);
-    return __fmul_rn(q, pow2i(n));
+    // n > 127: (q 2^127) 2^(n-127); n < -126: (q 2^(n+100)) 2^-100; else q 2^n (x 1)
+    const int n1 = n < -126 ? n + 100 : (n > 127 ? 127 : n);
+    const float y = __fmul_rn(__fmul_rn(q, pow2i(n1)), pow2i(n - n1));
+    return x > 88.72283935546875f ? __int_as_float(0x7f800000) : (x < -103.972084045410156f ? 0.0f : y);
 }
 
-__device__ __forceinline__ uint32_t silu_mul_bf16(float g, float u)
+__device__ __forceinline__ float2 exp_f32x2(float2 x)
 {
-    const float s = __fdiv_rn(g, __fadd_rn(1.0f, exp_f32(-g)));
-    const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(s, u));
-    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&h));
+    // arguments outside [-104, 89] give inf or 0 above; clamping keeps n in range
+    const float2 xc = make_float2(fminf(fmaxf(x.x, -104.0f), 89.0f), fminf(fmaxf(x.y, -104.0f), 89.0f));
+    const float2 t = __fmul2_rn(xc, make_float2(0x1.715476p+0f, 0x1.715476p+0f));
+    const float2 fn = make_float2(rintf(t.x), rintf(t.y));
+    const float2 nfn = make_float2(-fn.x, -fn.y);
+    float2 r = __ffma2_rn(nfn, make_float2(0x1.62e4p-1f, 0x1.62e4p-1f), xc);
+    r = __ffma2_rn(nfn, make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f), r);
+    float2 q = make_float2(0x1.a01a02p-16f, 0x1.a01a02p-16f);
+    q = __ffma2_rn(q, r, make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f));
+    q = __ffma2_rn(q, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    q = __ffma2_rn(q, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+    q = __ffma2_rn(q, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+    q = __ffma2_rn(q, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+    q = __ffma2_rn(q, r, make_float2(0x1.0p-1f, 0x1.0p-1f));
+    q = __ffma2_rn(q, r, make_float2(0x1.0p+0f, 0x1.0p+0f));
+    q = __ffma2_rn(q, r, make_float2(0x1.0p+0f, 0x1.0p+0f));
+    return make_float2(exp_finish(x.x, q.x, static_cast<int>(fn.x)), exp_finish(x.y, q.y, static_cast<int>(fn.y)));
 }
 
-// Two bf16 words of gate and up values -> the word of the two h values.
+// Two bf16 words of gate and up values -> the word of the two h values
+// (element 2i in the low half).
 __device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
 {
-    return silu_mul_bf16(bf16lo(gw), bf16lo(uw)) | (silu_mul_bf16(bf16hi(gw), bf16hi(uw)) << 16);
+    const float2 g = make_float2(bf16lo(gw), bf16hi(gw));
+    const float2 e = exp_f32x2(make_float2(-g.x, -g.y));
+    const float sx = __fdiv_rn(g.x, __fadd_rn(1.0f, e.x));
+    const float sy = __fdiv_rn(g.y, __fadd_rn(1.0f, e.y));
+    const float2 p = __fmul2_rn(make_float2(sx, sy), make_float2(bf16lo(uw), bf16hi(uw)));
+    const __nv_bfloat162 h = __floats2bfloat162_rn(p.x, p.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // The same transform as quant_block with the natural register pairing
@@ -782,6 +795,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 // kSilu: the rows are the sorted rows of a [rows, 2F] gate|up matrix; each
 // stage lands the gate and the up slab of every row and the consumer forms
 // h = SiLU(g) * u before the transform.
+
 template <int STAGES, bool kSilu>
 __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
@@ -817,7 +831,9 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     }
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    for (int e = t; e <= a.E; e += blockDim.x) s_off[e] = a.offsets[e];
+    // no offsets: one group of all rows (the dense SwiGLU input)
+    for (int e = t; e <= a.E; e += blockDim.x)
+        s_off[e] = a.offsets ? a.offsets[e] : (e == 0 ? 0 : static_cast<int32_t>(a.rows_valid));
     __syncthreads();
     if (t == 0) {
         int32_t acc = 0;
@@ -965,7 +981,14 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty0 + 8 * s);
         if (valid) {
-            if (ex != cur_e) {
+            if (kSilu) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) raw[i] = silu_mul_word(raw[i], up[i]);
+            }
+            // the row's expert factors: kept across rows of the same expert,
+            // except in the SwiGLU path, which reloads them (from L1) after h
+            // is formed so that they are not live during the SwiGLU step
+            if (kSilu || ex != cur_e) {
                 cur_e = ex;
                 const float4 *f4 = reinterpret_cast<const float4 *>(a.f + static_cast<int64_t>(ex) * a.K + 32 * kb);
 #pragma unroll
@@ -974,10 +997,6 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                     f[2 * q] = make_float2(v4.x, v4.y);
                     f[2 * q + 1] = make_float2(v4.z, v4.w);
                 }
-            }
-            if (kSilu) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) raw[i] = silu_mul_word(raw[i], up[i]);
             }
             uint4 codes;
             sbyte = quant_block_pairs<false>(raw, f, codes);

@@ -113,6 +113,30 @@ def make_dense(wl: DenseWorkload | str, with_weight: bool = True) -> dict:
     return out
 
 
+def make_dense_gated(wl: DenseWorkload | str) -> dict:
+    """The gated-MLP form of a SwiGLU-input workload: GU [M, 2K] bf16 with the
+    gate a ~ N(0,1) in columns 0..K-1 and the up b * col (b ~ N(0,1), the
+    outlier gains on the up side) in K..2K-1, so that SiLU(a) * b * col has
+    the distribution of the workload's X; calibration rows X_calib are drawn
+    as for make_dense (the down input itself); W as for make_dense."""
+    if isinstance(wl, str):
+        wl = DENSE[wl]
+    assert wl.act == "swiglu"
+    g = torch.Generator().manual_seed(wl.seed + 1000)
+    col, idx = _outlier_gain_vector(g, wl.K, wl.outlier_frac, wl.outlier_channels,
+                                    wl.outlier_gain)
+    GU = torch.empty(wl.M, 2 * wl.K, dtype=torch.bfloat16)
+    step = max(1, (1 << 24) // wl.K)
+    for r0 in range(0, wl.M, step):
+        r1 = min(wl.M, r0 + step)
+        a = torch.randn(r1 - r0, wl.K, generator=g)
+        b = torch.randn(r1 - r0, wl.K, generator=g)
+        GU[r0:r1, :wl.K] = a.to(torch.bfloat16)
+        GU[r0:r1, wl.K:] = (b * col).to(torch.bfloat16)
+    Xc = _draw_rows(g, wl.calib_rows, wl.K, col, wl.act)
+    return {"GU": GU, "X_calib": Xc, "outliers": idx, "workload": wl, "W": _draw_weight(g, (wl.N, wl.K))}
+
+
 def make_matrix(rows: int, K: int, seed: int, outlier_channels=(), gain: float = 50.0,
                 act: str = "normal") -> torch.Tensor:
     """A free-form seeded bf16 matrix for edge-case tests (ragged shapes)."""
