@@ -68,6 +68,7 @@ def lib():
             "oracle_silu_mul": [P, I, I, P],
             "oracle_exp_many": [P, I, P],
             "oracle_flip_hessian": [P, I, I, ctypes.c_float, P],
+            "oracle_moe_combine": [P, I, P, P, I, I, I, P],
             "oracle_flip_refine": [P, P, I, I, ctypes.c_int32, P, P, P],
         }
         for name, args in sig.items():
@@ -326,3 +327,20 @@ def flip_error(Wt: np.ndarray, H: np.ndarray, codes: np.ndarray, scales: np.ndar
     """E = (Wt - q)^T H (Wt - q) per row in fp64 (q the exact dequantised codes)."""
     r = np.asarray(Wt, np.float64) - dequant(codes, scales)
     return np.einsum("nk,nk->n", r @ np.asarray(H, np.float64), r)
+
+
+# ----------------------------------------------------------- MoE combine
+
+def moe_combine(Y, tok_rows: np.ndarray, tok_weights: np.ndarray) -> np.ndarray:
+    """Token outputs (bf16 bits [T, N]) from the expert rows Y (sorted order):
+    per token, the fp32 fused multiply-add chain over its top-k choices of
+    weight * row, from +0, rounded once to bf16."""
+    y = bf16_bits(Y)
+    n_cols = y.shape[1]
+    r = np.ascontiguousarray(tok_rows, dtype=np.int32)
+    w = np.ascontiguousarray(tok_weights, dtype=np.float32)
+    T, topk = r.shape
+    assert r.min() >= 0 and r.max() < y.shape[0]
+    out = np.empty((T, n_cols), np.uint16)
+    lib().oracle_moe_combine(_p(y), n_cols, _p(r), _p(w), T, topk, n_cols, _p(out))
+    return out

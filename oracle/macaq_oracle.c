@@ -40,6 +40,12 @@
  *                    store).  The CUDA path evaluates the same operations in
  *                    the same order; both are pinned against fp64 exp.
  *
+ *   MoE combine      (extension: the expert outputs of a token's top-k rows,
+ *                    weighted by their routing probabilities, summed into the
+ *                    token's output.)  Stated in fp32: a fused multiply-add
+ *                    chain over the token's choices in order, from +0, then
+ *                    one rounding to bf16.
+ *
  *   Flip Refinement  (page "What is MACaQ quantization", section "How MACaQ
  *                    works", step "Flip Refinement": instead of plain round to
  *                    nearest, a Hessian-aware coordinate descent moves single
@@ -609,5 +615,23 @@ void oracle_flip_refine(const float *wt, const float *h, int64_t n, int64_t k, i
         if (flips) flips[row] = moves;
         free(r);
         free(g);
+    }
+}
+
+/* ---------------------------------------------------------- MoE combine */
+
+/* out[t, n] = bf16( fma-chain over k = 0 .. topk-1 of w[t, k] * y[rows[t, k], n]
+ * from +0 ), y bf16 bits [*, n_cols] row pitch ldy, out bf16 bits [t, n_cols]. */
+void oracle_moe_combine(const uint16_t *y, int64_t ldy, const int32_t *rows, const float *w,
+                        int64_t t_count, int64_t topk, int64_t n_cols, uint16_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < t_count; ++t) {
+        for (int64_t n = 0; n < n_cols; ++n) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < topk; ++k)
+                acc = fmaf(w[t * topk + k], bf16_bits_to_f32(y[(int64_t)rows[t * topk + k] * ldy + n]), acc);
+            out[t * n_cols + n] = f32_to_bf16_rne(acc);
+        }
     }
 }

@@ -190,8 +190,10 @@ def route(logits: torch.Tensor, topk: int, E: int) -> dict:
     """Top-k routing by softmax probability, rows sorted by expert (stable).
 
     Returns ``row_src`` (token of each sorted row, int32), ``row_expert``,
-    ``offsets`` (int32 [E+1]) and ``weights`` (fp32 routing probability of
-    each sorted row).
+    ``offsets`` (int32 [E+1]), ``weights`` (fp32 routing probability of
+    each sorted row), and per token ``tok_rows`` (int32 [T, topk], the sorted
+    row of its k-th choice) and ``tok_weights`` (fp32 [T, topk], that choice's
+    probability).
     """
     probs = torch.softmax(logits.float(), dim=-1)
     topv, topi = probs.topk(topk, dim=-1)
@@ -204,7 +206,11 @@ def route(logits: torch.Tensor, topk: int, E: int) -> dict:
     counts = torch.bincount(row_expert, minlength=E)
     offsets = torch.zeros(E + 1, dtype=torch.int64)
     offsets[1:] = torch.cumsum(counts, 0)
+    inv = torch.empty_like(order)
+    inv[order] = torch.arange(order.numel(), dtype=order.dtype)
     return {
+        "tok_rows": inv.view(T, topk).to(torch.int32).contiguous(),
+        "tok_weights": topv.contiguous(),
         "row_src": flat_t[order].to(torch.int32),
         "row_expert": row_expert.to(torch.int32),
         "offsets": offsets.to(torch.int32),
