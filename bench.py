@@ -876,7 +876,8 @@ def gpu_arm_flip(args, rank: int, world: int):
 def moe_workload_config(wl):
     return {"workload": f"{wl.name}: {wl.T} tokens x top-{wl.topk} of {wl.E} experts = {wl.rows} rows; "
                         f"gate+up K={wl.K} N={2 * wl.F}, SiLU(gate)*up fused into the down input's "
-                        f"transform, down K={wl.F} N={wl.K}; bf16 in/out, MXFP4 W4A4",
+                        f"transform, down K={wl.F} N={wl.K}, weighted top-{wl.topk} combine into the "
+                        f"token outputs; bf16 in/out, MXFP4 W4A4",
             "T": wl.T, "E": wl.E, "topk": wl.topk, "K": wl.K, "F": wl.F, "rows": wl.rows,
             "l2": "weights (302 MB of codes) exceed L2; no input rotation needed"}
 
@@ -958,10 +959,13 @@ def gpu_arm_moe(args, rank: int, world: int):
     as_dn = torch.empty(mq.macaq_scale_bytes(P, F), dtype=torch.uint8, device=dev)
     Ygu = torch.empty(rows, 2 * F, dtype=torch.bfloat16, device=dev)
     Ydn = torch.empty(rows, K, dtype=torch.bfloat16, device=dev)
+    tok_rows = r["tok_rows"].to(dev)
+    tok_w = r["tok_weights"].to(dev)
+    Ytok = torch.empty(wl.T, K, dtype=torch.bfloat16, device=dev)
 
     def step(ev=None, Xin=None, Yout=None):
         Xin = X if Xin is None else Xin
-        Yout = Ydn if Yout is None else Yout
+        Yout = Ytok if Yout is None else Yout
         if ev is not None:
             ev[0].record(stream)
         mq.macaq_quant_act_grouped(Xin, row_src, offs, inv_gu, rows, E, a_gu, as_gu)
@@ -974,9 +978,13 @@ def gpu_arm_moe(args, rank: int, world: int):
         mq.macaq_quant_act_grouped_silu(Ygu, offs, inv_dn, rows, E, a_dn, as_dn)
         if ev is not None:
             ev[3].record(stream)
-        mq.macaq_grouped_w4a4_gemm(a_dn, as_dn, wdn_codes, wdn_scales, offs, rows, E, K, F, Y=Yout)
+        mq.macaq_grouped_w4a4_gemm(a_dn, as_dn, wdn_codes, wdn_scales, offs, rows, E, K, F, Y=Ydn)
         if ev is not None:
             ev[4].record(stream)
+        # the token outputs: each token's eight expert rows, weighted
+        mq.macaq_moe_combine(Ydn, tok_rows, tok_w, out=Yout)
+        if ev is not None:
+            ev[5].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -988,7 +996,7 @@ def gpu_arm_moe(args, rank: int, world: int):
     graph = None if args.no_graphs else capture_graph(lambda: [step() for _ in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
     timed = plan.event_steps
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)] for i in timed}
+    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(6)] for i in timed}
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -1012,7 +1020,7 @@ def gpu_arm_moe(args, rank: int, world: int):
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    avg = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs.values()) for j in range(4)]
+    avg = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs.values()) for j in range(5)]
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
@@ -1029,15 +1037,18 @@ def gpu_arm_moe(args, rank: int, world: int):
     q_bytes = [wl.T * K * 2 + rows * (K // 2 + K // 32), rows * 2 * F * 2 + rows * (F // 2 + F // 32)]
     gu_gbs = gu_bytes / (avg[1] * 1e-3) / 1e9
     dn_gbs = dn_bytes / (avg[3] * 1e-3) / 1e9
+    # combine: every expert row read once, every token row written once
+    cb_bytes = rows * K * 2 + wl.T * K * 2 + wl.T * wl.topk * 8
+    cb_gbs = cb_bytes / (avg[4] * 1e-3) / 1e9
 
-    # end to end through the C ABI: pinned host tokens in, pinned host down output out
+    # end to end through the C ABI: pinned host tokens in, pinned host token outputs out
     e2e_steps = max(3, min(args.steps, 20))
     Xh = d["X"].pin_memory()
-    Yh = [torch.empty(rows, K, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    Yh = [torch.empty(wl.T, K, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     for _ in range(2):
         X.copy_(Xh, non_blocking=True)
         step()
-        Yh[0].copy_(Ydn, non_blocking=True)
+        Yh[0].copy_(Ytok, non_blocking=True)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -1045,11 +1056,11 @@ def gpu_arm_moe(args, rank: int, world: int):
     for _ in range(e2e_steps):
         X.copy_(Xh, non_blocking=True)
         step()
-        Yh[0].copy_(Ydn, non_blocking=True)
+        Yh[0].copy_(Ytok, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
-    Xs, Ys = [X, torch.empty_like(X)], [Ydn, torch.empty_like(Ydn)]
+    Xs, Ys = [X, torch.empty_like(X)], [Ytok, torch.empty_like(Ytok)]
     e2e_ms = e2e_pipelined(stream, e2e_steps, 2,
                            lambda k: Xs[k].copy_(Xh, non_blocking=True),
                            lambda k: step(Xin=Xs[k], Yout=Ys[k]),
@@ -1091,6 +1102,9 @@ def gpu_arm_moe(args, rank: int, world: int):
         "down_gemm": {"achieved": dn_gbs, "unit": "GB/s", "frac": dn_gbs / peaks["hbm_gbs"],
                       "bytes_per_launch": dn_bytes, "avg_launch_us": avg[3] * 1e3,
                       "tflops": wl.flops_down / (avg[3] * 1e-3) / 1e12},
+        "combine": {"kernel": "moe_combine_kernel", "achieved": cb_gbs, "unit": "GB/s",
+                    "frac": cb_gbs / peaks["hbm_gbs"], "bytes_per_launch": cb_bytes,
+                    "avg_launch_us": avg[4] * 1e3},
         "act_quant": {"kernel": "quant_grouped_tma_kernel (token rows; SwiGLU-fused for the down input)",
                       "achieved": [q_bytes[0] / (avg[0] * 1e-3) / 1e9, q_bytes[1] / (avg[2] * 1e-3) / 1e9],
                       "peak": peaks["hbm_gbs"], "unit": "GB/s (gate+up input, down input)",
@@ -1099,11 +1113,11 @@ def gpu_arm_moe(args, rank: int, world: int):
                       "bytes_per_launch": q_bytes, "avg_launch_us": [avg[0] * 1e3, avg[2] * 1e3]},
         "cpu_baseline": cpu,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": wl.T * K * 2, "d2h_bytes_per_step": rows * K * 2,
+                "h2d_bytes_per_step": wl.T * K * 2, "d2h_bytes_per_step": wl.T * K * 2,
                 "ms_per_step": e2e_ms,
                 "copies": "overlapped across steps (2 buffer slots, separate copy streams)",
                 "serial_ms_per_step": e2e_serial_ms},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "clocks": sampler.summary(),

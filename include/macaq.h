@@ -363,6 +363,23 @@ macaq_status macaq_flip_sweeps(const float *H, int64_t N, int64_t K, int32_t swe
                                const uint8_t *w_scales, int32_t *flips, void *workspace, size_t ws_bytes,
                                macaq_stream_t stream);
 
+/* ------------------------------------------------------ MoE combine */
+
+/* The routed layer's output: token t's row is the weighted sum of the expert
+ * rows of its top-k choices (the rows macaq_grouped_w4a4_gemm wrote, in
+ * expert-sorted order).  The pages run the routed projections in W4A4 (page
+ * "Huawei MACaQ Is an Open-Source Model Quantizer", section "MACaQ
+ * Backends") and give no combine arithmetic; reading:
+ *   out[t, n] = bf16_rn( fp32 fused multiply-add chain over k = 0 .. topk-1
+ *               of tok_weights[t, k] * Y[tok_rows[t, k], n], from +0 )
+ * Y bf16 [y_rows, ldy]; tok_rows int32 [T, topk] (row of each choice; rows
+ * outside [0, y_rows) contribute nothing); tok_weights fp32 [T, topk]; out
+ * bf16 [T, ldo].  N % 8 == 0, ldy and ldo multiples of 8, Y and out 16-byte
+ * aligned; 0 < topk <= 1024. */
+macaq_status macaq_moe_combine(const void *Y, int64_t ldy, int64_t y_rows, const int32_t *tok_rows,
+                               const float *tok_weights, int64_t T, int64_t topk, int64_t N, void *out,
+                               int64_t ldo, macaq_stream_t stream);
+
 /* --------------------------------------------------- device errors */
 
 /* Every device-side wait of the GEMM kernels is bounded in time.  A wait that

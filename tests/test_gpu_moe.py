@@ -214,3 +214,47 @@ def test_down_fused_swiglu(name, experts):
         cw, sw = oracle.quantize(d["W_down"][e], s_np[e])
         da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
         check_gemm(bf16_to_np(Y[lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), F)
+
+
+@pytest.mark.parametrize("name", ["moe", "small"])
+def test_combine_bitexact_full_routing(name):
+    """The weighted combine over the MoE workloads' routing (4096 tokens x
+    top-8, N = 2048; 96 tokens x top-2, N = 256), bit-exact against the
+    oracle on the same expert rows."""
+    d = moe(name)
+    wl = d["workload"]
+    r = d["routing"]
+    rng = np.random.default_rng(4)
+    Y = torch.from_numpy(rng.normal(0, 1, (wl.rows, wl.K)).astype(np.float32)).to(torch.bfloat16)
+    out = mq.macaq_moe_combine(to_dev(Y), to_dev(r["tok_rows"]), to_dev(r["tok_weights"]))
+    torch.cuda.synchronize()
+    want = oracle.moe_combine(Y, r["tok_rows"].numpy(), r["tok_weights"].numpy())
+    np.testing.assert_array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), want)
+
+
+def test_combine_order_and_invalid_rows():
+    vals = np.array([1.0, 2.0 ** -8] + [2.0 ** -25] * 4, np.float32)
+    Y = torch.from_numpy(np.repeat(vals[:, None], 8, 1)).to(torch.bfloat16)
+    fwd = torch.arange(6, dtype=torch.int32).view(1, 6)
+    rev = torch.flip(fwd, [1]).contiguous()
+    w = torch.ones(1, 6, dtype=torch.float32)
+    a = mq.macaq_moe_combine(to_dev(Y), to_dev(fwd), to_dev(w)).float().cpu()
+    b = mq.macaq_moe_combine(to_dev(Y), to_dev(rev), to_dev(w)).float().cpu()
+    assert torch.all(a == 1.0) and torch.all(b == 1.0 + 2.0 ** -7)
+    # a choice outside the expert rows contributes nothing
+    rows = torch.tensor([[0, -1, 6, 1]], dtype=torch.int32)
+    wts = torch.tensor([[1.0, 1.0, 1.0, 4.0]])
+    c = mq.macaq_moe_combine(to_dev(Y), to_dev(rows), to_dev(wts)).float().cpu()
+    assert torch.all(c == 1.0 + 2.0 ** -6)
+
+
+@pytest.mark.parametrize("T,topk,N", [(37, 3, 64), (5, 1, 8), (300, 16, 136)])
+def test_combine_any_choice_count(T, topk, N):
+    rng = np.random.default_rng(T + topk)
+    Y = torch.from_numpy(rng.normal(0, 1, (T * topk + 5, N)).astype(np.float32)).to(torch.bfloat16)
+    rows = torch.from_numpy(rng.permutation(T * topk + 5)[:T * topk].astype(np.int32).reshape(T, topk))
+    w = torch.from_numpy(rng.uniform(0, 1, (T, topk)).astype(np.float32))
+    out = mq.macaq_moe_combine(to_dev(Y), to_dev(rows), to_dev(w))
+    torch.cuda.synchronize()
+    want = oracle.moe_combine(Y, rows.numpy(), w.numpy())
+    np.testing.assert_array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), want)

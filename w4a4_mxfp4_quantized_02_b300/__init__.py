@@ -73,6 +73,7 @@ _SIGS = {
     "macaq_flip_prepare": ([_P, _P, _I64, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_flip_sweeps": ([_P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_quant_act_silu": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_moe_combine": ([_P, _I64, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_check_device_error": ([_P], ctypes.c_int),
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
@@ -274,6 +275,22 @@ def macaq_linear_no_alloc(X: torch.Tensor, inv_s, w_codes, w_scales, N: int, Y=N
         _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y),
         _stream(stream)))
     return Y
+
+
+def macaq_moe_combine(Y: torch.Tensor, tok_rows: torch.Tensor, tok_weights: torch.Tensor, out=None,
+                      stream=None):
+    """Token outputs [T, N] from the expert rows Y (sorted order)."""
+    _dev(Y, "Y")
+    T, topk = tok_rows.shape
+    N = Y.shape[1]
+    if not tok_rows.is_contiguous() or not tok_weights.is_contiguous():
+        raise ValueError("tok_rows and tok_weights must be contiguous [T, topk]")
+    if out is None:
+        out = torch.empty(T, N, dtype=torch.bfloat16, device=Y.device)
+    _check("macaq_moe_combine", lib().macaq_moe_combine(
+        _ptr(Y), _ld(Y), Y.shape[0], _ptr(tok_rows), _ptr(tok_weights), T, topk, N, _ptr(out), _ld(out),
+        _stream(stream)))
+    return out
 
 
 # --------------------------------------------------------- W4A16 fallback

@@ -31,6 +31,7 @@ UNITS = {
     "static_scratch.cu": [],
     "w4a16.cu": [],
     "flip.cu": ["-fmad=false"],
+    "moe.cu": ["-fmad=false"],
 }
 HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh"]
 

@@ -536,6 +536,24 @@ macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_sc
     return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_moe_combine(const void *Y, int64_t ldy, int64_t y_rows, const int32_t *tok_rows,
+                               const float *tok_weights, int64_t T, int64_t topk, int64_t N, void *out,
+                               int64_t ldo, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_rows(T));
+    MACAQ_TRY(check_rows(N));
+    MACAQ_TRY(check_rows(y_rows));
+    if (topk <= 0 || topk > 1024 || N % 8 != 0) return MACAQ_ERR_INVALID_ARG;
+    if (T == 0 || N == 0) return MACAQ_OK;
+    if (!Y || !tok_rows || !tok_weights || !out || ldy < N || ldo < N) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(out) || ldy % 8 != 0 || ldo % 8 != 0 ||
+        (reinterpret_cast<uintptr_t>(tok_rows) & 3u) || (reinterpret_cast<uintptr_t>(tok_weights) & 3u))
+        return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_moe_combine(static_cast<const uint16_t *>(Y), ldy, y_rows, tok_rows, tok_weights, T,
+                                        topk, N, static_cast<uint16_t *>(out), ldo,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 macaq_status macaq_check_device_error(macaq_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -70,6 +70,11 @@ cudaError_t launch_flip_sweeps(const float *h, const float *g, int64_t n, int64_
                                uint8_t *codes, const uint8_t *scales, int32_t *flips, cudaStream_t stream);
 cudaError_t read_and_clear_flip_error(unsigned *flags);
 
+// MoE combine: out[t, :] = bf16(fma chain over k of w[t, k] * Y[rows[t, k], :]).
+cudaError_t launch_moe_combine(const uint16_t *Y, int64_t ldy, int64_t y_rows, const int32_t *rows,
+                               const float *w, int64_t T, int64_t topk, int64_t N, uint16_t *out, int64_t ldo,
+                               cudaStream_t stream);
+
 cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_rows, int64_t mc,
                            const uint16_t *w, int64_t n, int64_t k, float *s, float *inv_s,
                            cudaStream_t stream);
