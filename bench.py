@@ -402,10 +402,7 @@ def gpu_arm(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     q_ms = [e[0].elapsed_time(e[1]) for e in evs.values()]
     g_ms = [e[1].elapsed_time(e[2]) for e in evs.values()]
     status = mq.macaq_check_device_error()
@@ -638,10 +635,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
     g_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
     status = mq.macaq_check_device_error()
@@ -1016,10 +1010,7 @@ def gpu_arm_moe(args, rank: int, world: int):
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     avg = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs.values()) for j in range(5)]
     status = mq.macaq_check_device_error()
     if status != 0:
@@ -1153,6 +1144,18 @@ class StepPlan:
             return (f"{self.replays} replays of a CUDA graph of {self.chunk} steps, then "
                     f"{len(self.eager_steps)} eager steps with per-kernel events")
         return f"eager launches; per-kernel events on {len(self.event_steps)} steps"
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (one all-reduce; x itself when alone)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def e2e_pipelined(stream, steps: int, nslot: int, h2d, run, d2h) -> float:
