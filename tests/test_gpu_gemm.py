@@ -143,3 +143,26 @@ def test_empty_is_noop():
     a = torch.zeros(16, dtype=torch.uint8, device=DEV)
     mq.macaq_w4a4_gemm(a, a, a, a, 0, 64, 128, Y=Y)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,N,K", [(65, 136, 96), (130, 256, 288), (257, 520, 5120), (1000, 384, 1056),
+                                   (4097, 264, 768)])
+def test_linear_workspace_matches_two_calls(M, N, K):
+    """macaq_linear: the codes and every tiled scale byte it leaves in its
+    workspace, and Y, equal those of macaq_quant_act + macaq_w4a4_gemm."""
+    X = workloads.make_matrix(M, K + 8, seed=M + K, outlier_channels=(2, K // 2))[:, :K]
+    W = workloads.make_weight(N, K, seed=N)
+    f = torch.from_numpy(np.random.default_rng(M).uniform(0.05, 20.0, K).astype(np.float32)).to(DEV)
+    w_codes, w_scales = mq.macaq_quant_weight(to_dev(W), f)
+    Xd = to_dev(X)
+    ws = torch.full((mq.macaq_linear_workspace_bytes(M, K),), 0xAB, dtype=torch.uint8, device=DEV)
+    Y = mq.macaq_linear(Xd, f, w_codes, w_scales, N, workspace=ws)
+    a_codes, a_scales = mq.macaq_quant_act(Xd, f)
+    Y2 = mq.macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K)
+    torch.cuda.synchronize()
+    assert mq.macaq_check_device_error() == 0
+    nc = M * (K // 2)
+    off = (nc + 255) // 256 * 256
+    np.testing.assert_array_equal(u8(ws[:nc]).reshape(M, K // 2), u8(a_codes))
+    np.testing.assert_array_equal(u8(ws[off:off + a_scales.numel()]), u8(a_scales))
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
