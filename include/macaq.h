@@ -136,6 +136,13 @@ macaq_status macaq_quant_weight_grouped(const void *W, const float *s, int64_t E
                                         int64_t K, uint8_t *w_codes, uint8_t *w_scales,
                                         macaq_stream_t stream);
 
+/* The grouped weight preparation with a Hadamard block of 32 or 64 channels
+ * (see macaq_quant_act_hb; K % hadamard_block == 0); arguments and layouts as
+ * macaq_quant_weight_grouped. */
+macaq_status macaq_quant_weight_grouped_hb(const void *W, const float *s, int64_t E, int64_t N, int64_t K,
+                                           int64_t hadamard_block, uint8_t *w_codes, uint8_t *w_scales,
+                                           macaq_stream_t stream);
+
 /* ------------------------------------------------------------ GEMM */
 
 /* Block-scaled MXFP4 x MXFP4 GEMM with bf16 output (the hot path's second
@@ -206,6 +213,14 @@ macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *
                                      int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
                                      uint8_t *a_scales, macaq_stream_t stream);
 
+/* macaq_quant_act_grouped with a Hadamard block of 32 or 64 channels (the
+ * 64-channel block of macaq_quant_act_hb, the recipe's "--had-block 64");
+ * K % hadamard_block == 0. */
+macaq_status macaq_quant_act_grouped_hb(const void *X, int64_t ldx, const int32_t *row_src,
+                                        const int32_t *expert_offsets, const float *inv_s, int64_t rows,
+                                        int64_t E, int64_t K, int64_t hadamard_block, uint8_t *a_codes,
+                                        uint8_t *a_scales, macaq_stream_t stream);
+
 /* Grouped activation transform of a gated MLP's down-projection input,
  * fused with its SwiGLU step.  GU bf16 [rows, ldgu] holds, in sorted row
  * order, the gate (columns 0..F-1) and up (columns F..2F-1) outputs of the
@@ -225,6 +240,13 @@ macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *
 macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
                                           const float *inv_s, int64_t rows, int64_t E, int64_t F,
                                           uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream);
+
+/* macaq_quant_act_grouped_silu with a Hadamard block of 32 or 64 channels;
+ * F % hadamard_block == 0. */
+macaq_status macaq_quant_act_grouped_silu_hb(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
+                                             const float *inv_s, int64_t rows, int64_t E, int64_t F,
+                                             int64_t hadamard_block, uint8_t *a_codes, uint8_t *a_scales,
+                                             macaq_stream_t stream);
 
 /* The same fused SwiGLU transform for a dense gated MLP (the down
  * projection's input h = bf16(SiLU(g) * u), SiLU and rounding as

@@ -111,6 +111,15 @@ def test_hadamard_block_rejections(L):
     assert q(p, 96, p, 4, 96, 64, p, p, None) == INVALID        # K % 64 != 0
     assert w(p, p, 4, 96, 64, p, p, None) == INVALID
     assert q(p, 128, p, 0, 128, 64, p, p, None) == OK           # M = 0: nothing to do
+    g = L.macaq_quant_act_grouped_hb
+    assert g(p, 128, p, p, p, 100, 4, 128, 16, p, p, None) == INVALID     # block neither 32 nor 64
+    assert g(p, 96, p, p, p, 100, 4, 96, 64, p, p, None) == INVALID       # K % 64 != 0
+    z = L.macaq_quant_act_grouped_silu_hb
+    assert z(p, 256, p, p, 100, 4, 96, 64, p, p, None) == INVALID         # F % 64 != 0
+    wg = L.macaq_quant_weight_grouped_hb
+    assert wg(p, p, 4, 8, 96, 64, p, p, None) == INVALID
+    assert wg(p, p, 4, 8, 128, 48, p, p, None) == INVALID
+    assert wg(p, p, 0, 8, 128, 64, p, p, None) == OK
 
 
 def test_w4a16_rejections(L):

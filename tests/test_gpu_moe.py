@@ -45,7 +45,7 @@ def _calib_rows(routing, e):
     return routing["row_src"][off[e]:off[e + 1]]
 
 
-def run_gate_up(d, experts=None):
+def run_gate_up(d, experts=None, hb=32):
     """CUDA path and oracle for the gate+up projection; returns both sides."""
     wl = d["workload"]
     E, K, F = wl.E, wl.K, wl.F
@@ -57,12 +57,12 @@ def run_gate_up(d, experts=None):
         rows = to_dev(_calib_rows(d["calib_routing"], e))
         se, ie = mq.macaq_balance_scales(Xc, W[e], xc_rows=rows)
         s[e], inv[e] = se, ie
-    w_codes, w_scales = mq.macaq_quant_weight_grouped(W, s)
+    w_codes, w_scales = mq.macaq_quant_weight_grouped(W, s, hadamard_block=hb)
     r = d["routing"]
     rows_n = int(r["offsets"][-1])
     offs = to_dev(r["offsets"])
     a_codes, a_scales = mq.macaq_quant_act_grouped(to_dev(d["X"]), to_dev(r["row_src"]), offs, inv,
-                                                   rows_n, E)
+                                                   rows_n, E, hadamard_block=hb)
     Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, 2 * F, K)
     torch.cuda.synchronize()
     return dict(s=s, inv=inv, w_codes=w_codes, w_scales=w_scales, a_codes=a_codes,
@@ -258,3 +258,50 @@ def test_combine_any_choice_count(T, topk, N):
     torch.cuda.synchronize()
     want = oracle.moe_combine(Y, rows.numpy(), w.numpy())
     np.testing.assert_array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), want)
+
+
+@pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 3, 77, 127))])
+def test_moe_hadamard_block_64(name, experts):
+    """The 64-channel Hadamard block through the routed layer: grouped weight
+    preparation, grouped token transform, the SwiGLU-fused down input, all
+    bit-exact against the oracle's 64-block transform; GEMMs unchanged."""
+    d = moe(name)
+    wl = d["workload"]
+    E, K, F = wl.E, wl.K, wl.F
+    gpu = run_gate_up(d, hb=64)
+    r = d["routing"]
+    off = r["offsets"].numpy()
+    pos = padded_positions(off)
+    P = gpu["a_codes"].shape[0]
+    sb = mq.macaq_scale_bytes(2 * F, K)
+    sc = untile_scales(u8(gpu["a_scales"]), P, K)
+    s_all, inv_all = gpu["s"].cpu().numpy(), gpu["inv"].cpu().numpy()
+    for e in (range(E) if experts is None else experts):
+        cw, sw = oracle.quantize(d["W_gu"][e], s_all[e], hb=64)
+        np.testing.assert_array_equal(u8(gpu["w_codes"][e]), cw)
+        np.testing.assert_array_equal(u8(gpu["w_scales"][e * sb:(e + 1) * sb]), oracle.tile_scales(sw))
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        ca, sa = oracle.quantize(d["X"][r["row_src"][lo:hi].long()], inv_all[e], hb=64)
+        np.testing.assert_array_equal(u8(gpu["a_codes"])[pos[lo:hi]], ca)
+        np.testing.assert_array_equal(sc[pos[lo:hi]], sa)
+        da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+        check_gemm(bf16_to_np(gpu["Y"][lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
+    # the down input: SiLU fused, 64-channel block
+    rng = np.random.default_rng(9)
+    inv_dn = (np.float32(1.0) / rng.uniform(0.1, 10.0, (E, F)).astype(np.float32)).astype(np.float32)
+    rows_n = int(off[-1])
+    a_codes, a_scales = mq.macaq_quant_act_grouped_silu(gpu["Y"], to_dev(r["offsets"]),
+                                                        torch.from_numpy(inv_dn).to(DEV), rows_n, E,
+                                                        hadamard_block=64)
+    torch.cuda.synchronize()
+    H = oracle.silu_mul(gpu["Y"].cpu())
+    scd = untile_scales(u8(a_scales), a_codes.shape[0], F)
+    for e in (range(E) if experts is None else experts):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        ca, sa = oracle.quantize(H[lo:hi], inv_dn[e], hb=64)
+        np.testing.assert_array_equal(u8(a_codes)[pos[lo:hi]], ca)
+        np.testing.assert_array_equal(scd[pos[lo:hi]], sa)

@@ -74,6 +74,11 @@ _SIGS = {
     "macaq_flip_sweeps": ([_P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_quant_act_silu": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_moe_combine": ([_P, _I64, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_quant_weight_grouped_hb": ([_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_quant_act_grouped_hb": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P],
+                                   ctypes.c_int),
+    "macaq_quant_act_grouped_silu_hb": ([_P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P],
+                                        ctypes.c_int),
     "macaq_check_device_error": ([_P], ctypes.c_int),
     "macaq_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_int),
     "macaq_debug_wait_probe": ([_P], ctypes.c_int),
@@ -222,7 +227,7 @@ def macaq_quant_weight_hb(W: torch.Tensor, s: torch.Tensor, hadamard_block: int,
 
 
 def macaq_quant_weight_grouped(W: torch.Tensor, s: torch.Tensor, w_codes=None, w_scales=None,
-                               stream=None):
+                               stream=None, hadamard_block: int = 32):
     _dev(W, "W")
     E, N, K = W.shape
     if not W.is_contiguous():
@@ -231,8 +236,12 @@ def macaq_quant_weight_grouped(W: torch.Tensor, s: torch.Tensor, w_codes=None, w
         w_codes = torch.empty(E, N, K // 2, dtype=torch.uint8, device=W.device)
     if w_scales is None:
         w_scales = torch.empty(E * macaq_scale_bytes(N, K), dtype=torch.uint8, device=W.device)
-    _check("macaq_quant_weight_grouped", lib().macaq_quant_weight_grouped(
-        _ptr(W), _ptr(s), E, N, K, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
+    if hadamard_block == 32:
+        _check("macaq_quant_weight_grouped", lib().macaq_quant_weight_grouped(
+            _ptr(W), _ptr(s), E, N, K, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
+    else:
+        _check("macaq_quant_weight_grouped_hb", lib().macaq_quant_weight_grouped_hb(
+            _ptr(W), _ptr(s), E, N, K, hadamard_block, _ptr(w_codes), _ptr(w_scales), _stream(stream)))
     return w_codes, w_scales
 
 
@@ -430,7 +439,7 @@ def macaq_flip_sweeps(H: torch.Tensor, N: int, K: int, w_codes, w_scales, worksp
 # ----------------------------------------------------------- grouped (MoE)
 
 def macaq_quant_act_grouped(X, row_src, expert_offsets, inv_s, rows: int, E: int, a_codes=None,
-                            a_scales=None, stream=None):
+                            a_scales=None, stream=None, hadamard_block: int = 32):
     _dev(X, "X")
     K = X.shape[1]
     P = macaq_grouped_padded_rows(rows, E)
@@ -438,9 +447,14 @@ def macaq_quant_act_grouped(X, row_src, expert_offsets, inv_s, rows: int, E: int
         a_codes = torch.empty(P, K // 2, dtype=torch.uint8, device=X.device)
     if a_scales is None:
         a_scales = torch.empty(macaq_scale_bytes(P, K), dtype=torch.uint8, device=X.device)
-    _check("macaq_quant_act_grouped", lib().macaq_quant_act_grouped(
-        _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
-        _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    if hadamard_block == 32:
+        _check("macaq_quant_act_grouped", lib().macaq_quant_act_grouped(
+            _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
+            _ptr(a_codes), _ptr(a_scales), _stream(stream)))
+    else:
+        _check("macaq_quant_act_grouped_hb", lib().macaq_quant_act_grouped_hb(
+            _ptr(X), _ld(X), _ptr(row_src), _ptr(expert_offsets), _ptr(inv_s), rows, E, K,
+            hadamard_block, _ptr(a_codes), _ptr(a_scales), _stream(stream)))
     return a_codes, a_scales
 
 
@@ -460,7 +474,7 @@ def macaq_quant_act_silu(GU: torch.Tensor, inv_s: torch.Tensor, a_codes=None, a_
 
 
 def macaq_quant_act_grouped_silu(GU, expert_offsets, inv_s, rows: int, E: int, a_codes=None,
-                                 a_scales=None, stream=None):
+                                 a_scales=None, stream=None, hadamard_block: int = 32):
     """Down-projection input of the grouped experts: h = bf16(SiLU(g) * u) of the
     gate|up GEMM output GU [rows, 2F] (sorted rows), transformed into the
     expert-padded MXFP4 layout (see the header)."""
@@ -471,8 +485,8 @@ def macaq_quant_act_grouped_silu(GU, expert_offsets, inv_s, rows: int, E: int, a
         a_codes = torch.empty(P, F // 2, dtype=torch.uint8, device=GU.device)
     if a_scales is None:
         a_scales = torch.empty(macaq_scale_bytes(P, F), dtype=torch.uint8, device=GU.device)
-    _check("macaq_quant_act_grouped_silu", lib().macaq_quant_act_grouped_silu(
-        _ptr(GU), _ld(GU), _ptr(expert_offsets), _ptr(inv_s), rows, E, F,
+    _check("macaq_quant_act_grouped_silu_hb", lib().macaq_quant_act_grouped_silu_hb(
+        _ptr(GU), _ld(GU), _ptr(expert_offsets), _ptr(inv_s), rows, E, F, hadamard_block,
         _ptr(a_codes), _ptr(a_scales), _stream(stream)))
     return a_codes, a_scales
 

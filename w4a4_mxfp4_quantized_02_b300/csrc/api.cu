@@ -180,6 +180,30 @@ macaq_status macaq_quant_weight_grouped(const void *W, const float *s, int64_t E
     return from_cuda(launch_quant(QuantMode::WeightGrouped, a, static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_quant_weight_grouped_hb(const void *W, const float *s, int64_t E, int64_t N, int64_t K,
+                                           int64_t hadamard_block, uint8_t *w_codes, uint8_t *w_scales,
+                                           macaq_stream_t stream)
+{
+    if (hadamard_block == 32) return macaq_quant_weight_grouped(W, s, E, N, K, w_codes, w_scales, stream);
+    if (hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_k(K));
+    if (K % 64 != 0) return MACAQ_ERR_INVALID_ARG;
+    MACAQ_TRY(check_rows(N));
+    if (E < 0) return MACAQ_ERR_INVALID_ARG;
+    if (E == 0 || N == 0) return MACAQ_OK;
+    if (E * pad_rows(N) > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (!W || !s || !w_codes || !w_scales) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(s) || !aligned16(w_codes) || !aligned16(w_scales)) return MACAQ_ERR_ALIGNMENT;
+    // expert by expert through the dense transform (offline preparation)
+    const size_t sbytes = tiled_scale_bytes(N, K);
+    for (int64_t e = 0; e < E; ++e) {
+        const uint16_t *We = static_cast<const uint16_t *>(W) + e * N * K;
+        MACAQ_TRY(macaq_quant_weight_hb(We, s + e * K, N, K, 64, w_codes + e * N * (K / 2), w_scales + e * sbytes,
+                                        stream));
+    }
+    return MACAQ_OK;
+}
+
 macaq_status macaq_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                              const uint8_t *w_codes, const uint8_t *w_scales, int64_t M, int64_t N,
                              int64_t K, void *Y, int64_t ldy, macaq_stream_t stream)
@@ -419,12 +443,14 @@ macaq_status macaq_flip_refine(const float *Wt, const float *H, int64_t N, int64
     return macaq_flip_sweeps(H, N, K, sweeps, w_codes, w_scales, flips, workspace, ws_bytes, stream);
 }
 
-macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *row_src,
-                                     const int32_t *expert_offsets, const float *inv_s,
-                                     int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
-                                     uint8_t *a_scales, macaq_stream_t stream)
+macaq_status macaq_quant_act_grouped_hb(const void *X, int64_t ldx, const int32_t *row_src,
+                                        const int32_t *expert_offsets, const float *inv_s, int64_t rows,
+                                        int64_t E, int64_t K, int64_t hadamard_block, uint8_t *a_codes,
+                                        uint8_t *a_scales, macaq_stream_t stream)
 {
+    if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
     MACAQ_TRY(check_k(K));
+    if (K % hadamard_block != 0) return MACAQ_ERR_INVALID_ARG;
     MACAQ_TRY(check_rows(rows));
     if (E <= 0) return MACAQ_ERR_INVALID_ARG;
     if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
@@ -446,14 +472,27 @@ macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *
     a.E = static_cast<int32_t>(E);
     a.codes = a_codes;
     a.scales = a_scales;
+    a.had = static_cast<int32_t>(hadamard_block);
     return from_cuda(launch_quant(QuantMode::ActGrouped, a, static_cast<cudaStream_t>(stream)));
 }
 
-macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
-                                          const float *inv_s, int64_t rows, int64_t E, int64_t F,
-                                          uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
+macaq_status macaq_quant_act_grouped(const void *X, int64_t ldx, const int32_t *row_src,
+                                     const int32_t *expert_offsets, const float *inv_s,
+                                     int64_t rows, int64_t E, int64_t K, uint8_t *a_codes,
+                                     uint8_t *a_scales, macaq_stream_t stream)
 {
+    return macaq_quant_act_grouped_hb(X, ldx, row_src, expert_offsets, inv_s, rows, E, K, 32, a_codes, a_scales,
+                                      stream);
+}
+
+macaq_status macaq_quant_act_grouped_silu_hb(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
+                                             const float *inv_s, int64_t rows, int64_t E, int64_t F,
+                                             int64_t hadamard_block, uint8_t *a_codes, uint8_t *a_scales,
+                                             macaq_stream_t stream)
+{
+    if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
     MACAQ_TRY(check_k(F));
+    if (F % hadamard_block != 0) return MACAQ_ERR_INVALID_ARG;
     MACAQ_TRY(check_rows(rows));
     if (E <= 0) return MACAQ_ERR_INVALID_ARG;
     if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
@@ -475,7 +514,16 @@ macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const in
     a.E = static_cast<int32_t>(E);
     a.codes = a_codes;
     a.scales = a_scales;
+    a.had = static_cast<int32_t>(hadamard_block);
     return from_cuda(launch_quant(QuantMode::ActGroupedSilu, a, static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_quant_act_grouped_silu(const void *GU, int64_t ldgu, const int32_t *expert_offsets,
+                                          const float *inv_s, int64_t rows, int64_t E, int64_t F,
+                                          uint8_t *a_codes, uint8_t *a_scales, macaq_stream_t stream)
+{
+    return macaq_quant_act_grouped_silu_hb(GU, ldgu, expert_offsets, inv_s, rows, E, F, 32, a_codes, a_scales,
+                                           stream);
 }
 
 macaq_status macaq_quant_act_silu(const void *GU, int64_t ldgu, const float *inv_s, int64_t M, int64_t F,

@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 // stage lands the gate and the up slab of every row and the consumer forms
 // h = SiLU(g) * u before the transform.
 
-template <int STAGES, bool kSilu>
+template <int STAGES, bool kSilu, bool kH64>
 __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
                                                                     int32_t RT, int32_t per_cta)
@@ -999,7 +999,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
                 }
             }
             uint4 codes;
-            sbyte = quant_block_pairs<false>(raw, f, codes);
+            sbyte = quant_block_pairs<kH64>(raw, f, codes);
             *reinterpret_cast<uint4 *>(a.codes + p * half_k + 16 * kb) = codes;
         }
         uint32_t word = sbyte << (8 * (lane & 3));
@@ -1299,11 +1299,22 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaSuccess;
-    auto kern = silu ? (stages == 6 ? quant_grouped_tma_kernel<6, true>
-                                    : stages == 4 ? quant_grouped_tma_kernel<4, true> : quant_grouped_tma_kernel<3, true>)
-                     : (stages == 6 ? quant_grouped_tma_kernel<6, false>
-                                    : stages == 4 ? quant_grouped_tma_kernel<4, false> : quant_grouped_tma_kernel<3, false>);
-    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : stages == 4 ? 1 : 2) + (silu ? 3 : 0) + 2, smem));
+    void (*kern)(CUtensorMap, QuantArgs, int32_t, int32_t, int32_t, int32_t);
+    if (a.had == 64)
+        kern = silu ? (stages == 6 ? quant_grouped_tma_kernel<6, true, true>
+                                   : stages == 4 ? quant_grouped_tma_kernel<4, true, true>
+                                                 : quant_grouped_tma_kernel<3, true, true>)
+                    : (stages == 6 ? quant_grouped_tma_kernel<6, false, true>
+                                   : stages == 4 ? quant_grouped_tma_kernel<4, false, true>
+                                                 : quant_grouped_tma_kernel<3, false, true>);
+    else
+        kern = silu ? (stages == 6 ? quant_grouped_tma_kernel<6, true, false>
+                                   : stages == 4 ? quant_grouped_tma_kernel<4, true, false>
+                                                 : quant_grouped_tma_kernel<3, true, false>)
+                    : (stages == 6 ? quant_grouped_tma_kernel<6, false, false>
+                                   : stages == 4 ? quant_grouped_tma_kernel<4, false, false>
+                                                 : quant_grouped_tma_kernel<3, false, false>);
+    MACAQ_TRY_CUDA(open_smem(kern, (stages == 6 ? 0 : stages == 4 ? 1 : 2) + (silu ? 3 : 0) + (a.had == 64 ? 22 : 2), smem));
     dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(ctas_y));
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
