@@ -80,6 +80,7 @@ struct Params {
     int32_t n_rb;            // 128-row scale blocks of one weight
     int32_t num_full;        // whole 256-column tiles run first ...
     int32_t num_split;       // ... then the last num_split tiles as two 128-column halves
+    int32_t n_fastest;       // tile order: column blocks fastest (else row-pair blocks)
 };
 
 struct Tile {
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_cp_pair_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r, db + (r * L::KATOMS + at) * kAtom);
         }
     };
-    // Tiles t run over (pair m-block t % num_mp (m fastest), n-block t / num_mp).
+    // Tiles t run over (pair m-block t % num_mp (m fastest), n-block t / num_mp),
+    // or with n_fastest over (pair m-block t / num_nb, n-block t % num_nb).
     // Units 0 .. num_full-1 are whole tiles; when the tiles do not fill the
     // last round of pairs, the remaining num_split tiles run as two units of
     // 128 columns each, so the last round takes about half as long.
@@ -310,8 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             t = num_full + (u - num_full) / 2;
             half = static_cast<int32_t>((u - num_full) & 1);
         }
-        const int32_t mp = static_cast<int32_t>(t % num_mp);
-        const int32_t nb = static_cast<int32_t>(t / num_mp);
+        const int32_t mp = static_cast<int32_t>(p.n_fastest ? t / p.num_nb : t % num_mp);
+        const int32_t nb = static_cast<int32_t>(p.n_fastest ? t % p.num_nb : t / num_mp);
         ti.n0 = nb * BN + (half > 0 ? BN / 2 : 0);
         ti.ncols = half < 0 ? BN : BN / 2;
         if (!GROUPED) {
@@ -801,6 +803,11 @@ cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
     p.num_kstages = static_cast<int32_t>((g.K + 2 * KB - 1) / (2 * KB));
     p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
+    // column blocks fastest when A would not stay in L2 across a pass over
+    // the column blocks: grouped A (each expert's rows then meet all of its
+    // weight tiles in a row, so an expert's weight tile is read once for both
+    // of its pair tiles), and dense A of more than half of L2
+    p.n_fastest = (GROUPED || static_cast<uint64_t>(g.a_rows) * kb > (64ull << 20)) ? 1 : 0;
 
     const int64_t pairs_max = sms / 2;
     int64_t units;
