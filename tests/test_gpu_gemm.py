@@ -68,11 +68,12 @@ def test_gemm_random_scales(M, N, K, seed):
 
 @pytest.mark.parametrize("M,N,K,seed", [(8, 136, 32, 5), (17, 1000, 768, 6), (40, 296, 4096, 7),
                                         (64, 5120, 5120, 8), (1, 520, 9216, 9), (33, 2048, 1280, 10),
-                                        (16, 19200, 2048, 11), (5, 25600, 1024, 12)])
+                                        (16, 19200, 2048, 11), (5, 25600, 1024, 12),
+                                        (2, 2056, 5120, 13), (3, 200, 160, 14), (4, 4096, 25600, 15),
+                                        (1, 25600, 5120, 16)])
 def test_gemm_few_rows(M, N, K, seed):
     """Up to 64 rows: weight rows on the MMA's M side, K split over a cluster of
-    CTAs when there are few weight tiles, or when splitting evens out the
-    weight bytes per SM (more tiles than SMs); partials added in rank order."""
+    CTAs when there are few weight tiles (partials added in rank order)."""
     ca, sa, cw, sw = _rand_operands(M, N, K, seed, 110, 140)
     Y = _gpu_gemm(ca, sa, cw, sw, M, N, K)
     Y2 = _gpu_gemm(ca, sa, cw, sw, M, N, K)
