@@ -652,16 +652,6 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
-    for (int idx = t; idx < TB * 8; idx += blockDim.x) {
-        const int bx = idx >> 3, c = idx & 7;
-        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (slab0 + bx < a.K / 32) v4 = __ldg(reinterpret_cast<const float4 *>(a.f + 32 * (slab0 + bx)) + c);
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ftab + 128 * bx + 16 * ((c + bx) & 7)),
-                     "f"(v4.x), "f"(v4.y), "f"(v4.z), "f"(v4.w)
-                     : "memory");
-    }
-    __syncthreads();
-
     const int32_t my_groups = blockIdx.y < static_cast<uint32_t>(groups)
                                   ? (groups - 1 - static_cast<int32_t>(blockIdx.y)) / static_cast<int32_t>(gridDim.y) + 1
                                   : 0;
@@ -693,6 +683,17 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
     }
 
     // ---------------------------------------------------- consumer warps
+    // The consumers fill the balance-factor table while the producer's first
+    // copies are in flight, and sync among themselves on a named barrier.
+    for (int idx = t; idx < TB * 8; idx += NC) {
+        const int bx = idx >> 3, c = idx & 7;
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (slab0 + bx < a.K / 32) v4 = __ldg(reinterpret_cast<const float4 *>(a.f + 32 * (slab0 + bx)) + c);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ftab + 128 * bx + 16 * ((c + bx) & 7)),
+                     "f"(v4.x), "f"(v4.y), "f"(v4.z), "f"(v4.w)
+                     : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
     const int tx = t % TB, ty = t / TB;
     const int64_t nkb = a.K / 32;
     const int64_t nka = ((nkb + 7) / 8 * 8) / 4;
