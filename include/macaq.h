@@ -180,10 +180,14 @@ macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s,
  * macaq_linear_workspace_bytes(M, K) exceeds the array is rejected with
  * MACAQ_ERR_WORKSPACE before anything is launched.  Nothing is allocated:
  * the first call on a device looks up the array's device address (make that
- * first call before any stream capture).  All calls on a device share the
- * one array, so calls that can overlap on the GPU (different streams without
- * ordering) race; the array keeps the last call's contents, which no call
- * depends on. */
+ * first call before any stream capture).  The address belongs to the CUDA
+ * context current at the call: each context that loads the library holds its
+ * own copy of the array, and a call made under a different context than the
+ * previous one on that device (after cudaDeviceReset, or under a caller's own
+ * driver-API context) looks the address up again, so that call too belongs
+ * before any stream capture.  All calls in one context share the one array,
+ * so calls that can overlap on the GPU (different streams without ordering)
+ * race; the array keeps the last call's contents, which no call depends on. */
 #define MACAQ_LINEAR_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 macaq_status macaq_linear_no_alloc(const void *X, int64_t ldx, const float *inv_s,
                                    const uint8_t *w_codes, const uint8_t *w_scales, int64_t M,

@@ -35,6 +35,51 @@ def test_exports_every_declared_symbol(L):
         assert n in mq._SIGS, f"binding lacks {n}"
 
 
+def _param_type(p: str) -> str:
+    """The type part of one C parameter declaration (drops the name, if any)."""
+    if "*" in p:
+        return p[: p.rindex("*") + 1].strip()
+    tokens = p.split()
+    return " ".join(tokens[:-1]) if len(tokens) > 1 and tokens[-2] != "const" else p
+
+
+def declared_signatures():
+    """name -> list of parameter type strings, from the header's prototypes."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"#define[^\n]*", "", text)
+    sigs = {}
+    for m in re.finditer(r"\b(macaq_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        sigs[m.group(1)] = [_param_type(p) for p in params]
+    return sigs
+
+
+def _ctype_of(decl: str):
+    decl = decl.replace("const ", "").strip()
+    if "*" in decl or decl == "macaq_stream_t":
+        return ctypes.c_void_p
+    return {"int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "int32_t": ctypes.c_int32,
+            "int": ctypes.c_int32, "float": ctypes.c_float, "uint64_t": ctypes.c_uint64,
+            "macaq_status": ctypes.c_int32}[decl]
+
+
+def test_binding_signatures_match_header(L):
+    """Every binding passes the header's parameter count and types (incl. the no-alloc entry)."""
+    sigs = declared_signatures()
+    assert "macaq_linear_no_alloc" in sigs and "macaq_linear" in sigs
+    for name, params in sigs.items():
+        args, _ = mq._SIGS[name]
+        assert len(args) == len(params), f"{name}: header {len(params)} params, binding {len(args)}"
+        for i, (decl, a) in enumerate(zip(params, args)):
+            want = _ctype_of(decl)
+            assert ctypes.sizeof(want) == ctypes.sizeof(a) and (want is ctypes.c_void_p) == (a is ctypes.c_void_p) \
+                and (want is ctypes.c_float) == (a is ctypes.c_float), f"{name} arg {i}: {decl} vs {a}"
+    # the no-alloc entry point is macaq_linear without the workspace pair
+    full, noalloc = sigs["macaq_linear"], sigs["macaq_linear_no_alloc"]
+    assert noalloc == full[:10] + full[12:]
+
+
 def test_sizes(L):
     assert mq.macaq_scale_bytes(16, 128) == 128 * 8
     assert mq.macaq_scale_bytes(129, 256) == 256 * 8

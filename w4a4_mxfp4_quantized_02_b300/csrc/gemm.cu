@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             // (rank 0's) stage is full once both CTAs' copies have landed
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);  // one MMA commit, multicast to both CTAs
+            mbar_init(empty_bar(s), 1);  // one MMA commit, arriving in both CTAs
             mbar_init(ready_bar(s), 1);
         }
         mbar_init(acc_full, 1);
@@ -961,8 +961,7 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     if (g.E == 0 && g.M <= 16) return launch_skinny<16, 5>(g, stream, 4);
     if (g.E == 0 && g.M <= 32) return launch_skinny<32, 5>(g, stream, 5);
     if (g.E == 0 && g.M <= 64) return launch_skinny<64, 4>(g, stream, 6);
-    // grouped: per-expert B tiles, one CTA per tile; dense: CTA pairs share
-    // (multicast) the B tile of adjacent m-blocks
+    // everything else: CTA pairs on 256 x 256 tiles (grouped: per-expert B)
     if (g.E > 0) return launch_pair<6, true>(g, stream, 7);
     return launch_pair<6, false>(g, stream, 3);
 }

@@ -282,38 +282,6 @@ __device__ __forceinline__ void cluster_sync()
                      : "memory");
 }
 
-// TMA 2D load multicast to the CTAs in `mask`: data and the complete_tx
-// signal land at the same CTA-relative offsets in every destination CTA.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(map), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void *src, uint32_t bytes,
-                                             uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar), "h"(mask)
-        : "memory");
-}
-
-// tcgen05.commit arriving on `bar` at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
-
 // ------------------------------------------------- CTA pairs (cta_group::2)
 //
 // A pair of CTAs (cluster ranks 0 and 1) shares one tensor-core operation:

@@ -7,6 +7,7 @@
 // device memory at start-up and forbids cudaMalloc afterwards.  For them the
 // library keeps one scratch array of fixed size in its own module image, so
 // the call needs nothing beyond the caller's inputs and outputs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -21,11 +22,36 @@ namespace {
 // Every GPU that loads the library holds this array until the process exits.
 static __device__ __align__(256) uint8_t g_linear_scratch[MACAQ_LINEAR_STATIC_SCRATCH_BYTES];
 
-// Device address of g_linear_scratch per device.  The array's name in host
-// code is only a host-side handle; the address comes from the runtime, once
-// per device, with that device current.
-void *g_scratch_addr[64];
+// Device address of g_linear_scratch, looked up once per device with that
+// device current.  The array's name in host code is only a host-side handle;
+// its device address belongs to the CUDA context that loaded the module, so
+// the entry also records that context: when a different context is current on
+// the device (after cudaDeviceReset, or under a caller's own driver-API
+// context) the address is looked up again instead of reusing a stale one.
+struct ScratchEntry {
+    CUcontext ctx = nullptr;
+    void *addr = nullptr;
+};
+ScratchEntry g_scratch[64];
 std::mutex g_scratch_mu;
+
+// cuCtxGetCurrent through the runtime's driver entry-point query (the library
+// does not link the driver library itself).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn ctx_get_current_fn()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
+}
 
 cudaError_t scratch_address(void **out)
 {
@@ -33,14 +59,23 @@ cudaError_t scratch_address(void **out)
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (get_ctx == nullptr) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchEntry &e = g_scratch[dev];
+    if (e.addr == nullptr || ctx == nullptr || e.ctx != ctx) {
+        // with no context current yet, the lookup itself makes the device's
+        // primary context current; the entry records whichever is current
         void *p = nullptr;
         err = cudaGetSymbolAddress(&p, g_linear_scratch);
         if (err != cudaSuccess) return err;
-        g_scratch_addr[dev] = p;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+        e.ctx = ctx;
+        e.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return cudaSuccess;
 }
 
