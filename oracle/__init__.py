@@ -65,8 +65,8 @@ def lib():
             "oracle_tile_scales": [P, I, I, P],
             "oracle_e2m1_encode_many": [P, I, P],
             "oracle_scale_exponent_many": [P, I, P],
-            "oracle_silu_mul": [P, I, I, P],
-            "oracle_exp_many": [P, I, P],
+            "oracle_silu_mul": [P, I, I, P, P],
+            "oracle_f64_to_bf16_many": [P, I, P],
             "oracle_flip_hessian": [P, I, I, ctypes.c_float, P],
             "oracle_moe_combine": [P, I, P, P, I, I, I, P],
             "oracle_flip_refine": [P, P, I, I, ctypes.c_int32, P, P, P],
@@ -252,24 +252,32 @@ def quantize_grouped(Xrows, offsets: np.ndarray, inv_s_e: np.ndarray):
     return codes, scales
 
 
-def exp_f32(x: np.ndarray) -> np.ndarray:
-    """The fp32 e^x the SwiGLU step is stated with (range reduction and a
-    degree-8 Taylor polynomial, see macaq_oracle.c)."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    y = np.empty_like(x)
-    lib().oracle_exp_many(_p(x), x.size, _p(y))
-    return y
-
-
 def silu_mul(GU) -> np.ndarray:
-    """h = bf16(SiLU(g) * u) of a [rows, 2F] bf16 gate|up matrix, as bf16 bits
-    (uint16) [rows, F]."""
+    """h = bf16_rn(SiLU(g) * u), SiLU(g) = g / (1 + e^-g): the exact value of a
+    [rows, 2F] bf16 gate|up matrix rounded once to bf16, as bits (uint16)
+    [rows, F]."""
+    return silu_mul_window(GU)[0]
+
+
+def silu_mul_window(GU) -> tuple[np.ndarray, np.ndarray]:
+    """(h, h_alt): h as ``silu_mul``; h_alt the other bf16 neighbour where the
+    exact value lies within 2^-20 (relative) of a rounding boundary -- where an
+    fp32 evaluation may round either way -- and h elsewhere."""
     bits = np.ascontiguousarray(bf16_bits(GU))
     rows, two_f = bits.shape
     F = two_f // 2
     h = np.empty((rows, F), dtype=np.uint16)
-    lib().oracle_silu_mul(_p(bits), rows, F, _p(h))
-    return h
+    alt = np.empty((rows, F), dtype=np.uint16)
+    lib().oracle_silu_mul(_p(bits), rows, F, _p(h), _p(alt))
+    return h, alt
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp64 -> bf16 bits, rounded once to nearest even (the oracle's route)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_f64_to_bf16_many(_p(x), x.size, _p(out))
+    return out
 
 
 def f32_to_bf16_bits(y: np.ndarray) -> np.ndarray:

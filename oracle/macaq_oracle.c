@@ -32,13 +32,15 @@
  *   GEMM reference   Y = deq(A) . deq(W)^T accumulated in fp64.
  *
  *   SwiGLU input     (extension: the down projection of a gated MLP reads
- *                    h = SiLU(g) * u of the gate and up outputs g, u.)  Stated
- *                    in fp32: e^x by range reduction x = n ln2 + r and a
- *                    degree-8 Taylor polynomial in r (both as fused
- *                    multiply-adds), SiLU(g) = g / (1 + e^-g),
- *                    h rounded once to bf16 (the value an unfused layer would
- *                    store).  The CUDA path evaluates the same operations in
- *                    the same order; both are pinned against fp64 exp.
+ *                    h = SiLU(g) * u of the gate and up outputs g, u.)  Its
+ *                    definition: the real value g * u / (1 + e^-g), rounded
+ *                    once to bf16 (the value an unfused layer would store).
+ *                    Evaluated here in fp64 with the C library's exp, then
+ *                    rounded to bf16 directly (no intermediate fp32).  Next to
+ *                    each result the oracle reports the other bf16 neighbour
+ *                    wherever the exact value lies within 2^-20 (relative) of a
+ *                    rounding boundary: an fp32 evaluation, whose error is below
+ *                    2^-21 relative, may land on either side there.
  *
  *   MoE combine      (extension: the expert outputs of a token's top-k rows,
  *                    weighted by their routing probabilities, summed into the
@@ -445,39 +447,7 @@ void oracle_scale_exponent_many(const float *amax, int64_t n, int32_t *se)
 
 /* ------------------------------------------------------------------ SwiGLU */
 
-/* e^x in fp32 (round to nearest at every step, no contraction):
- *   n = nearest integer to x * log2(e),
- *   r = (x - n * ln2_hi) - n * ln2_lo      with ln2_hi + ln2_lo = ln 2 and
- *                                          ln2_hi short enough that n * ln2_hi
- *                                          is exact for |n| < 256,
- *   e^r by Horner on the Taylor series to r^8 / 8!  (|r| <= 0.35: the
- *   truncation is below 2^-30 relative),
- *   e^x = e^r * 2^n, scaled in two steps where 2^n is not a normal float.
- * Overflow past ln(FLT_MAX) gives +inf, underflow below the smallest
- * subnormal gives +0. */
-float oracle_exp_f32(float x)
-{
-    if (x > 88.72283935546875f) return INFINITY;
-    if (x < -103.972084045410156f) return 0.0f;
-    const float t = x * 0x1.715476p+0f;               /* log2(e) */
-    const float fn = rintf(t);
-    const int n = (int)fn;
-    float r = fmaf(-fn, 0x1.62e4p-1f, x);             /* ln2_hi = 0.693145751953125 */
-    r = fmaf(-fn, 0x1.7f7d1cp-20f, r);                /* ln2_lo */
-    float p = 0x1.a01a02p-16f;                        /* 1/8! */
-    p = fmaf(p, r, 0x1.a01a02p-13f);                  /* 1/7! */
-    p = fmaf(p, r, 0x1.6c16c2p-10f);                  /* 1/6! */
-    p = fmaf(p, r, 0x1.111112p-7f);                   /* 1/5! */
-    p = fmaf(p, r, 0x1.555556p-5f);                   /* 1/4! */
-    p = fmaf(p, r, 0x1.555556p-3f);                   /* 1/3! */
-    p = fmaf(p, r, 0x1.0p-1f);                        /* 1/2! */
-    p = fmaf(p, r, 0x1.0p+0f);                        /* 1/1! */
-    p = fmaf(p, r, 0x1.0p+0f);                        /* 1/0! */
-    if (n > 127) return (p * 0x1.0p+127f) * ldexpf(1.0f, n - 127);
-    if (n < -126) return (p * ldexpf(1.0f, n + 100)) * 0x1.0p-100f;
-    return p * ldexpf(1.0f, n);
-}
-
+/* fp32 -> bf16 bits, round to nearest even (finite inputs). */
 static uint16_t f32_to_bf16_rne(float f)
 {
     const uint32_t u = f32_bits(f);
@@ -485,28 +455,70 @@ static uint16_t f32_to_bf16_rne(float f)
     return (uint16_t)((u + 0x7fffu + lsb) >> 16);
 }
 
-/* h = bf16( SiLU(g) * u ) with SiLU(g) = g / (1 + e^-g), all in fp32. */
-uint16_t oracle_silu_mul_bf16(uint16_t g_bits, uint16_t u_bits)
+/* Round a finite double to the nearest bf16 (ties to even), directly: the
+ * quantum is 2^(e - 8) for |v| in [2^(e-1), 2^e) (8 significant bits), and
+ * 2^-133 below the smallest normal 2^-126 (bf16 subnormals); rint() rounds to
+ * nearest even in the default rounding mode and the division by the quantum
+ * is exact.  Results above the largest bf16 become infinities. */
+static uint16_t f64_to_bf16_rne(double v)
 {
-    const float g = bf16_bits_to_f32(g_bits);
-    const float u = bf16_bits_to_f32(u_bits);
-    const float e = oracle_exp_f32(-g);
-    const float s = g / (1.0f + e);
-    return f32_to_bf16_rne(s * u);
+    if (v == 0.0) return signbit(v) ? 0x8000u : 0x0000u;
+    int e;
+    (void)frexp(v, &e);
+    const int qexp = (e - 8 > -133) ? e - 8 : -133;
+    const double r = ldexp(rint(ldexp(v, -qexp)), qexp);
+    const float f = (float)r;   /* exact: r has at most 8 significant bits */
+    uint32_t u = f32_bits(f);
+    if (isinf(f) || fabs(r) > 0x1.fep+127) u = signbit(v) ? 0xff800000u : 0x7f800000u;
+    if (r == 0.0) u = signbit(v) ? 0x80000000u : 0u;
+    return (uint16_t)(u >> 16);
 }
 
-/* gu: [rows, 2F] bf16 (gate in columns 0..F-1, up in F..2F-1) -> h [rows, F]. */
-void oracle_silu_mul(const uint16_t *gu, int64_t rows, int64_t F, uint16_t *h)
+/* The exact value of SiLU(g) * u = g * u / (1 + e^-g), in fp64. */
+static double silu_mul_f64(double g, double u)
+{
+    const double e = exp(-g);               /* +inf for very negative g: -> -0 */
+    return g / (1.0 + e) * u;
+}
+
+/* Half-width of the window (relative, plus an absolute floor far below any
+ * bf16 normal) around a rounding boundary inside which an fp32 evaluation
+ * may round either way. */
+#define SILU_WINDOW_REL 0x1.0p-20
+#define SILU_WINDOW_ABS 0x1.0p-140
+
+/* h = bf16_rn( SiLU(g) * u ) of one element; *alt = the other bf16
+ * neighbour when the exact value lies within the window of a rounding
+ * boundary, else h. */
+static uint16_t silu_mul_bf16(uint16_t g_bits, uint16_t u_bits, uint16_t *alt)
+{
+    const double g = (double)bf16_bits_to_f32(g_bits);
+    const double u = (double)bf16_bits_to_f32(u_bits);
+    const double v = silu_mul_f64(g, u);
+    const uint16_t h = f64_to_bf16_rne(v);
+    const double w = SILU_WINDOW_REL * fabs(v) + SILU_WINDOW_ABS;
+    const uint16_t lo = f64_to_bf16_rne(v - w), hi = f64_to_bf16_rne(v + w);
+    *alt = (lo != h) ? lo : hi;
+    return h;
+}
+
+/* gu: [rows, 2F] bf16 (gate in columns 0..F-1, up in F..2F-1) -> h [rows, F]
+ * and, if h_alt is not NULL, the other admissible neighbour [rows, F]. */
+void oracle_silu_mul(const uint16_t *gu, int64_t rows, int64_t F, uint16_t *h, uint16_t *h_alt)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r)
-        for (int64_t j = 0; j < F; ++j)
-            h[r * F + j] = oracle_silu_mul_bf16(gu[r * 2 * F + j], gu[r * 2 * F + F + j]);
+        for (int64_t j = 0; j < F; ++j) {
+            uint16_t alt;
+            h[r * F + j] = silu_mul_bf16(gu[r * 2 * F + j], gu[r * 2 * F + F + j], &alt);
+            if (h_alt) h_alt[r * F + j] = alt;
+        }
 }
 
-void oracle_exp_many(const float *x, int64_t n, float *y)
+/* The fp64 -> bf16 rounding on its own (for the pins). */
+void oracle_f64_to_bf16_many(const double *x, int64_t n, uint16_t *out)
 {
-    for (int64_t i = 0; i < n; ++i) y[i] = oracle_exp_f32(x[i]);
+    for (int64_t i = 0; i < n; ++i) out[i] = f64_to_bf16_rne(x[i]);
 }
 
 /* ------------------------------------------------------ Flip Refinement */

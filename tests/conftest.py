@@ -17,3 +17,16 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the session's parity counts (GEMM tolerance, SwiGLU blocks)."""
+    try:
+        from helpers import parity_lines
+    except ImportError:
+        return
+    lines = parity_lines()
+    if lines:
+        terminalreporter.write_sep("-", "parity counts per test")
+        for line in lines:
+            terminalreporter.write_line(line)

@@ -51,3 +51,59 @@ def to_dev(t: torch.Tensor) -> torch.Tensor:
 
 def u8(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy().astype(np.uint8)
+
+
+def check_silu_blocks(codes: np.ndarray, scales: np.ndarray, GU, f: np.ndarray, hb: int = 32,
+                      max_window_frac: float = 0.05):
+    """Check the GPU's MXFP4 of h = bf16_rn(SiLU(g) * u) (fused SwiGLU transform)
+    against the oracle, whose h is the exact value rounded once to bf16.
+
+    The GPU forms h in fp32 (error below 2^-21 relative), so where the exact
+    value lies within 2^-20 of a bf16 rounding boundary either neighbour is
+    admissible (the oracle reports both).  Per Hadamard block of hb channels
+    of a row: codes and scales must equal the oracle's bit for bit when no
+    element of the block is in that window; otherwise they must equal the
+    oracle's for one admissible choice of the windowed elements.
+
+    codes [rows, F/2], scales row-major [rows, F/32] (the GPU's); GU bf16
+    [rows, 2F] (gate | up); f fp32 [F] balance factors.  Returns (ca, sa): the
+    admissible oracle codes and scales the GPU matched, for downstream checks.
+    """
+    from helpers import record_parity
+
+    H, H_alt = oracle.silu_mul_window(GU)
+    rows, F = H.shape
+    ca, sa = oracle.quantize(H, f, hb)
+    ca, sa = ca.copy(), sa.copy()
+    codes = np.asarray(codes, np.uint8).reshape(rows, F // 2)
+    scales = np.asarray(scales, np.uint8).reshape(rows, F // 32)
+    nb = F // hb
+    same = ((codes == ca).reshape(rows, nb, hb // 2).all(-1)
+            & (scales == sa).reshape(rows, nb, hb // 32).all(-1))
+    windowed = (H != H_alt).reshape(rows, nb, hb).any(-1)
+    stray = ~same & ~windowed
+    if stray.any():
+        r, b = np.argwhere(stray)[0]
+        raise AssertionError(f"{int(stray.sum())} blocks differ with no element near a bf16 boundary "
+                             f"(first: row {r}, channels {b * hb}..{b * hb + hb - 1})")
+    f = np.asarray(f, np.float32)
+    for r, b in np.argwhere(~same):
+        c0 = b * hb
+        ks = np.flatnonzero(H[r, c0:c0 + hb] != H_alt[r, c0:c0 + hb])
+        assert 0 < len(ks) <= 12, f"row {r} block {b}: {len(ks)} windowed elements"
+        cand = np.repeat(H[r:r + 1, c0:c0 + hb], (1 << len(ks)) - 1, axis=0)
+        for m in range(1, 1 << len(ks)):
+            for i, k in enumerate(ks):
+                if m >> i & 1:
+                    cand[m - 1, k] = H_alt[r, c0 + k]
+        cc, cs = oracle.quantize(np.ascontiguousarray(cand), np.ascontiguousarray(f[c0:c0 + hb]), hb)
+        hit = np.flatnonzero((cc == codes[r, c0 // 2:(c0 + hb) // 2]).all(1)
+                             & (cs == scales[r, c0 // 32:(c0 + hb) // 32]).all(1))
+        assert hit.size, f"row {r}, channels {c0}..{c0 + hb - 1}: no admissible rounding gives the GPU's codes"
+        ca[r, c0 // 2:(c0 + hb) // 2] = cc[hit[0]]
+        sa[r, c0 // 32:(c0 + hb) // 32] = cs[hit[0]]
+    frac = float(windowed.mean()) if windowed.size else 0.0
+    record_parity("silu", blocks=int(same.size), windowed=int(windowed.sum()),
+                  differ=int((~same).sum()), window_frac=frac)
+    assert frac <= max_window_frac, f"{frac:.3%} of blocks have an element near a boundary"
+    return ca, sa

@@ -9,8 +9,39 @@ doubled) and are counted separately.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
+
+# Parity counts of the session, summed per (kind, test): GEMM tolerance
+# counts and SwiGLU block counts; conftest prints them in pytest's terminal
+# summary.
+PARITY_LOG: dict = {}
+
+
+def record_parity(kind: str, **stats) -> None:
+    """Add one check's counts: integers are summed, "strict" keeps the minimum,
+    other floats the maximum."""
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0].split("::", 1)[-1]
+    agg = PARITY_LOG.setdefault((kind, test), {})
+    for k, v in stats.items():
+        if k not in agg:
+            agg[k] = v
+        elif isinstance(v, int):
+            agg[k] += v
+        elif k == "strict":
+            agg[k] = min(agg[k], v)
+        else:
+            agg[k] = max(agg[k], v)
+
+
+def parity_lines() -> list[str]:
+    out = []
+    for (kind, test), agg in PARITY_LOG.items():
+        body = " ".join(f"{k}={v:.6g}" if isinstance(v, float) else f"{k}={v}" for k, v in agg.items())
+        out.append(f"{kind} {test}: {body}")
+    return out
 
 
 def untile_scales(tiled: np.ndarray, rows: int, K: int) -> np.ndarray:
@@ -47,16 +78,25 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def check_gemm(Y: np.ndarray, Yref: np.ndarray, absref: np.ndarray, K: int, ulps: float = 2.0):
-    """Assert the GEMM criterion; return (fraction strict, number of cancellation cases)."""
+    """Assert the GEMM criterion; return (fraction strict, number of cancellation cases).
+
+    Every call is also logged: outputs checked, the non-strict (cancellation)
+    count, and for those the worst error in units of the strict tolerance and
+    as a fraction of the accumulation bound."""
     Y = np.asarray(Y, np.float64)
     err = np.abs(Y - Yref)
     tol = ulps * bf16_ulp(Yref)
+    bound = tol + K * 2.0 ** -23 * absref
     strict = err <= tol
-    loose = err <= tol + K * 2.0 ** -23 * absref
+    loose = err <= bound
     bad = ~(strict | loose)
+    ns = ~strict
+    record_parity("gemm", n=int(err.size), strict=float(strict.mean()), nonstrict=int(ns.sum()),
+                  worst_over_2ulp=float((err[ns] / tol[ns]).max()) if ns.any() else 0.0,
+                  worst_of_bound=float((err / bound).max()) if err.size else 0.0)
     if bad.any():
         idx = np.argwhere(bad)[:10]
         msg = "; ".join(f"{tuple(i)}: got {Y[tuple(i)]:.6g} want {Yref[tuple(i)]:.6g} "
                         f"(sum|ab| {absref[tuple(i)]:.3g})" for i in idx)
         raise AssertionError(f"{bad.sum()} of {bad.size} GEMM outputs out of tolerance: {msg}")
-    return float(strict.mean()), int((~strict).sum())
+    return float(strict.mean()), int(ns.sum())

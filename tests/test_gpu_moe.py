@@ -14,7 +14,7 @@ import torch
 import oracle
 import workloads
 import w4a4_mxfp4_quantized_02_b300 as mq
-from gpu_common import DEV, require_gpu, to_dev, u8
+from gpu_common import DEV, check_silu_blocks, require_gpu, to_dev, u8
 from helpers import bf16_to_np, check_gemm, untile_scales
 
 pytestmark = pytest.mark.gpu
@@ -179,8 +179,10 @@ def test_uneven_and_empty_experts(counts):
 @pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 7, 64, 127))])
 def test_down_fused_swiglu(name, experts):
     """Down-projection input formed from the gate+up GEMM's own output:
-    h = bf16(SiLU(g) * u) fused with the grouped transform (bit-exact against
-    the oracle's SwiGLU step and transform), then the down GEMM."""
+    h = bf16(SiLU(g) * u) fused with the grouped transform, against the
+    oracle's exact-then-rounded h and transform (bit-exact on every block with
+    no h value next to a bf16 rounding boundary, an admissible rounding on the
+    others), then the down GEMM."""
     d = moe(name)
     wl = d["workload"]
     E, F, Kh = wl.E, wl.F, wl.K
@@ -198,7 +200,7 @@ def test_down_fused_swiglu(name, experts):
                                                         rows_n, E)
     Y = mq.macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, offs, rows_n, E, Kh, F)
     torch.cuda.synchronize()
-    H = oracle.silu_mul(gu["Y"].cpu())                 # bf16 bits [rows, F]
+    GU = gu["Y"].cpu()                                  # bf16 gate|up [rows, 2F]
     pos = padded_positions(off)
     P = a_codes.shape[0]
     sc = untile_scales(u8(a_scales), P, F)
@@ -208,9 +210,7 @@ def test_down_fused_swiglu(name, experts):
         lo, hi = off[e], off[e + 1]
         if hi == lo:
             continue
-        ca, sa = oracle.quantize(H[lo:hi], inv_np[e])
-        np.testing.assert_array_equal(u8(a_codes)[pos[lo:hi]], ca)
-        np.testing.assert_array_equal(sc[pos[lo:hi]], sa)
+        ca, sa = check_silu_blocks(u8(a_codes)[pos[lo:hi]], sc[pos[lo:hi]], GU[lo:hi], inv_np[e])
         cw, sw = oracle.quantize(d["W_down"][e], s_np[e])
         da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
         check_gemm(bf16_to_np(Y[lo:hi]), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), F)
@@ -264,7 +264,8 @@ def test_combine_any_choice_count(T, topk, N):
 def test_moe_hadamard_block_64(name, experts):
     """The 64-channel Hadamard block through the routed layer: grouped weight
     preparation, grouped token transform, the SwiGLU-fused down input, all
-    bit-exact against the oracle's 64-block transform; GEMMs unchanged."""
+    bit-exact against the oracle's 64-block transform (the SwiGLU input with
+    the admissible-rounding rule of test_down_fused_swiglu); GEMMs unchanged."""
     d = moe(name)
     wl = d["workload"]
     E, K, F = wl.E, wl.K, wl.F
@@ -296,12 +297,10 @@ def test_moe_hadamard_block_64(name, experts):
                                                         torch.from_numpy(inv_dn).to(DEV), rows_n, E,
                                                         hadamard_block=64)
     torch.cuda.synchronize()
-    H = oracle.silu_mul(gpu["Y"].cpu())
+    GU = gpu["Y"].cpu()
     scd = untile_scales(u8(a_scales), a_codes.shape[0], F)
     for e in (range(E) if experts is None else experts):
         lo, hi = off[e], off[e + 1]
         if hi == lo:
             continue
-        ca, sa = oracle.quantize(H[lo:hi], inv_dn[e], hb=64)
-        np.testing.assert_array_equal(u8(a_codes)[pos[lo:hi]], ca)
-        np.testing.assert_array_equal(scd[pos[lo:hi]], sa)
+        check_silu_blocks(u8(a_codes)[pos[lo:hi]], scd[pos[lo:hi]], GU[lo:hi], inv_dn[e], hb=64)

@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads
 import w4a4_mxfp4_quantized_02_b300 as mq
-from gpu_common import DEV, dense, oracle_weight, require_gpu, sample_rows, to_dev, u8
+from gpu_common import DEV, check_silu_blocks, dense, oracle_weight, require_gpu, sample_rows, to_dev, u8
 from helpers import padding_of_tiled, untile_scales
 
 pytestmark = pytest.mark.gpu
@@ -164,19 +164,18 @@ def test_linear_h64_attn_rows():
 
 
 @pytest.mark.parametrize("M,F,ld_pad", [(1, 32, 0), (37, 768, 16), (300, 2048, 0), (130, 25600, 8)])
-def test_quant_act_silu_dense_bitexact(M, F, ld_pad):
+def test_quant_act_silu_dense(M, F, ld_pad):
     """Dense gated MLP: MXFP4 of h = bf16(SiLU(gate) * up) straight from the
-    [M, 2F] gate|up matrix, bit-exact against the oracle's SwiGLU step and
-    transform; padding rows of the scale tile get zero scales."""
+    [M, 2F] gate|up matrix, against the oracle's exact-then-rounded h and
+    transform (bit-exact on every block with no h value next to a bf16
+    rounding boundary, an admissible rounding on the others); padding rows of
+    the scale tile get zero scales."""
     gate = workloads.make_matrix(M, F, seed=M + F)
     up = workloads.make_matrix(M, F, seed=M + 2 * F, outlier_channels=(1, F // 2, F - 3))
     GU = torch.cat([gate, up, torch.zeros(M, ld_pad, dtype=torch.bfloat16)], 1)
     f = np.random.default_rng(M * F).uniform(0.02, 50.0, F).astype(np.float32)
     codes, scales = mq.macaq_quant_act_silu(to_dev(GU)[:, :2 * F], torch.from_numpy(f).to(DEV))
     torch.cuda.synchronize()
-    H = oracle.silu_mul(GU[:, :2 * F].contiguous())
-    c_ref, s_ref = oracle.quantize(H, f)
-    np.testing.assert_array_equal(u8(codes), c_ref)
     sc = u8(scales)
-    np.testing.assert_array_equal(untile_scales(sc, M, F), s_ref)
+    check_silu_blocks(u8(codes), untile_scales(sc, M, F), GU[:, :2 * F].contiguous(), f)
     assert not untile_scales(sc, (M + 127) // 128 * 128, F)[M:].any()
