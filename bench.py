@@ -4,9 +4,10 @@
 One step = the whole online hot path on one batch: the activation transform
 (balance, 32-channel block Hadamard, MXFP4 encode; one CUDA kernel) followed by
 the block-scaled MXFP4 GEMM (one tcgen05 kernel), i.e. ``macaq_linear`` on the
-prefill attention projection M=4096 tokens, K=5120, N=5120 (``--config`` picks
-another dense workload).  Weights are prepared once, outside the timed region
-(balance from a 512-row calibration batch, fold, quantise).
+prefill MLP down-projection M=8192 tokens, K=25600, N=5120 (the largest
+single-GPU configuration; ``--config`` picks another workload).  Weights are
+prepared once, outside the timed region (balance from a 512-row calibration
+batch, fold, quantise).
 
 Reported (one JSON line on rank 0):
   value          W4A4 linear TFLOP/s (2*M*N*K per step / device time), whole job
@@ -19,6 +20,9 @@ Reported (one JSON line on rank 0):
                  compute (two copy streams, rotating buffer slots); the fully
                  serialised figure is reported beside it
   cpu_baseline   the CPU oracle on a bounded row sample of the same workload
+  per_config     the same device timing (value, GEMM roofline, transform GB/s)
+                 for the prefill attention projection (N=5120 and fused QKV
+                 N=7168), decode M=1/8/16 and the routed MoE layer
 
 Timing: W warm-up steps, then exactly K steps between a barrier and a device
 synchronise, CUDA events on the launching stream around every kernel; inputs
@@ -201,7 +205,8 @@ def reference_arm_moe(args, rank: int, world: int):
     import workloads
     import oracle
 
-    d = workloads.make_moe(workloads.MOE if args.config == "moe" else workloads.MOE_SMALL)
+    config = config or args.config
+    d = workloads.make_moe(workloads.MOE if config == "moe" else workloads.MOE_SMALL)
     wl = d["workload"]
     r, cr = d["routing"], d["calib_routing"]
     off, coff = r["offsets"].numpy(), cr["offsets"].numpy()
@@ -293,7 +298,7 @@ def reference_arm(args, rank: int, world: int):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (fp32 transform)", "data": "synthetic",
-        "config": workload_config(wl),
+        "config": dict(workload_config(wl), hadamard_block=32),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -313,23 +318,31 @@ def workload_config(wl):
             "l2": "inputs rotate over copies larger than L2 between steps"}
 
 
+def gemm_kernel_name(M: int) -> str:
+    """The GEMM kernel macaq_w4a4_gemm launches for M token rows."""
+    return "gemm_mxf4_skinny_kernel" if M <= 64 else "gemm_mxf4_pair_kernel"
+
+
 # ------------------------------------------------------------------- GPU arm
 
-def gpu_arm(args, rank: int, world: int):
+def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool = False):
+    """The dense layer's line (rank 0; None elsewhere).  light: device timing
+    only (no end-to-end leg, no CPU baseline), for the per-configuration table."""
     import torch
     import torch.distributed as dist
 
     import workloads
     import w4a4_mxfp4_quantized_02_b300 as mq
 
+    config = config or args.config
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     mq.lib()
     peaks = load_peaks()
-    fused = args.fused_swiglu
-    if fused and (workloads.DENSE[args.config].act != "swiglu" or args.hadamard_block != 32):
+    fused = args.fused_swiglu and not light
+    if fused and (workloads.DENSE[config].act != "swiglu" or args.hadamard_block != 32):
         raise SystemExit("--fused-swiglu needs a SwiGLU-input workload (down) and --hadamard-block 32")
-    d = workloads.make_dense_gated(args.config) if fused else workloads.make_dense(args.config)
+    d = workloads.make_dense_gated(config) if fused else workloads.make_dense(config)
     wl = d["workload"]
     M, N, K = wl.M, wl.N, wl.K
     stream = torch.cuda.current_stream()
@@ -418,42 +431,44 @@ def gpu_arm(args, rank: int, world: int):
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
 
-    # end to end through the C ABI: pinned host X in, pinned host Y out
-    def layer(b):
-        if fused:
-            mq.macaq_quant_act_silu(b["X"], inv, b["a_codes"], b["a_scales"])
-            mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
-        elif hb == 32:
-            mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
-        else:
-            mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
-            mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
-
-    e2e_steps = max(3, min(args.steps, 50))
-    Xh = (d["GU"] if fused else d["X"]).pin_memory()
+    e2e_value = e2e_ms = e2e_serial_ms = None
     nslot = min(3, nsets)
-    Yh = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(nslot)]
-    b = sets[0]
-    for _ in range(2):
-        b["X"].copy_(Xh, non_blocking=True)
-        layer(b)
-        Yh[0].copy_(b["Y"], non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        b["X"].copy_(Xh, non_blocking=True)
-        layer(b)
-        Yh[0].copy_(b["Y"], non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_ms = e2e_pipelined(stream, e2e_steps, nslot,
-                           lambda k: sets[k]["X"].copy_(Xh, non_blocking=True),
-                           lambda k: layer(sets[k]),
-                           lambda k: Yh[k].copy_(sets[k]["Y"], non_blocking=True))
-    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    if not light:
+        # end to end through the C ABI: pinned host X in, pinned host Y out
+        def layer(b):
+            if fused:
+                mq.macaq_quant_act_silu(b["X"], inv, b["a_codes"], b["a_scales"])
+                mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
+            elif hb == 32:
+                mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"])
+            else:
+                mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
+                mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
+
+        e2e_steps = max(3, min(args.steps, 50))
+        Xh = (d["GU"] if fused else d["X"]).pin_memory()
+        Yh = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(nslot)]
+        b = sets[0]
+        for _ in range(2):
+            b["X"].copy_(Xh, non_blocking=True)
+            layer(b)
+            Yh[0].copy_(b["Y"], non_blocking=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            b["X"].copy_(Xh, non_blocking=True)
+            layer(b)
+            Yh[0].copy_(b["Y"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e_ms = e2e_pipelined(stream, e2e_steps, nslot,
+                               lambda k: sets[k]["X"].copy_(Xh, non_blocking=True),
+                               lambda k: layer(sets[k]),
+                               lambda k: Yh[k].copy_(sets[k]["Y"], non_blocking=True))
+        e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
 
     traffic = None
     prof = os.path.join(ROOT, "profiles", "gemm_traffic.json")
@@ -464,9 +479,9 @@ def gpu_arm(args, rank: int, world: int):
             traffic = tj.get("dram_bytes_per_launch")
 
     if rank != 0:
-        return 0
+        return None
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not light:
         try:
             rate, rows, dt, threads = oracle_linear_rate(d, wl.M, args.cpu_seconds)
             cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -482,7 +497,7 @@ def gpu_arm(args, rank: int, world: int):
     timing = (f"CUDA events around the launch in {len(timed)} of the {args.steps} timed steps "
               "(includes the launch gap)")
     if flops / gemm_bytes >= fp4_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
-        roofline = {"bound": "tensor", "kernel": "gemm_mxf4_pair_kernel",
+        roofline = {"bound": "tensor", "kernel": gemm_kernel_name(M),
                     "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
                     "frac": gemm_tflops / fp4_peak, "traffic": traffic,
                     "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x "
@@ -491,7 +506,7 @@ def gpu_arm(args, rank: int, world: int):
     else:
         gbs = gemm_bytes / (gemm_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm",
-                    "kernel": "gemm_mxf4_skinny_kernel" if M <= 64 else "gemm_mxf4_pair_kernel",
+                    "kernel": gemm_kernel_name(M),
                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": gemm_bytes,
                     "peak_note": f"{peaks['source']} HBM copy bandwidth",
@@ -520,17 +535,17 @@ def gpu_arm(args, rank: int, world: int):
                       "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
                       "avg_launch_us": quant_avg * 1e3},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * xcols * 2,
-                "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
-                "copies": f"overlapped across steps ({nslot} buffer slots, separate copy streams)",
-                "serial_ms_per_step": e2e_serial_ms},
+        "e2e": None if light else {
+            "value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": M * xcols * 2,
+            "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
+            "copies": f"overlapped across steps ({nslot} buffer slots, separate copy streams)",
+            "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": 2 * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "clocks": sampler.summary(),
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 # ------------------------------------------------------- W4A16 GPU arm
@@ -905,7 +920,8 @@ def oracle_moe_rate(d, target_s: float):
     return done_flops / dt / 1e12, experts, dt, threads
 
 
-def gpu_arm_moe(args, rank: int, world: int):
+def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: bool = False):
+    """The routed layer's line (rank 0; None elsewhere); light as gpu_arm."""
     import torch
     import torch.distributed as dist
 
@@ -916,7 +932,8 @@ def gpu_arm_moe(args, rank: int, world: int):
     torch.cuda.set_device(dev)
     mq.lib()
     peaks = load_peaks()
-    d = workloads.make_moe(workloads.MOE if args.config == "moe" else workloads.MOE_SMALL)
+    config = config or args.config
+    d = workloads.make_moe(workloads.MOE if config == "moe" else workloads.MOE_SMALL)
     wl = d["workload"]
     E, K, F, rows = wl.E, wl.K, wl.F, wl.rows
     stream = torch.cuda.current_stream()
@@ -1032,35 +1049,37 @@ def gpu_arm_moe(args, rank: int, world: int):
     cb_bytes = rows * K * 2 + wl.T * K * 2 + wl.T * wl.topk * 8
     cb_gbs = cb_bytes / (avg[4] * 1e-3) / 1e9
 
-    # end to end through the C ABI: pinned host tokens in, pinned host token outputs out
-    e2e_steps = max(3, min(args.steps, 20))
-    Xh = d["X"].pin_memory()
-    Yh = [torch.empty(wl.T, K, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    for _ in range(2):
-        X.copy_(Xh, non_blocking=True)
-        step()
-        Yh[0].copy_(Ytok, non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        X.copy_(Xh, non_blocking=True)
-        step()
-        Yh[0].copy_(Ytok, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
-    Xs, Ys = [X, torch.empty_like(X)], [Ytok, torch.empty_like(Ytok)]
-    e2e_ms = e2e_pipelined(stream, e2e_steps, 2,
-                           lambda k: Xs[k].copy_(Xh, non_blocking=True),
-                           lambda k: step(Xin=Xs[k], Yout=Ys[k]),
-                           lambda k: Yh[k].copy_(Ys[k], non_blocking=True))
+    e2e_ms = e2e_serial_ms = None
+    if not light:
+        # end to end through the C ABI: pinned host tokens in, pinned host token outputs out
+        e2e_steps = max(3, min(args.steps, 20))
+        Xh = d["X"].pin_memory()
+        Yh = [torch.empty(wl.T, K, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        for _ in range(2):
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh[0].copy_(Ytok, non_blocking=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh[0].copy_(Ytok, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+        Xs, Ys = [X, torch.empty_like(X)], [Ytok, torch.empty_like(Ytok)]
+        e2e_ms = e2e_pipelined(stream, e2e_steps, 2,
+                               lambda k: Xs[k].copy_(Xh, non_blocking=True),
+                               lambda k: step(Xin=Xs[k], Yout=Ys[k]),
+                               lambda k: Yh[k].copy_(Ys[k], non_blocking=True))
 
     if rank != 0:
-        return 0
+        return None
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not light:
         try:
             rate, experts, dt, threads = oracle_moe_rate(d, args.cpu_seconds)
             cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -1103,18 +1122,18 @@ def gpu_arm_moe(args, rank: int, world: int):
                                q_bytes[1] / (avg[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]],
                       "bytes_per_launch": q_bytes, "avg_launch_us": [avg[0] * 1e3, avg[2] * 1e3]},
         "cpu_baseline": cpu,
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": wl.T * K * 2, "d2h_bytes_per_step": wl.T * K * 2,
-                "ms_per_step": e2e_ms,
-                "copies": "overlapped across steps (2 buffer slots, separate copy streams)",
-                "serial_ms_per_step": e2e_serial_ms},
+        "e2e": None if light else {
+            "value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": wl.T * K * 2, "d2h_bytes_per_step": wl.T * K * 2,
+            "ms_per_step": e2e_ms,
+            "copies": "overlapped across steps (2 buffer slots, separate copy streams)",
+            "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": 5 * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "clocks": sampler.summary(),
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 class StepPlan:
@@ -1250,14 +1269,53 @@ def mma_probe():
     return 0
 
 
+PER_CONFIG = ("attn", "attn_qkv", "decode_m1", "decode_m8", "decode_m16", "moe")
+
+
+def _summary(line: dict) -> dict:
+    """The device-timed part of a configuration's line."""
+    keep_r = ("bound", "kernel", "achieved", "peak", "unit", "frac", "avg_launch_us", "tflops")
+    keep_q = ("kernel", "achieved", "unit", "frac", "avg_launch_us", "bytes_per_launch")
+    out = {"workload": line["config"]["workload"], "value": line["value"], "unit": line["unit"],
+           "ms_per_step": line["ms_per_step"], "steps": line["steps"],
+           "roofline": {k: v for k, v in line["roofline"].items() if k in keep_r},
+           "act_quant": {k: v for k, v in line["act_quant"].items() if k in keep_q}}
+    for k in ("down_gemm", "combine"):
+        if k in line:
+            out[k] = line[k]
+    return out
+
+
+def per_config_table(args, rank: int, world: int) -> dict:
+    """Device timing of the other configurations (same steps and warm-up, no
+    end-to-end leg and no CPU baseline), one after another on this GPU."""
+    import torch
+
+    table = {}
+    for name in PER_CONFIG:
+        if name.startswith("moe"):
+            line = gpu_arm_moe(args, rank, world, config=name, light=True)
+        else:
+            line = gpu_arm(args, rank, world, config=name, light=True)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        if line is not None:
+            table[name] = _summary(line)
+    return table
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["macaq", "reference"], default="macaq")
-    ap.add_argument("--config", default="attn")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--config", default="down",
+                    help="workload of the line: down (default: prefill MLP down-projection, the "
+                         "largest single-GPU configuration), attn, attn_qkv, decode_m1/m8/m16, tiny, moe")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the device-timed table of the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--hadamard-block", type=int, choices=[32, 64], default=32,
                     help="Hadamard block of the transform (dense workloads)")
@@ -1288,13 +1346,22 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     try:
-        if args.config.startswith("moe"):
-            return gpu_arm_moe(args, rank, world)
         if args.stage == "flip":
             return gpu_arm_flip(args, rank, world)
         if args.precision == "w4a16":
             return gpu_arm_w4a16(args, rank, world)
-        return gpu_arm(args, rank, world)
+        if args.config.startswith("moe"):
+            line = gpu_arm_moe(args, rank, world)
+        else:
+            line = gpu_arm(args, rank, world)
+            if (not args.no_per_config and args.config == "down" and args.hadamard_block == 32
+                    and not args.fused_swiglu):
+                table = per_config_table(args, rank, world)
+                if line is not None:
+                    line["per_config"] = table
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
     finally:
         if world > 1:
             import torch.distributed as dist

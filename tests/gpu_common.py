@@ -53,8 +53,7 @@ def u8(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy().astype(np.uint8)
 
 
-def check_silu_blocks(codes: np.ndarray, scales: np.ndarray, GU, f: np.ndarray, hb: int = 32,
-                      max_window_frac: float = 0.05):
+def check_silu_blocks(codes: np.ndarray, scales: np.ndarray, GU, f: np.ndarray, hb: int = 32):
     """Check the GPU's MXFP4 of h = bf16_rn(SiLU(g) * u) (fused SwiGLU transform)
     against the oracle, whose h is the exact value rounded once to bf16.
 
@@ -63,7 +62,8 @@ def check_silu_blocks(codes: np.ndarray, scales: np.ndarray, GU, f: np.ndarray, 
     admissible (the oracle reports both).  Per Hadamard block of hb channels
     of a row: codes and scales must equal the oracle's bit for bit when no
     element of the block is in that window; otherwise they must equal the
-    oracle's for one admissible choice of the windowed elements.
+    oracle's for one admissible choice of the windowed elements.  The share
+    of windowed blocks must stay near its expected hb * 2^-11.
 
     codes [rows, F/2], scales row-major [rows, F/32] (the GPU's); GU bf16
     [rows, 2F] (gate | up); f fp32 [F] balance factors.  Returns (ca, sa): the
@@ -105,5 +105,10 @@ def check_silu_blocks(codes: np.ndarray, scales: np.ndarray, GU, f: np.ndarray, 
     frac = float(windowed.mean()) if windowed.size else 0.0
     record_parity("silu", blocks=int(same.size), windowed=int(windowed.sum()),
                   differ=int((~same).sum()), window_frac=frac)
-    assert frac <= max_window_frac, f"{frac:.3%} of blocks have an element near a boundary"
+    # an element falls in the window with probability about 2 * 2^-20 / 2^-8 =
+    # 2^-11, a block of hb elements about hb * 2^-11; the check stays
+    # meaningful (nearly every block compared bit for bit) below four times
+    # that, with a few blocks of slack for small samples
+    limit = 4 * hb * 2.0 ** -11 + 5.0 / max(1, same.size)
+    assert frac <= limit, f"{frac:.3%} of blocks have an element near a boundary (limit {limit:.3%})"
     return ca, sa
