@@ -371,19 +371,20 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
             "a_scales": torch.empty(mq.macaq_scale_bytes(M, K), dtype=torch.uint8, device=dev),
         })
 
-    def step(i, ev=None):
+    def quant_part(i):
         b = sets[i % nsets]
-        if ev is not None:
-            ev[0].record(stream)
         if fused:
             mq.macaq_quant_act_silu(b["X"], inv, b["a_codes"], b["a_scales"])
         else:
             mq.macaq_quant_act_hb(b["X"], inv, hb, b["a_codes"], b["a_scales"])
-        if ev is not None:
-            ev[1].record(stream)
+
+    def gemm_part(i):
+        b = sets[i % nsets]
         mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
-        if ev is not None:
-            ev[2].record(stream)
+
+    def step(i):
+        quant_part(i)
+        gemm_part(i)
 
     for i in range(args.warmup):
         step(i)
@@ -394,8 +395,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     chunk = nsets * max(1, math.ceil(8 / nsets))
     graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
-    timed = plan.event_steps
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in timed}
+    batches = KernelBatches(plan.eager_steps, min(nsets, 4), 2)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -407,8 +407,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         h0 = time.perf_counter()
         for _ in range(plan.replays):
             graph.replay()
-        for i in plan.eager_steps:
-            step(i, evs.get(i))
+        batches.run([quant_part, gemm_part], stream)
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -416,16 +415,13 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    q_ms = [e[0].elapsed_time(e[1]) for e in evs.values()]
-    g_ms = [e[1].elapsed_time(e[2]) for e in evs.values()]
+    quant_avg, gemm_avg = batches.per_launch_ms()
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
 
     flops = 2.0 * M * N * K
     value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
-    gemm_avg = statistics.mean(g_ms)
-    quant_avg = statistics.mean(q_ms)
     gemm_tflops = flops / (gemm_avg * 1e-3) / 1e12
     quant_bytes = M * xcols * 2 + M * K // 2 + M * K // 32
     quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
@@ -494,8 +490,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     # the GEMM's bound: FP4 tensor throughput above the ridge intensity, HBM
     # bytes below it (decode: the weight bytes)
     gemm_bytes = M * (K // 2 + K // 32) + N * (K // 2 + K // 32) + M * N * 2
-    timing = (f"CUDA events around the launch in {len(timed)} of the {args.steps} timed steps "
-              "(includes the launch gap)")
+    timing = (f"CUDA events around kernel groups: {batches.describe()} of the {args.steps} timed steps")
     if flops / gemm_bytes >= fp4_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
         roofline = {"bound": "tensor", "kernel": gemm_kernel_name(M),
                     "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
@@ -615,16 +610,17 @@ def gpu_arm_w4a16(args, rank: int, world: int):
              "Xt": torch.empty(M, K, dtype=torch.bfloat16, device=dev),
              "Y": torch.empty(M, N, dtype=torch.bfloat16, device=dev)} for i in range(nsets)]
 
-    def step(i, ev=None):
+    def transform_part(i):
         b = sets[i % nsets]
-        if ev is not None:
-            ev[0].record(stream)
         mq.macaq_transform_act_bf16(b["X"], inv, hb, Xt=b["Xt"])
-        if ev is not None:
-            ev[1].record(stream)
+
+    def gemm_part(i):
+        b = sets[i % nsets]
         mq.macaq_w4a16_gemm(b["Xt"], b["Wd"], Y=b["Y"], workspace=gemm_ws)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def step(i):
+        transform_part(i)
+        gemm_part(i)
 
     for i in range(args.warmup):
         step(i)
@@ -632,7 +628,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
     chunk = nsets * max(1, math.ceil(8 / nsets))
     graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for i in plan.event_steps}
+    batches = KernelBatches(plan.eager_steps, min(nsets, 4), 2)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -643,16 +639,14 @@ def gpu_arm_w4a16(args, rank: int, world: int):
         t_start.record(stream)
         for _ in range(plan.replays):
             graph.replay()
-        for i in plan.eager_steps:
-            step(i, evs.get(i))
+        batches.run([transform_part, gemm_part], stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs.values())
-    g_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs.values())
+    q_ms, g_ms = batches.per_launch_ms()
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
@@ -691,8 +685,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
             cpu = {"value": None, "unit": "TFLOP/s", "cores": None, "kind": "oracle",
                    "sample": f"failed: {e}"}
     bf16_peak = peaks["bf16_tflops"]
-    timing = (f"CUDA events around the launch in {len(evs)} of the {args.steps} timed steps "
-              "(includes the launch gap)")
+    timing = f"CUDA events around kernel groups: {batches.describe()} of the {args.steps} timed steps"
     if flops / gemm_bytes >= bf16_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
         roofline = {"bound": "tensor", "kernel": "cuBLASLt bf16 GEMM (library)",
                     "achieved": gemm_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
@@ -974,28 +967,31 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     tok_w = r["tok_weights"].to(dev)
     Ytok = torch.empty(wl.T, K, dtype=torch.bfloat16, device=dev)
 
-    def step(ev=None, Xin=None, Yout=None):
-        Xin = X if Xin is None else Xin
-        Yout = Ytok if Yout is None else Yout
-        if ev is not None:
-            ev[0].record(stream)
-        mq.macaq_quant_act_grouped(Xin, row_src, offs, inv_gu, rows, E, a_gu, as_gu)
-        if ev is not None:
-            ev[1].record(stream)
+    def k_quant_gu(i, Xin=None):
+        mq.macaq_quant_act_grouped(X if Xin is None else Xin, row_src, offs, inv_gu, rows, E, a_gu, as_gu)
+
+    def k_gemm_gu(i):
         mq.macaq_grouped_w4a4_gemm(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, 2 * F, K, Y=Ygu)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def k_quant_dn(i):
         # the down input is SiLU(gate) * up of the gate+up output, fused into its transform
         mq.macaq_quant_act_grouped_silu(Ygu, offs, inv_dn, rows, E, a_dn, as_dn)
-        if ev is not None:
-            ev[3].record(stream)
+
+    def k_gemm_dn(i):
         mq.macaq_grouped_w4a4_gemm(a_dn, as_dn, wdn_codes, wdn_scales, offs, rows, E, K, F, Y=Ydn)
-        if ev is not None:
-            ev[4].record(stream)
+
+    def k_combine(i, Yout=None):
         # the token outputs: each token's eight expert rows, weighted
-        mq.macaq_moe_combine(Ydn, tok_rows, tok_w, out=Yout)
-        if ev is not None:
-            ev[5].record(stream)
+        mq.macaq_moe_combine(Ydn, tok_rows, tok_w, out=Ytok if Yout is None else Yout)
+
+    parts = [k_quant_gu, k_gemm_gu, k_quant_dn, k_gemm_dn, k_combine]
+
+    def step(Xin=None, Yout=None):
+        k_quant_gu(0, Xin)
+        k_gemm_gu(0)
+        k_quant_dn(0)
+        k_gemm_dn(0)
+        k_combine(0, Yout)
 
     for _ in range(args.warmup):
         step()
@@ -1006,8 +1002,9 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     chunk = 4
     graph = None if args.no_graphs else capture_graph(lambda: [step() for _ in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
-    timed = plan.event_steps
-    evs = {i: [torch.cuda.Event(enable_timing=True) for _ in range(6)] for i in timed}
+    # every step computes the same layer on the same tokens, so a batch of
+    # steps may share the one set of intermediate buffers
+    batches = KernelBatches(plan.eager_steps, 2, 5)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -1019,8 +1016,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         h0 = time.perf_counter()
         for _ in range(plan.replays):
             graph.replay()
-        for i in plan.eager_steps:
-            step(evs.get(i))
+        batches.run(parts, stream)
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -1028,7 +1024,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    avg = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs.values()) for j in range(5)]
+    avg = batches.per_launch_ms()
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
@@ -1107,8 +1103,8 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
                      "frac": gu_gbs / peaks["hbm_gbs"], "traffic": None,
                      "bytes_per_launch": gu_bytes, "avg_launch_us": avg[1] * 1e3,
                      "tflops": wl.flops_gate_up / (avg[1] * 1e-3) / 1e12,
-                     "timing": f"CUDA events around the launch in {len(timed)} of the {args.steps} "
-                               "timed steps (includes the launch gap)"},
+                     "timing": f"CUDA events around kernel groups: {batches.describe()} of the "
+                               f"{args.steps} timed steps"},
         "down_gemm": {"achieved": dn_gbs, "unit": "GB/s", "frac": dn_gbs / peaks["hbm_gbs"],
                       "bytes_per_launch": dn_bytes, "avg_launch_us": avg[3] * 1e3,
                       "tflops": wl.flops_down / (avg[3] * 1e-3) / 1e12},
@@ -1137,12 +1133,10 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
 
 
 class StepPlan:
-    """How the timed steps run.  Per-kernel CUDA events bracket the launches of
-    about one step in `every`: an event between two kernels stops the second
-    from starting its set-up while the first finishes (programmatic dependent
-    launch), so they are kept off most steps.  With a captured graph of `chunk`
-    steps, the unbracketed steps run as whole-graph replays (the host's launch
-    cost then does not pace short steps) and the rest, all bracketed, eagerly."""
+    """How the timed steps run.  About one step in `every` runs eagerly for
+    per-kernel timing (KernelBatches).  With a captured graph of `chunk` steps,
+    the other steps run as whole-graph replays (the host's launch cost then
+    does not pace short steps); without one, every step runs eagerly."""
 
     def __init__(self, steps: int, every: int, chunk: int):
         every = max(1, every)
@@ -1155,14 +1149,50 @@ class StepPlan:
         else:
             self.replays = 0
             self.eager_steps = list(range(steps))
-            self.event_steps = [i for i in range(steps) if i % every == 0]
+            self.event_steps = list(self.eager_steps)
         self.chunk = chunk
 
     def describe(self) -> str:
         if self.replays:
             return (f"{self.replays} replays of a CUDA graph of {self.chunk} steps, then "
-                    f"{len(self.eager_steps)} eager steps with per-kernel events")
-        return f"eager launches; per-kernel events on {len(self.event_steps)} steps"
+                    f"{len(self.eager_steps)} eager steps in kernel-by-kernel batches with CUDA events")
+        return "eager launches in kernel-by-kernel batches with CUDA events"
+
+
+class KernelBatches:
+    """The eager steps of the timed region, run in batches of `nb` whole steps
+    kernel by kernel -- every step's first kernel, then every step's second,
+    and so on -- with one CUDA event between kernel groups on the launching
+    stream.  Consecutive launches of one kernel keep their programmatic launch
+    overlap (as in a stack of layers), and an event's launch gap is paid once
+    per group instead of once per launch.  Every step still runs all of its
+    kernels on its own buffers; a batch never reuses a buffer set."""
+
+    def __init__(self, steps: list, nb: int, nparts: int):
+        import torch
+
+        nb = max(1, nb)
+        self.groups = [steps[i:i + nb] for i in range(0, len(steps), nb)]
+        self.nparts = nparts
+        self.events = [[torch.cuda.Event(enable_timing=True) for _ in range(nparts + 1)]
+                       for _ in self.groups]
+
+    def run(self, parts, stream):
+        for group, ev in zip(self.groups, self.events):
+            ev[0].record(stream)
+            for j, part in enumerate(parts):
+                for i in group:
+                    part(i)
+                ev[j + 1].record(stream)
+
+    def per_launch_ms(self) -> list:
+        """Average device time per launch of each kernel (after a synchronize)."""
+        n = sum(len(g) for g in self.groups)
+        return [sum(ev[j].elapsed_time(ev[j + 1]) for ev in self.events) / n for j in range(self.nparts)]
+
+    def describe(self) -> str:
+        sizes = sorted({len(g) for g in self.groups})
+        return f"{sum(len(g) for g in self.groups)} eager steps in kernel-by-kernel batches of {sizes}"
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
