@@ -875,11 +875,12 @@ def gpu_arm_flip(args, rank: int, world: int):
 
 # ------------------------------------------------------------- MoE GPU arm
 
-def moe_workload_config(wl):
+def moe_workload_config(wl, fused: bool = True):
+    how = ("the gate+up GEMM epilogue writes the down input's MXFP4 (SiLU(gate)*up, transform)" if fused
+           else "SiLU(gate)*up fused into the down input's transform")
     return {"workload": f"{wl.name}: {wl.T} tokens x top-{wl.topk} of {wl.E} experts = {wl.rows} rows; "
-                        f"gate+up K={wl.K} N={2 * wl.F}, SiLU(gate)*up fused into the down input's "
-                        f"transform, down K={wl.F} N={wl.K}, weighted top-{wl.topk} combine into the "
-                        f"token outputs; bf16 in/out, MXFP4 W4A4",
+                        f"gate+up K={wl.K} N={2 * wl.F}, {how}, down K={wl.F} N={wl.K}, weighted "
+                        f"top-{wl.topk} combine into the token outputs; bf16 in/out, MXFP4 W4A4",
             "T": wl.T, "E": wl.E, "topk": wl.topk, "K": wl.K, "F": wl.F, "rows": wl.rows,
             "l2": "weights (302 MB of codes) exceed L2; no input rotation needed"}
 
@@ -942,7 +943,15 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     inv_gu = torch.empty_like(s_gu)
     for e in range(E):
         s_gu[e], inv_gu[e] = mq.macaq_balance_scales(Xc, W[e], xc_rows=c_rows[coff[e]:coff[e + 1]])
-    wgu_codes, wgu_scales = mq.macaq_quant_weight_grouped(W, s_gu)
+    fused = not args.moe_unfused
+    if fused:
+        # gate and up rows interleaved in chunks of 64 channels: the gate+up
+        # GEMM's epilogue then writes the down input's MXFP4 directly
+        Wil = mq.macaq_interleave_gate_up(W)
+        wgu_codes, wgu_scales = mq.macaq_quant_weight_grouped(Wil, s_gu)
+        del Wil
+    else:
+        wgu_codes, wgu_scales = mq.macaq_quant_weight_grouped(W, s_gu)
     del W
     W = d["W_down"].to(dev)
     s_dn = torch.empty(E, F, dtype=torch.float32, device=dev)
@@ -971,10 +980,16 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         mq.macaq_quant_act_grouped(X if Xin is None else Xin, row_src, offs, inv_gu, rows, E, a_gu, as_gu)
 
     def k_gemm_gu(i):
-        mq.macaq_grouped_w4a4_gemm(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, 2 * F, K, Y=Ygu)
+        if fused:
+            # the epilogue forms h = SiLU(gate) * up and writes the down input's MXFP4
+            mq.macaq_grouped_w4a4_gemm_swiglu(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, F, K, inv_dn,
+                                              h_codes=a_dn, h_scales=as_dn)
+        else:
+            mq.macaq_grouped_w4a4_gemm(a_gu, as_gu, wgu_codes, wgu_scales, offs, rows, E, 2 * F, K, Y=Ygu)
 
     def k_quant_dn(i):
-        # the down input is SiLU(gate) * up of the gate+up output, fused into its transform
+        # unfused route: the down input is SiLU(gate) * up of the bf16 gate+up
+        # output, fused into its transform
         mq.macaq_quant_act_grouped_silu(Ygu, offs, inv_dn, rows, E, a_dn, as_dn)
 
     def k_gemm_dn(i):
@@ -984,13 +999,12 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         # the token outputs: each token's eight expert rows, weighted
         mq.macaq_moe_combine(Ydn, tok_rows, tok_w, out=Ytok if Yout is None else Yout)
 
-    parts = [k_quant_gu, k_gemm_gu, k_quant_dn, k_gemm_dn, k_combine]
+    parts = [k_quant_gu, k_gemm_gu] + ([] if fused else [k_quant_dn]) + [k_gemm_dn, k_combine]
 
     def step(Xin=None, Yout=None):
         k_quant_gu(0, Xin)
-        k_gemm_gu(0)
-        k_quant_dn(0)
-        k_gemm_dn(0)
+        for part in parts[1:-1]:
+            part(0)
         k_combine(0, Yout)
 
     for _ in range(args.warmup):
@@ -1004,7 +1018,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
     # every step computes the same layer on the same tokens, so a batch of
     # steps may share the one set of intermediate buffers
-    batches = KernelBatches(plan.eager_steps, 2, 5)
+    batches = KernelBatches(plan.eager_steps, 2, len(parts))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -1025,6 +1039,8 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     avg = batches.per_launch_ms()
+    if fused:
+        avg = avg[:2] + [None] + avg[2:]   # no separate down-input transform
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
@@ -1033,9 +1049,11 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
     # algorithmic bytes: codes + scales of A and W, bf16 Y (the grouped GEMMs are
     # bound by the weight bytes at this token count)
-    def gemm_bytes(n, k):
-        return rows * (k // 2 + k // 32) + E * n * (k // 2 + k // 32) + rows * n * 2
-    gu_bytes, dn_bytes = gemm_bytes(2 * F, K), gemm_bytes(K, F)
+    def gemm_bytes(n, k, out_bytes):
+        return rows * (k // 2 + k // 32) + E * n * (k // 2 + k // 32) + out_bytes
+    # the fused gate+up GEMM writes the down input's codes and scales instead of bf16 g|u
+    gu_out = rows * (F // 2 + F // 32) if fused else rows * 2 * F * 2
+    gu_bytes, dn_bytes = gemm_bytes(2 * F, K, gu_out), gemm_bytes(K, F, rows * K * 2)
     # algorithmic bytes: each token row read once (its eight expert copies are
     # gathered from L2), every sorted row's codes and scales written once
     q_bytes = [wl.T * K * 2 + rows * (K // 2 + K // 32), rows * 2 * F * 2 + rows * (F // 2 + F // 32)]
@@ -1097,8 +1115,10 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         "vs_baseline": None,
         "dtype": "mxfp4 (e2m1 codes, e8m0 block scales, fp32 accumulate; fp32 transform)",
         "data": "synthetic",
-        "config": moe_workload_config(wl),
-        "roofline": {"bound": "hbm", "kernel": "gemm_mxf4_pair_kernel<6, true> (grouped, gate+up)",
+        "config": moe_workload_config(wl, fused),
+        "roofline": {"bound": "hbm",
+                     "kernel": ("gemm_mxf4_pair_kernel<6, true, 1> (grouped gate+up, MXFP4 h epilogue)" if fused
+                                else "gemm_mxf4_pair_kernel<6, true> (grouped, gate+up)"),
                      "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gu_gbs / peaks["hbm_gbs"], "traffic": None,
                      "bytes_per_launch": gu_bytes, "avg_launch_us": avg[1] * 1e3,
@@ -1111,12 +1131,17 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         "combine": {"kernel": "moe_combine_kernel", "achieved": cb_gbs, "unit": "GB/s",
                     "frac": cb_gbs / peaks["hbm_gbs"], "bytes_per_launch": cb_bytes,
                     "avg_launch_us": avg[4] * 1e3},
-        "act_quant": {"kernel": "quant_grouped_tma_kernel (token rows; SwiGLU-fused for the down input)",
-                      "achieved": [q_bytes[0] / (avg[0] * 1e-3) / 1e9, q_bytes[1] / (avg[2] * 1e-3) / 1e9],
-                      "peak": peaks["hbm_gbs"], "unit": "GB/s (gate+up input, down input)",
-                      "frac": [q_bytes[0] / (avg[0] * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                               q_bytes[1] / (avg[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]],
-                      "bytes_per_launch": q_bytes, "avg_launch_us": [avg[0] * 1e3, avg[2] * 1e3]},
+        "act_quant": ({"kernel": "quant_grouped_tma_kernel (token rows; the down input comes from the "
+                                 "gate+up GEMM's epilogue)",
+                       "achieved": q_bytes[0] / (avg[0] * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": q_bytes[0] / (avg[0] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                       "bytes_per_launch": q_bytes[0], "avg_launch_us": avg[0] * 1e3} if fused else
+                      {"kernel": "quant_grouped_tma_kernel (token rows; SwiGLU-fused for the down input)",
+                       "achieved": [q_bytes[0] / (avg[0] * 1e-3) / 1e9, q_bytes[1] / (avg[2] * 1e-3) / 1e9],
+                       "peak": peaks["hbm_gbs"], "unit": "GB/s (gate+up input, down input)",
+                       "frac": [q_bytes[0] / (avg[0] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                q_bytes[1] / (avg[2] * 1e-3) / 1e9 / peaks["hbm_gbs"]],
+                       "bytes_per_launch": q_bytes, "avg_launch_us": [avg[0] * 1e3, avg[2] * 1e3]}),
         "cpu_baseline": cpu,
         "e2e": None if light else {
             "value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -1124,7 +1149,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
             "ms_per_step": e2e_ms,
             "copies": "overlapped across steps (2 buffer slots, separate copy streams)",
             "serial_ms_per_step": e2e_serial_ms},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": len(parts) * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "clocks": sampler.summary(),
@@ -1344,6 +1369,8 @@ def main():
                     help="workload of the line: down (default: prefill MLP down-projection, the "
                          "largest single-GPU configuration), attn, attn_qkv, decode_m1/m8/m16, tiny, moe")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--moe-unfused", action="store_true",
+                    help="moe: the gate+up GEMM writes bf16 gate|up and a separate kernel forms the down input")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the device-timed table of the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true")

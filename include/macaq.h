@@ -272,6 +272,43 @@ macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_sc
                                      int64_t N, int64_t K, void *Y, int64_t ldy,
                                      macaq_stream_t stream);
 
+/* The gate+up projection of a routed gated MLP with its output written
+ * directly as the down projection's MXFP4 input (the routed experts run W4A4,
+ * page "Huawei MACaQ Is an Open-Source Model Quantizer", section "MACaQ
+ * Backends"; the scale and rotation run online at inference time, page "What
+ * is MACaQ quantization", section "How MACaQ works", closing paragraph): the
+ * grouped GEMM's epilogue forms, per sorted row r of expert e and channel j,
+ *   g = bf16_rn(gate GEMM output), u = bf16_rn(up GEMM output),
+ *   h_j = bf16_rn( SiLU(g) * u )          (as macaq_quant_act_grouped_silu)
+ * and runs the activation transform on h with the down projection's balance
+ * factors inv_s row e (fp32 [E, F]; Hadamard block 32 or 64, MXFP4) into
+ * padded row P_e + r - offsets[e] -- exactly the codes and scales that
+ * macaq_grouped_w4a4_gemm with bf16 output followed by
+ * macaq_quant_act_grouped_silu(_hb) produce, without writing the bf16
+ * gate|up matrix.
+ * a_codes / a_scales: the grouped token transform (macaq_quant_act_grouped);
+ * w_codes [E, 2F, K/2] and w_scales (E tiled arrays of 2F rows): the gate and
+ * up weights prepared with macaq_quant_weight_grouped(_hb) from the rows
+ * macaq_interleave_gate_up arranged; h_codes [P, F/2] and h_scales tiled for
+ * P = macaq_grouped_padded_rows(rows, E) rows of F channels, as
+ * macaq_quant_act_grouped_silu writes them (scale bytes of padding rows 0,
+ * codes of padding rows unspecified).  F % 64 == 0, K % 32 == 0, E <= 256,
+ * hadamard_block 32 or 64 (F % 64 == 0 covers both). */
+macaq_status macaq_grouped_w4a4_gemm_swiglu(const uint8_t *a_codes, const uint8_t *a_scales,
+                                            const uint8_t *w_codes, const uint8_t *w_scales,
+                                            const int32_t *expert_offsets, int64_t rows, int64_t E, int64_t F,
+                                            int64_t K, const float *inv_s, int64_t hadamard_block,
+                                            uint8_t *h_codes, uint8_t *h_scales, macaq_stream_t stream);
+
+/* Weight preparation for macaq_grouped_w4a4_gemm_swiglu: W_gu bf16
+ * [E, 2F, K] with each expert's gate rows 0 .. F-1 and up rows F .. 2F-1 ->
+ * W_out bf16 [E, 2F, K] whose rows 128c .. 128c+63 are gate rows 64c ..
+ * 64c+63 and rows 128c+64 .. 128c+127 the up rows of the same channels (a
+ * row permutation; no arithmetic).  F % 64 == 0; W_gu and W_out distinct,
+ * 16-byte aligned, row pitch K. */
+macaq_status macaq_interleave_gate_up(const void *W_gu, int64_t E, int64_t F, int64_t K, void *W_out,
+                                      macaq_stream_t stream);
+
 /* ------------------------------------------------ W4A16 fallback */
 
 /* The weight-only fallback (page "Huawei MACaQ: Choosing GGUF or vLLM and

@@ -148,6 +148,23 @@ def test_grouped_rejections(L):
 
 
 
+def test_gate_up_swiglu_rejections(L):
+    g = L.macaq_grouped_w4a4_gemm_swiglu
+    i = L.macaq_interleave_gate_up
+    p = _fake()
+    assert g(p, p, p, p, p, 100, 4, 96, 128, p, 32, p, p, None) == INVALID     # F % 64
+    assert g(p, p, p, p, p, 100, 4, 128, 128, p, 16, p, p, None) == INVALID    # block neither 32 nor 64
+    assert g(p, p, p, p, p, 100, 0, 128, 128, p, 32, p, p, None) == INVALID    # E = 0
+    assert g(p, p, p, p, p, 100, 300, 128, 128, p, 32, p, p, None) == UNSUPPORTED
+    assert g(p, p, p, p, p, 100, 4, 128, 128, None, 32, p, p, None) == INVALID  # no factors
+    assert g(p, p, p, p, p, 100, 4, 128, 128, _fake(0x10004), 32, p, p, None) == ALIGN
+    assert g(p, p, p, p, p, 0, 4, 128, 128, p, 32, p, p, None) == OK           # no rows: nothing to do
+    assert i(p, 4, 96, 128, _fake(0x20000), None) == INVALID                      # F % 64
+    assert i(p, 4, 128, 128, p, None) == INVALID                                  # in place
+    assert i(p, 4, 128, 128, _fake(0x20008), None) == ALIGN
+    assert i(p, 0, 128, 128, _fake(0x20000), None) == OK
+
+
 def test_hadamard_block_rejections(L):
     q = L.macaq_quant_act_hb
     w = L.macaq_quant_weight_hb

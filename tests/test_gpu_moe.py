@@ -304,3 +304,68 @@ def test_moe_hadamard_block_64(name, experts):
         if hi == lo:
             continue
         check_silu_blocks(u8(a_codes)[pos[lo:hi]], scd[pos[lo:hi]], GU[lo:hi], inv_dn[e], hb=64)
+
+
+def interleave_index(F: int) -> np.ndarray:
+    """Source row of each output row of the gate/up interleave (chunks of 64)."""
+    n = np.arange(2 * F)
+    c, j = n // 128, n % 128
+    return np.where(j < 64, 64 * c + j, F + 64 * c + (j - 64))
+
+
+@pytest.mark.parametrize("hb", [32, 64])
+@pytest.mark.parametrize("name,experts", [("small", None), ("full", (0, 7, 64, 127))])
+def test_gate_up_epilogue_writes_mxfp4(name, experts, hb):
+    """The fused gate+up GEMM writes the down input's MXFP4 directly: bit for
+    bit the codes and scales of the unfused route (bf16 gate|up output, then
+    the SwiGLU-fused grouped transform) on every row, padding-row scales zero,
+    and against the oracle's exact-then-rounded h with the admissible-rounding
+    rule (tests/gpu_common.py)."""
+    d = moe(name)
+    wl = d["workload"]
+    E, K, F = wl.E, wl.K, wl.F
+    gpu = run_gate_up(d, hb=hb)
+    r = d["routing"]
+    off = r["offsets"].numpy()
+    rows_n = int(off[-1])
+    offs = to_dev(r["offsets"])
+    # the weight rows interleaved in chunks of 64 channels: a pure permutation
+    W = to_dev(d["W_gu"])
+    Wil = mq.macaq_interleave_gate_up(W)
+    torch.cuda.synchronize()
+    idx = torch.from_numpy(interleave_index(F))
+    assert torch.equal(Wil.cpu().view(torch.int16), d["W_gu"][:, idx].view(torch.int16))
+    wil_codes, wil_scales = mq.macaq_quant_weight_grouped(Wil, gpu["s"], hadamard_block=hb)
+    del W, Wil
+    rng = np.random.default_rng(11 + hb)
+    inv_dn = (np.float32(1.0) / rng.uniform(0.1, 10.0, (E, F)).astype(np.float32)).astype(np.float32)
+    inv_dev = torch.from_numpy(inv_dn).to(DEV)
+    P = mq.macaq_grouped_padded_rows(rows_n, E)
+    # start from garbage so that every byte the contract fixes must be written
+    h_codes = torch.full((P, F // 2), 0xA5, dtype=torch.uint8, device=DEV)
+    h_scales = torch.full((mq.macaq_scale_bytes(P, F),), 0xFF, dtype=torch.uint8, device=DEV)
+    mq.macaq_grouped_w4a4_gemm_swiglu(gpu["a_codes"], gpu["a_scales"], wil_codes, wil_scales, offs, rows_n,
+                                      E, F, K, inv_dev, h_codes=h_codes, h_scales=h_scales, hadamard_block=hb)
+    a_dn, as_dn = mq.macaq_quant_act_grouped_silu(gpu["Y"], offs, inv_dev, rows_n, E, hadamard_block=hb)
+    torch.cuda.synchronize()
+    assert mq.macaq_check_device_error() == 0
+    pos = padded_positions(off)
+    used = int(np.sum((np.diff(off) + 127) // 128 * 128))
+    # codes of every routed row and every scale byte of the used padded rows
+    np.testing.assert_array_equal(u8(h_codes)[pos], u8(a_dn)[pos])
+    sc_f = untile_scales(u8(h_scales), P, F)
+    sc_u = untile_scales(u8(as_dn), P, F)
+    np.testing.assert_array_equal(sc_f[:used], sc_u[:used])
+    assert not sc_f[np.setdiff1d(np.arange(used), pos)].any()
+    # padding scale columns of the tiled layout are zero too
+    pad_cols = (F // 32 + 7) // 8 * 8
+    full = u8(h_scales)[: (used + 127) // 128 * 128 * pad_cols]
+    tiled = full.reshape(-1, pad_cols // 4, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1, pad_cols)
+    assert not tiled[:used, F // 32:].any()
+    # the oracle, with the GPU's own bf16 gate|up values as the SwiGLU input
+    GU = gpu["Y"].cpu()
+    for e in (range(E) if experts is None else experts):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        check_silu_blocks(u8(h_codes)[pos[lo:hi]], sc_f[pos[lo:hi]], GU[lo:hi], inv_dn[e], hb=hb)

@@ -73,6 +73,9 @@ _SIGS = {
     "macaq_flip_prepare": ([_P, _P, _I64, _I64, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_flip_sweeps": ([_P, _I64, _I64, ctypes.c_int32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
     "macaq_quant_act_silu": ([_P, _I64, _P, _I64, _I64, _P, _P, _P], ctypes.c_int),
+    "macaq_grouped_w4a4_gemm_swiglu": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _P, _P],
+                                       ctypes.c_int),
+    "macaq_interleave_gate_up": ([_P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
     "macaq_moe_combine": ([_P, _I64, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_quant_weight_grouped_hb": ([_P, _P, _I64, _I64, _I64, _I64, _P, _P, _P], ctypes.c_int),
     "macaq_quant_act_grouped_hb": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _P, _P],
@@ -499,6 +502,36 @@ def macaq_grouped_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, expert_offsets
         _ptr(a_codes), _ptr(a_scales), _ptr(w_codes), _ptr(w_scales), _ptr(expert_offsets), rows,
         E, N, K, _ptr(Y), _ld(Y), _stream(stream)))
     return Y
+
+
+def macaq_interleave_gate_up(W_gu: torch.Tensor, W_out=None, stream=None) -> torch.Tensor:
+    """Gate/up weight rows [E, 2F, K] interleaved in chunks of 64 channels, the
+    layout macaq_grouped_w4a4_gemm_swiglu reads (see the header)."""
+    _dev(W_gu, "W_gu")
+    W_gu = W_gu.contiguous()
+    E, two_f, K = W_gu.shape
+    if W_out is None:
+        W_out = torch.empty_like(W_gu)
+    _check("macaq_interleave_gate_up", lib().macaq_interleave_gate_up(
+        _ptr(W_gu), E, two_f // 2, K, _ptr(W_out), _stream(stream)))
+    return W_out
+
+
+def macaq_grouped_w4a4_gemm_swiglu(a_codes, a_scales, w_codes, w_scales, expert_offsets, rows: int,
+                                   E: int, F: int, K: int, inv_s, h_codes=None, h_scales=None,
+                                   stream=None, hadamard_block: int = 32):
+    """Grouped gate+up GEMM (interleaved weights) whose epilogue writes the down
+    projection's MXFP4 input h = SiLU(g) * u directly; returns (h_codes, h_scales)
+    in the expert-padded layout of macaq_quant_act_grouped_silu."""
+    P = macaq_grouped_padded_rows(rows, E)
+    if h_codes is None:
+        h_codes = torch.empty(P, F // 2, dtype=torch.uint8, device=a_codes.device)
+    if h_scales is None:
+        h_scales = torch.empty(macaq_scale_bytes(P, F), dtype=torch.uint8, device=a_codes.device)
+    _check("macaq_grouped_w4a4_gemm_swiglu", lib().macaq_grouped_w4a4_gemm_swiglu(
+        _ptr(a_codes), _ptr(a_scales), _ptr(w_codes), _ptr(w_scales), _ptr(expert_offsets), rows, E, F, K,
+        _ptr(inv_s), hadamard_block, _ptr(h_codes), _ptr(h_scales), _stream(stream)))
+    return h_codes, h_scales
 
 
 # ---------------------------------------------------------- device errors

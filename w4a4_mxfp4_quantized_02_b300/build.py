@@ -1,7 +1,8 @@
 """Build the CUDA library ``libmacaq.so`` in-tree for sm_103a (B300).
 
 Each translation unit is compiled with nvcc for ``compute_103a``/``sm_103a``
-only; the quantisation kernels additionally with ``-fmad=false`` (their
+only; the units with transform arithmetic (the quantisation kernels and the
+GEMM, whose epilogue can encode MXFP4) additionally with ``-fmad=false`` (their
 arithmetic must not be contracted into FMAs).  The CUDA runtime is linked
 statically and the driver API is reached through the runtime's entry-point
 query, so the library loads on machines without a GPU driver (for symbol and
@@ -26,14 +27,14 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 UNITS = {
     "quant.cu": ["-fmad=false"],
-    "gemm.cu": [],
+    "gemm.cu": ["-fmad=false"],
     "api.cu": [],
     "static_scratch.cu": [],
     "w4a16.cu": [],
     "flip.cu": ["-fmad=false"],
     "moe.cu": ["-fmad=false"],
 }
-HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh", "mx_block.cuh"]
 
 
 def _mtime(path: str) -> float:

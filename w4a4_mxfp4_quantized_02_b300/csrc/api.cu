@@ -584,6 +584,59 @@ macaq_status macaq_grouped_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_sc
     return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
+macaq_status macaq_interleave_gate_up(const void *W_gu, int64_t E, int64_t F, int64_t K, void *W_out,
+                                      macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(F));
+    if (E < 0 || F % 64 != 0) return MACAQ_ERR_INVALID_ARG;
+    if (E == 0 || F == 0) return MACAQ_OK;
+    if (E * 2 * F > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (!W_gu || !W_out || W_gu == W_out) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(W_gu) || !aligned16(W_out)) return MACAQ_ERR_ALIGNMENT;
+    return from_cuda(launch_interleave_gate_up(static_cast<const uint16_t *>(W_gu), E, F, K,
+                                               static_cast<uint16_t *>(W_out), static_cast<cudaStream_t>(stream)));
+}
+
+macaq_status macaq_grouped_w4a4_gemm_swiglu(const uint8_t *a_codes, const uint8_t *a_scales,
+                                            const uint8_t *w_codes, const uint8_t *w_scales,
+                                            const int32_t *expert_offsets, int64_t rows, int64_t E, int64_t F,
+                                            int64_t K, const float *inv_s, int64_t hadamard_block,
+                                            uint8_t *h_codes, uint8_t *h_scales, macaq_stream_t stream)
+{
+    MACAQ_TRY(check_k(K));
+    MACAQ_TRY(check_rows(rows));
+    MACAQ_TRY(check_rows(F));
+    if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
+    if (E <= 0 || F % 64 != 0) return MACAQ_ERR_INVALID_ARG;
+    if (E > kMaxExperts) return MACAQ_ERR_UNSUPPORTED;
+    if (grouped_padded_rows(rows, E) > kMaxDim || E * 2 * F > kMaxDim) return MACAQ_ERR_UNSUPPORTED;
+    if (rows == 0 || F == 0) return MACAQ_OK;
+    if (!a_codes || !a_scales || !w_codes || !w_scales || !expert_offsets || !inv_s || !h_codes || !h_scales)
+        return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) ||
+        !aligned16(inv_s) || !aligned16(h_codes) || !aligned16(h_scales))
+        return MACAQ_ERR_ALIGNMENT;
+    GemmArgs g{};
+    g.a_codes = a_codes;
+    g.a_scales = a_scales;
+    g.w_codes = w_codes;
+    g.w_scales = w_scales;
+    g.offsets = expert_offsets;
+    g.M = rows;
+    g.a_rows = grouped_padded_rows(rows, E);
+    g.N = 2 * F;
+    g.K = K;
+    g.E = static_cast<int32_t>(E);
+    g.Y = nullptr;
+    g.ldy = 0;
+    g.epi = hadamard_block == 64 ? 2 : 1;
+    g.h_codes = h_codes;
+    g.h_scales = h_scales;
+    g.h_f = inv_s;
+    return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
 macaq_status macaq_moe_combine(const void *Y, int64_t ldy, int64_t y_rows, const int32_t *tok_rows,
                                const float *tok_weights, int64_t T, int64_t topk, int64_t N, void *out,
                                int64_t ldo, macaq_stream_t stream)

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "mx_block.cuh"
 #include "ptx.cuh"
 
 #ifndef MACAQ_TRACE
@@ -81,6 +82,14 @@ struct Params {
     int32_t num_full;        // whole 256-column tiles run first ...
     int32_t num_split;       // ... then the last num_split tiles as two 128-column halves
     int32_t n_fastest;       // tile order: column blocks fastest (else row-pair blocks)
+    // EPI != 0 (grouped gate+up with interleaved weight rows): the epilogue
+    // writes the down projection's input h = SiLU(g) * u as MXFP4 instead of Y
+    uint8_t *h_codes;        // [P, F/2], padded rows
+    uint8_t *h_scales;       // tiled for P rows of F channels
+    const float *h_f;        // down balance factors [E, F]
+    int32_t F;
+    int32_t h_nka;           // scale atoms per 128-row block of the down input
+    int32_t h_pad_cols;      // padded scale columns of F
 };
 
 struct Tile {
@@ -190,7 +199,19 @@ struct PairLayout {
 // a multiple of 128 of the padded layout, sorted rows in Y), B is [E, N, K/2].
 // A pair tile is two consecutive 128-row blocks of one expert's rows; a rank
 // whose block lies past its expert's rows computes nothing that is stored.
-template <int STAGES, bool GROUPED>
+//
+// EPI (grouped only): 0 stores bf16 Y; 1 and 2 are the gate+up projection of
+// a gated MLP whose weight rows come interleaved in chunks of 64 channels
+// (tile columns 128c .. 128c+63 are gate rows 64c .., the next 64 up rows of
+// the same channels).  Each epilogue warp then holds gate and up of 64
+// channels for its 32 rows, and each thread, owning one row, forms
+// h = bf16(SiLU(bf16(g)) * bf16(u)) -- the values the unfused layer would
+// store and re-read -- and runs the down input's transform on it in its own
+// registers: balance with the expert's down factors, 32-point butterflies
+// (EPI 1) or the 64-channel block (EPI 2), E8M0 scale, E2M1 codes, written to
+// the down input's padded rows.  Padding rows of an expert's last block get
+// zero scales; a block past the expert's rows writes nothing.
+template <int STAGES, bool GROUPED, int EPI = 0>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmY,
@@ -504,6 +525,64 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (warp == EPI_WARP0) MACAQ_TRACE(8, tc);
 
             const int row0 = 32 * q;
+            if constexpr (EPI != 0) {
+                if (ti.rows_valid <= 0 || half * 128 >= ti.ncols) continue;
+                const int32_t c0 = ((ti.n0 + half * 128) >> 7) * 64;  // this warp's 64 channels
+                if (c0 >= p.F) continue;
+                const int r = row0 + lane;
+                const int64_t prow = static_cast<int64_t>(ti.a_row) + r;
+                uint32_t sw = 0;
+                if (r < ti.rows_valid) {
+                    uint32_t hlo[16], hhi[16];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int gc = 2 * i, uc = 64 + 2 * i;
+                        const __nv_bfloat162 gb = __floats2bfloat162_rn(__uint_as_float(acc[gc >> 5][gc & 31]),
+                                                                        __uint_as_float(acc[gc >> 5][(gc & 31) + 1]));
+                        const __nv_bfloat162 ub = __floats2bfloat162_rn(__uint_as_float(acc[uc >> 5][uc & 31]),
+                                                                        __uint_as_float(acc[uc >> 5][(uc & 31) + 1]));
+                        const uint32_t hw = mx::silu_mul_word(*reinterpret_cast<const uint32_t *>(&gb),
+                                                              *reinterpret_cast<const uint32_t *>(&ub));
+                        if (i < 16) hlo[i] = hw; else hhi[i - 16] = hw;
+                    }
+                    const float4 *f4 = reinterpret_cast<const float4 *>(
+                        p.h_f + static_cast<int64_t>(ti.expert) * p.F + c0);
+                    float2 flo[16], fhi[16];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 a4 = __ldg(f4 + j);
+                        const float4 b4 = __ldg(f4 + 8 + j);
+                        flo[2 * j] = make_float2(a4.x, a4.y);
+                        flo[2 * j + 1] = make_float2(a4.z, a4.w);
+                        fhi[2 * j] = make_float2(b4.x, b4.y);
+                        fhi[2 * j + 1] = make_float2(b4.z, b4.w);
+                    }
+                    uint4 clo, chi;
+                    uint32_t slo, shi;
+                    if constexpr (EPI == 1) {
+                        slo = mx::quant_block_pairs<false>(hlo, flo, clo);
+                        shi = mx::quant_block_pairs<false>(hhi, fhi, chi);
+                    } else {
+                        mx::quant_block64_pairs(hlo, hhi, flo, fhi, clo, chi, slo, shi);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.h_codes + prow * (p.F / 2) + c0 / 2);
+                    dst[0] = clo;
+                    dst[1] = chi;
+                    sw = slo | (shi << 8);
+                }
+                // the row's two scale bytes (zero on padding rows), and on the
+                // last chunk the row's padding scale columns
+                const int64_t rb = (prow >> 7) * p.h_nka;
+                const int64_t in_atom = (prow & 31) * 16 + ((prow & 127) >> 5) * 4;
+                const int32_t kb0 = c0 / 32;
+                *reinterpret_cast<uint16_t *>(p.h_scales + (rb + (kb0 >> 2)) * 512 + in_atom + (kb0 & 3)) =
+                    static_cast<uint16_t>(sw);
+                if (c0 + 64 == p.F) {
+                    for (int32_t kb = kb0 + 2; kb < p.h_pad_cols; ++kb)
+                        p.h_scales[(rb + (kb >> 2)) * 512 + in_atom + (kb & 3)] = 0;
+                }
+                continue;
+            }
             const bool any_row = row0 < ti.rows_valid;
             if (!any_row || half * 128 >= ti.ncols) continue;
             // Grouped: rows past an expert's last row belong to the next expert
@@ -709,13 +788,13 @@ bool encode_4d(CUtensorMap *m, const void *base, const uint64_t *dims, const uin
 
 struct DeviceInfo {
     int sms = 0;
-    bool attr_set[8] = {false, false, false, false, false, false, false, false};
+    bool attr_set[16] = {};
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
 
-// Dense (GROUPED = false) or expert-grouped GEMM on CTA pairs.
-template <int STAGES, bool GROUPED>
+// Dense (GROUPED = false) or expert-grouped GEMM on CTA pairs; EPI as the kernel.
+template <int STAGES, bool GROUPED, int EPI = 0>
 cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
 {
     using L = PairLayout<STAGES>;
@@ -725,7 +804,7 @@ cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kern = gemm_mxf4_pair_kernel<STAGES, GROUPED>;
+    auto kern = gemm_mxf4_pair_kernel<STAGES, GROUPED, EPI>;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         DeviceInfo &di = g_dev[dev];
@@ -769,13 +848,15 @@ cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
                 return cudaErrorInvalidValue;
         }
     }
-    {
+    if (EPI == 0) {
         uint64_t dims[2] = {static_cast<uint64_t>(g.N), static_cast<uint64_t>(g.M)};
         uint64_t strides[1] = {static_cast<uint64_t>(g.ldy) * 2};
         uint32_t box[2] = {16, 32};
         if (!encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.Y, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_32B))
             return cudaErrorInvalidValue;
+    } else {
+        std::memset(&tmY, 0, sizeof(tmY));  // no bf16 output: never read
     }
     // Scale blocks: the tiled layout viewed as (256 B, 2 halves of a 512-byte
     // atom, k atom, 128-row block); grouped weights: the experts' tiled arrays
@@ -803,6 +884,12 @@ cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
     p.num_kstages = static_cast<int32_t>((g.K + 2 * KB - 1) / (2 * KB));
     p.num_nb = static_cast<int32_t>((g.N + BN - 1) / BN);
     p.n_rb = static_cast<int32_t>((g.N + 127) / 128);
+    p.h_codes = g.h_codes;
+    p.h_scales = g.h_scales;
+    p.h_f = g.h_f;
+    p.F = static_cast<int32_t>(g.N / 2);
+    p.h_nka = static_cast<int32_t>(pad_scale_cols(g.N / 2) / 4);
+    p.h_pad_cols = static_cast<int32_t>(pad_scale_cols(g.N / 2));
     // column blocks fastest when A would not stay in L2 across a pass over
     // the column blocks: grouped A (each expert's rows then meet all of its
     // weight tiles in a row, so an expert's weight tile is read once for both
@@ -962,6 +1049,8 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     if (g.E == 0 && g.M <= 32) return launch_skinny<32, 5>(g, stream, 5);
     if (g.E == 0 && g.M <= 64) return launch_skinny<64, 4>(g, stream, 6);
     // everything else: CTA pairs on 256 x 256 tiles (grouped: per-expert B)
+    if (g.E > 0 && g.epi == 1) return launch_pair<6, true, 1>(g, stream, 0);
+    if (g.E > 0 && g.epi == 2) return launch_pair<6, true, 2>(g, stream, 1);
     if (g.E > 0) return launch_pair<6, true>(g, stream, 7);
     return launch_pair<6, false>(g, stream, 3);
 }

@@ -75,6 +75,11 @@ cudaError_t launch_moe_combine(const uint16_t *Y, int64_t ldy, int64_t y_rows, c
                                const float *w, int64_t T, int64_t topk, int64_t N, uint16_t *out, int64_t ldo,
                                cudaStream_t stream);
 
+// W_gu [E, 2F, K] bf16 -> rows interleaved in chunks of 64 channels (gate
+// then up), the layout the fused gate+up GEMM epilogue reads.
+cudaError_t launch_interleave_gate_up(const uint16_t *w, int64_t E, int64_t F, int64_t K, uint16_t *out,
+                                      cudaStream_t stream);
+
 cudaError_t launch_balance(const uint16_t *xc, int64_t ldxc, const int32_t *xc_rows, int64_t mc,
                            const uint16_t *w, int64_t n, int64_t k, float *s, float *inv_s,
                            cudaStream_t stream);
@@ -93,6 +98,13 @@ struct GemmArgs {
     int32_t E;               // 0 = dense
     void *Y;
     int64_t ldy;
+    // grouped gate+up with interleaved weight rows (N = 2F): epi 1 / 2 write
+    // the down input h = SiLU(g) * u as MXFP4 (Hadamard block 32 / 64) into
+    // h_codes / h_scales with the down balance factors h_f [E, F]; Y unused
+    int32_t epi = 0;
+    uint8_t *h_codes = nullptr;
+    uint8_t *h_scales = nullptr;
+    const float *h_f = nullptr;
 };
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);

@@ -101,4 +101,37 @@ cudaError_t launch_moe_combine(const uint16_t *Y, int64_t ldy, int64_t y_rows, c
     return cudaGetLastError();
 }
 
+// ------------------------------------------------ gate/up row interleave
+//
+// Weight preparation for the fused gate+up epilogue: W_gu [E, 2F, K] (gate
+// rows 0 .. F-1, up rows F .. 2F-1 of each expert) -> W_out [E, 2F, K] with
+// output row 128c + j = gate row 64c + j and output row 128c + 64 + j = up
+// row 64c + j (j < 64), so that every 128 output rows hold gate and up of the
+// same 64 channels.  A row copy per warp (16-byte loads and stores).
+namespace {
+
+__global__ void __launch_bounds__(256) interleave_gate_up_kernel(const uint4 *w, int64_t E, int64_t F,
+                                                                 int64_t k16, uint4 *out)
+{
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= E * 2 * F) return;
+    const int64_t e = row / (2 * F), n = row - e * 2 * F;
+    const int64_t c = n >> 7, j = n & 127;
+    const int64_t src = (j < 64) ? 64 * c + j : F + 64 * c + (j - 64);
+    const uint4 *s = w + (e * 2 * F + src) * k16;
+    uint4 *d = out + row * k16;
+    for (int64_t i = threadIdx.x & 31; i < k16; i += 32) d[i] = s[i];
+}
+
+}  // namespace
+
+cudaError_t launch_interleave_gate_up(const uint16_t *w, int64_t E, int64_t F, int64_t K, uint16_t *out,
+                                      cudaStream_t stream)
+{
+    const int64_t rows = E * 2 * F;
+    interleave_gate_up_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(w), E, F, K / 8, reinterpret_cast<uint4 *>(out));
+    return cudaGetLastError();
+}
+
 }  // namespace macaq

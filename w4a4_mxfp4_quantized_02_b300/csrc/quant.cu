@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "mx_block.cuh"
 #include "ptx.cuh"
 
 namespace macaq {
@@ -35,6 +36,8 @@ namespace macaq {
 __device__ unsigned int g_quant_error_flags;
 
 namespace {
+
+using namespace mx;
 
 constexpr uint64_t kQuantWaitNs = 2000000000ull;
 
@@ -50,36 +53,6 @@ __device__ __forceinline__ bool quant_wait(uint32_t bar, uint32_t parity)
             return false;
         }
     }
-}
-
-// fp32 nearest to 2^-2.5 = 1/sqrt(32).
-constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// Two fp32 -> one byte of two E2M1 codes (lo in bits 0..3, hi in bits 4..7),
-// round to nearest even, saturating.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
-{
-#ifdef MACAQ_SOFT_E2M1
-    auto enc = [](float t) -> uint32_t {
-        const uint32_t s = (__float_as_uint(t) >> 31) << 3;
-        const float a = fabsf(t);
-        uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-                     (a >= 3.5f) + (a > 5.0f);
-        return s | m;
-    };
-    return enc(lo) | (enc(hi) << 4);
-#else
-    uint16_t r;
-    asm("{\n\t.reg .b8 t;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-        "cvt.u16.u8 %0, t;\n\t}"
-        : "=h"(r)
-        : "f"(hi), "f"(lo));
-    return r;
-#endif
 }
 
 // Packed fp32x2 multiply / add / subtract, each lane rounded to nearest even.
@@ -418,181 +391,6 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
 
 
 // ------------------------------------------------ TMA-staged dense variant
-
-// ------------------------------------------------------------- SwiGLU step
-//
-// h = bf16( SiLU(g) * u ), SiLU(g) = g / (1 + e^-g), in fp32 with one round
-// to nearest per operation (the file is built with -fmad=false and every
-// fused multiply-add is explicit).  e^x: Cody-Waite range reduction
-// x = n ln2 + r (ln2 split into a 16-bit head, so n * head is exact, and a
-// tail; both steps fused multiply-adds), the Taylor series of e^r to r^8 / 8!
-// by Horner with fused multiply-adds (|r| <= 0.35, truncation below 2^-30
-// relative), then the scaling by 2^n, in two steps where 2^n is not a normal
-// float.  The two elements of a bf16 word go through the polynomial as one
-// packed pair.
-__device__ __forceinline__ float pow2i(int k)  // 2^k, -126 <= k <= 127
-{
-    return __int_as_float((k + 127) << 23);
-}
-
-// e^x of one element from its reduced-range polynomial value q and n: the
-// case analysis (inf above the largest argument, 0 below the smallest, the
-// scaling by 2^n in two steps outside the normal range) with selects instead
-// of branches, so that independent elements interleave
-__device__ __forceinline__ float exp_finish(float x, float q, int n)
-{
-    // n > 127: (q 2^127) 2^(n-127); n < -126: (q 2^(n+100)) 2^-100; else q 2^n (x 1)
-    const int n1 = n < -126 ? n + 100 : (n > 127 ? 127 : n);
-    const float y = __fmul_rn(__fmul_rn(q, pow2i(n1)), pow2i(n - n1));
-    return x > 88.72283935546875f ? __int_as_float(0x7f800000) : (x < -103.972084045410156f ? 0.0f : y);
-}
-
-__device__ __forceinline__ float2 exp_f32x2(float2 x)
-{
-    // arguments outside [-104, 89] give inf or 0 above; clamping keeps n in range
-    const float2 xc = make_float2(fminf(fmaxf(x.x, -104.0f), 89.0f), fminf(fmaxf(x.y, -104.0f), 89.0f));
-    const float2 t = __fmul2_rn(xc, make_float2(0x1.715476p+0f, 0x1.715476p+0f));
-    const float2 fn = make_float2(rintf(t.x), rintf(t.y));
-    const float2 nfn = make_float2(-fn.x, -fn.y);
-    float2 r = __ffma2_rn(nfn, make_float2(0x1.62e4p-1f, 0x1.62e4p-1f), xc);
-    r = __ffma2_rn(nfn, make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f), r);
-    float2 q = make_float2(0x1.a01a02p-16f, 0x1.a01a02p-16f);
-    q = __ffma2_rn(q, r, make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f));
-    q = __ffma2_rn(q, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
-    q = __ffma2_rn(q, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
-    q = __ffma2_rn(q, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
-    q = __ffma2_rn(q, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
-    q = __ffma2_rn(q, r, make_float2(0x1.0p-1f, 0x1.0p-1f));
-    q = __ffma2_rn(q, r, make_float2(0x1.0p+0f, 0x1.0p+0f));
-    q = __ffma2_rn(q, r, make_float2(0x1.0p+0f, 0x1.0p+0f));
-    return make_float2(exp_finish(x.x, q.x, static_cast<int>(fn.x)), exp_finish(x.y, q.y, static_cast<int>(fn.y)));
-}
-
-// Two bf16 words of gate and up values -> the word of the two h values
-// (element 2i in the low half).
-__device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
-{
-    const float2 g = make_float2(bf16lo(gw), bf16hi(gw));
-    const float2 e = exp_f32x2(make_float2(-g.x, -g.y));
-    const float sx = __fdiv_rn(g.x, __fadd_rn(1.0f, e.x));
-    const float sy = __fdiv_rn(g.y, __fadd_rn(1.0f, e.y));
-    const float2 p = __fmul2_rn(make_float2(sx, sy), make_float2(bf16lo(uw), bf16hi(uw)));
-    const __nv_bfloat162 h = __floats2bfloat162_rn(p.x, p.y);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// The same transform as quant_block with the natural register pairing
-// v[i] = (element 2i, element 2i+1): the stride-1 stage (fed by products, so
-// scalar) pairs the halves of a register, strides 2, 4, 8, 16 pair whole
-// registers i and i + h/2 and run as packed adds; the bf16 words and the
-// output bytes already come in this pairing.
-//
-// kH64: the block is one half of a 64-channel Hadamard block whose other half
-// is held by the neighbouring lane (lane ^ 1; the even lane holds the lower
-// half).  After the five 32-point stages the stride-32 stage pairs element i
-// of the two halves through a shuffle, and the normalisation is the exact
-// 1/8; the MX block stays these 32 values.
-template <bool kH64>
-__device__ __forceinline__ void hadamard_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
-                                                     float2 (&v)[16])
-{
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        // one packed multiply for the pair; the stride-1 stage that consumes it
-        // is scalar, so no packed add follows a packed multiply here
-        const float2 ab = __fmul2_rn(make_float2(bf16lo(raw[i]), bf16hi(raw[i])), f[i]);
-        v[i] = make_float2(__fadd_rn(ab.x, ab.y), __fsub_rn(ab.x, ab.y));
-    }
-#pragma unroll
-    for (int hh = 1; hh < 16; hh <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i & hh) continue;
-            const float2 a = v[i];
-            const float2 b = v[i + hh];
-            // sums of sums: no multiply feeds these adds, so the packed
-            // intrinsics cannot be contracted into an FMA
-            v[i] = __fadd2_rn(a, b);
-            v[i + hh] = __fadd2_rn(a, make_float2(-b.x, -b.y));
-        }
-    }
-    if (kH64) {
-        const unsigned mask = __activemask();
-        // lower half: own + partner; upper half: partner - own.  As p + sgn * v
-        // with sgn = +-1 the product is exact, so one fused multiply-add gives
-        // exactly the rounded sum or difference.
-        const float sgn = (threadIdx.x & 1u) ? -1.0f : 1.0f;
-        const float2 sgn2 = make_float2(sgn, sgn);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float2 p = make_float2(__shfl_xor_sync(mask, v[i].x, 1), __shfl_xor_sync(mask, v[i].y, 1));
-            v[i] = __ffma2_rn(sgn2, v[i], p);
-        }
-    }
-}
-
-// The W4A16 activation: the normalised transform rounded once to bf16
-// (element 2i in the low half of word i).
-template <bool kH64>
-__device__ __forceinline__ void bf16_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
-                                                 uint32_t (&out)[16])
-{
-    constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
-    float2 v[16];
-    hadamard_block_pairs<kH64>(raw, f, v);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float2 y = __fmul2_rn(v[i], make_float2(kNorm, kNorm));
-        const __nv_bfloat162 b = __floats2bfloat162_rn(y.x, y.y);
-        out[i] = *reinterpret_cast<const uint32_t *>(&b);
-    }
-}
-
-template <bool kH64>
-__device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
-                                                      uint4 &codes)
-{
-    constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
-    float2 v[16];
-    hadamard_block_pairs<kH64>(raw, f, v);
-    float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        m0 = fmaxf(m0, fabsf(v[i].x));
-        m1 = fmaxf(m1, fabsf(v[i].y));
-    }
-    const float vmax = fmaxf(m0, m1);
-    const float amax = __fmul_rn(vmax, kNorm);
-    const int ef = static_cast<int>(__float_as_uint(amax) >> 23);
-    const uint32_t sbyte = static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
-    const int se = static_cast<int>(sbyte) - 127;
-    if (se >= -124 && se <= 122) {
-        const float g = __int_as_float(__float_as_int(kNorm) - se * (1 << 23));
-        const float2 g2 = make_float2(g, g);
-        // the scaled values feed only the encoder: no add follows this multiply
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __fmul2_rn(v[i], g2);
-    } else {
-        const float c = kNorm;
-        const float inv = __uint_as_float((254u - sbyte) << 23);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            v[i] = __fmul2_rn(v[i], make_float2(c, c));
-            v[i] = __fmul2_rn(v[i], make_float2(inv, inv));
-        }
-    }
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t b0 = e2m1x2(v[4 * q].x, v[4 * q].y);
-        const uint32_t b1 = e2m1x2(v[4 * q + 1].x, v[4 * q + 1].y);
-        const uint32_t b2 = e2m1x2(v[4 * q + 2].x, v[4 * q + 2].y);
-        const uint32_t b3 = e2m1x2(v[4 * q + 3].x, v[4 * q + 3].y);
-        w[q] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
-    }
-    codes = make_uint4(w[0], w[1], w[2], w[3]);
-    return sbyte;
-}
 
 // Dense rows through a TMA ring.  X is viewed as [rows][blocks][32 values];
 // one box per stage brings RT rows x TB blocks (64 bytes each, 64-byte
