@@ -328,38 +328,38 @@ macaq_status macaq_transform_act_bf16(const void *X, int64_t ldx, const float *i
                                       int64_t K, int64_t hadamard_block, void *Xt, int64_t ldxt,
                                       macaq_stream_t stream);
 
-/* Weight expansion: Wd[n, k] = the MXFP4 value (E2M1 code times 2^(scale -
- * 127)) as bf16, exact for every scale an fp32 input can produce.  w_codes
- * [N, K/2] and tiled w_scales as macaq_quant_weight writes them; Wd bf16
- * [N, K] (row pitch K), 16-byte aligned. */
+/* Weight expansion on its own: Wd[n, k] = the MXFP4 value (E2M1 code times
+ * 2^(scale - 127)) as bf16, exact for every scale an fp32 input can produce.
+ * w_codes [N, K/2] and tiled w_scales as macaq_quant_weight writes them; Wd
+ * bf16 [N, K] (row pitch K), 16-byte aligned.  The W4A16 GEMM below does
+ * not need it (it expands tiles on chip); it is the checkpoint's bf16 form
+ * for callers that want one. */
 macaq_status macaq_dequant_weight_bf16(const uint8_t *w_codes, const uint8_t *w_scales, int64_t N,
                                        int64_t K, void *Wd, macaq_stream_t stream);
 
-/* The W4A16 GEMM alone: Y[m, n] = bf16_rn( sum_k Xt(m, k) * Wd(n, k) ), fp32
- * accumulation, a plain bf16 library GEMM (cuBLASLt; its algorithm is chosen
- * once per shape and workspace size and cached).  Xt bf16 [M, ldxt]; Wd bf16
- * [N, K] row pitch K; Y bf16 [M, ldy]; ldxt and ldy multiples of 8.
- * workspace: device scratch of ws_bytes bytes (256-byte aligned; may be
- * NULL with ws_bytes 0).  MACAQ_ERR_UNSUPPORTED if the library offers no
- * algorithm for the shape within ws_bytes. */
-macaq_status macaq_w4a16_gemm(const void *Xt, int64_t ldxt, const void *Wd, int64_t M, int64_t N,
-                              int64_t K, void *Y, int64_t ldy, void *workspace, size_t ws_bytes,
-                              macaq_stream_t stream);
+/* The W4A16 GEMM: Y[m, n] = bf16_rn( sum_k Xt(m, k) * Wd(n, k) ), Wd(n, k) the
+ * bf16 value of the MXFP4 weight (as macaq_dequant_weight_bf16), expanded
+ * tile by tile in shared memory so the weight is read at 4.25 bits per
+ * value; bf16 products accumulated in fp32 on the tensor cores.  Xt bf16
+ * [M, ldxt] (ldxt >= K); w_codes [N, K/2] and tiled w_scales from
+ * macaq_quant_weight(_hb); Y bf16 [M, ldy] (ldy >= N); ldxt and ldy
+ * multiples of 8, pointers 16-byte aligned. */
+macaq_status macaq_w4a16_gemm(const void *Xt, int64_t ldxt, const uint8_t *w_codes, const uint8_t *w_scales,
+                              int64_t M, int64_t N, int64_t K, void *Y, int64_t ldy, macaq_stream_t stream);
 
-/* Workspace bytes macaq_w4a16_linear needs for M rows of K channels: the bf16
- * transform plus the GEMM's scratch. */
+/* Workspace bytes macaq_w4a16_linear needs for M rows of K channels (the
+ * bf16 transform of the activations). */
 size_t macaq_w4a16_linear_workspace_bytes(int64_t M, int64_t K);
 
 /* The W4A16 layer: macaq_transform_act_bf16 into `workspace`, then
- *   Y[m, n] = bf16_rn( sum_k Xt(m, k) * Wd(n, k) )  (fp32 accumulation)
- * with macaq_w4a16_gemm, both on `stream`.  Wd bf16 [N, K] from
- * macaq_dequant_weight_bf16 (the same hadamard_block as the weights were
- * prepared with); Y bf16 [M, ldy], ldy >= N, a multiple of 8; workspace as
- * macaq_linear (256-byte aligned, ws_bytes >=
- * macaq_w4a16_linear_workspace_bytes(M, K)); errors as macaq_w4a16_gemm. */
-macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, const void *Wd,
-                                int64_t M, int64_t N, int64_t K, int64_t hadamard_block, void *Y,
-                                int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream);
+ * macaq_w4a16_gemm, both on `stream`.  w_codes / w_scales prepared with the
+ * same hadamard_block; Y bf16 [M, ldy], ldy >= N, a multiple of 8; workspace
+ * as macaq_linear (256-byte aligned, ws_bytes >=
+ * macaq_w4a16_linear_workspace_bytes(M, K)). */
+macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, const uint8_t *w_codes,
+                                const uint8_t *w_scales, int64_t M, int64_t N, int64_t K,
+                                int64_t hadamard_block, void *Y, int64_t ldy, void *workspace, size_t ws_bytes,
+                                macaq_stream_t stream);
 
 /* --------------------------------------------- Flip Refinement (offline) */
 

@@ -198,12 +198,18 @@ def test_w4a16_rejections(L):
     assert d(p, p, 4, 128, _fake(0x10008), None) == ALIGN
     assert d(p, p, 0, 128, p, None) == OK
     need = mq.macaq_w4a16_linear_workspace_bytes(16, 128)
-    assert need == 16 * 128 * 2 + (32 << 20)
-    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, None, need, None) == WORKSPACE
-    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, p, need - 1, None) == WORKSPACE
-    assert f(p, 128, p, p, 16, 64, 128, 32, p, 64, _fake(0x10010), need, None) == ALIGN
-    assert f(p, 128, p, p, 16, 64, 128, 32, p, 32, p, need, None) == INVALID   # ldy < N
-    assert f(p, 96, p, p, 16, 64, 96, 64, p, 64, p, need, None) == INVALID     # K % 64
+    assert need == 16 * 128 * 2
+    assert f(p, 128, p, p, p, 16, 64, 128, 32, p, 64, None, need, None) == WORKSPACE
+    assert f(p, 128, p, p, p, 16, 64, 128, 32, p, 64, p, need - 1, None) == WORKSPACE
+    assert f(p, 128, p, p, p, 16, 64, 128, 32, p, 64, _fake(0x10010), need, None) == ALIGN
+    assert f(p, 128, p, p, p, 16, 64, 128, 32, p, 32, p, need, None) == INVALID   # ldy < N
+    assert f(p, 96, p, p, p, 16, 64, 96, 64, p, 64, p, need, None) == INVALID     # K % 64
+    g = L.macaq_w4a16_gemm
+    assert g(p, 128, p, p, 16, 64, 100, p, 64, None) == INVALID                 # K % 32
+    assert g(p, 128, p, None, 16, 64, 128, p, 64, None) == INVALID              # no scales
+    assert g(p, 128, p, _fake(0x10008), 16, 64, 128, p, 64, None) == ALIGN
+    assert g(p, 132, p, p, 16, 64, 128, p, 64, None) == ALIGN                   # ldxt % 8
+    assert g(p, 128, p, p, 0, 64, 128, p, 64, None) == OK                       # M = 0
 
 
 def test_flip_rejections(L):

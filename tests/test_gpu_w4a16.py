@@ -3,8 +3,9 @@ and Avoiding Setup Mistakes", section "vLLM checkpoints have different
 constraints": the weight-only mode expands the weights for a BF16 matmul).
 
 The bf16 activation transform and the bf16 weight expansion are bit-exact
-against the oracle; the layer output is within the GEMM criterion of the
-oracle's fp64 product of those two bf16 operands.
+against the oracle; the layer output -- the GEMM reading the MXFP4 weight and
+expanding it to bf16 on chip -- is within the GEMM criterion of the oracle's
+fp64 product of those two bf16 operands.
 """
 import numpy as np
 import pytest
@@ -78,11 +79,11 @@ def test_w4a16_linear(name, hb):
     else:
         s_ref, inv_ref = oracle.balance_scales(d["X_calib"], d["W"])
         cw, sw = oracle.quantize(d["W"], s_ref, hb=64)
-    # the checkpoint as the weight kernel writes it, then the bf16 expansion
+    # the checkpoint as the weight kernel writes it; the bf16 expansion on its own
     w_codes, w_scales = mq.macaq_quant_weight_hb(to_dev(d["W"]), torch.from_numpy(s_ref).to(DEV), hb)
     Wd = mq.macaq_dequant_weight_bf16(w_codes, w_scales, wl.N, wl.K)
     X = to_dev(d["X"])
-    Y = mq.macaq_w4a16_linear(X, torch.from_numpy(inv_ref).to(DEV), Wd, hb)
+    Y = mq.macaq_w4a16_linear(X, torch.from_numpy(inv_ref).to(DEV), w_codes, w_scales, wl.N, hb)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(u8(w_codes), cw)
     wd_ref = oracle.dequant_bf16(cw, sw)
@@ -103,9 +104,8 @@ def test_w4a16_linear_padded_pitches():
     s = np.random.default_rng(1).uniform(0.5, 2.0, K).astype(np.float32)
     inv = (1.0 / s.astype(np.float64)).astype(np.float32)
     w_codes, w_scales = mq.macaq_quant_weight(to_dev(W), torch.from_numpy(s).to(DEV))
-    Wd = mq.macaq_dequant_weight_bf16(w_codes, w_scales, N, K)
     Y = torch.full((M, N + 8), 5.0, dtype=torch.bfloat16, device=DEV)
-    mq.macaq_w4a16_linear(to_dev(X)[:, :K], torch.from_numpy(inv).to(DEV), Wd, 32, Y=Y[:, :N])
+    mq.macaq_w4a16_linear(to_dev(X)[:, :K], torch.from_numpy(inv).to(DEV), w_codes, w_scales, N, 32, Y=Y[:, :N])
     torch.cuda.synchronize()
     cw, sw = oracle.quantize(W, s)
     a = bits_to_f64(oracle.transform_bf16(X[:, :K].contiguous(), inv))
@@ -115,14 +115,24 @@ def test_w4a16_linear_padded_pitches():
     assert np.all(got[:, N:] == 5.0)
 
 
-@pytest.mark.parametrize("M,N,K,ws", [(1, 64, 4096, 0), (33, 200, 160, 1 << 20), (256, 512, 1024, 32 << 20)])
-def test_w4a16_gemm_alone(M, N, K, ws):
-    """The bf16 GEMM entry on its own, with and without scratch."""
+@pytest.mark.parametrize("M,N,K", [(1, 64, 4096), (16, 128, 64), (33, 200, 160), (64, 384, 2048),
+                                   (100, 136, 96), (256, 512, 1024), (300, 1000, 5120)])
+def test_w4a16_gemm_alone(M, N, K):
+    """The W4A16 GEMM entry on its own: bf16 activations against MXFP4 weights
+    covering every code byte and a wide range of scales (including the
+    subnormal scale 0), every token tile size, ragged M, N and a K with a
+    half-filled last stage."""
     rng = np.random.default_rng(M + N + K)
     a = torch.from_numpy(rng.normal(0, 1, (M, K)).astype(np.float32)).to(torch.bfloat16)
-    w = torch.from_numpy(rng.normal(0, 1, (N, K)).astype(np.float32)).to(torch.bfloat16)
-    work = torch.empty(ws, dtype=torch.uint8, device=DEV) if ws else None
-    Y = mq.macaq_w4a16_gemm(a.to(DEV), w.to(DEV), workspace=work)
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    codes.flat[:min(256, codes.size)] = np.arange(min(256, codes.size), dtype=np.uint8)
+    scales = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+    scales.flat[0] = 0
+    scales.flat[-1] = 200
+    Y = mq.macaq_w4a16_gemm(a.to(DEV), torch.from_numpy(codes).to(DEV),
+                            torch.from_numpy(oracle.tile_scales(scales)).to(DEV), N)
     torch.cuda.synchronize()
-    a64, w64 = a.double().numpy(), w.double().numpy()
+    assert mq.macaq_check_device_error() == 0
+    a64 = bits_to_f64(a.view(torch.int16).numpy().view(np.uint16))
+    w64 = bits_to_f64(oracle.dequant_bf16(codes, scales))
     check_gemm(Y.float().cpu().numpy().astype(np.float64), a64 @ w64.T, np.abs(a64) @ np.abs(w64).T, K)

@@ -63,8 +63,8 @@ _SIGS = {
     "macaq_transform_act_bf16": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_dequant_weight_bf16": ([_P, _P, _I64, _I64, _P, _P], ctypes.c_int),
     "macaq_w4a16_linear_workspace_bytes": ([_I64, _I64], _SZ),
-    "macaq_w4a16_gemm": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P], ctypes.c_int),
-    "macaq_w4a16_linear": ([_P, _I64, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
+    "macaq_w4a16_gemm": ([_P, _I64, _P, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "macaq_w4a16_linear": ([_P, _I64, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64, _P, _SZ, _P],
                            ctypes.c_int),
     "macaq_transform_f32": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
     "macaq_flip_hessian": ([_P, _I64, _I64, ctypes.c_float, _P, _P], ctypes.c_int),
@@ -330,19 +330,16 @@ def macaq_dequant_weight_bf16(w_codes: torch.Tensor, w_scales: torch.Tensor, N: 
     return Wd
 
 
-def macaq_w4a16_gemm(Xt: torch.Tensor, Wd: torch.Tensor, Y=None, workspace=None, stream=None):
-    """Y = Xt . Wd^T in bf16 (fp32 accumulation): the W4A16 GEMM alone."""
+def macaq_w4a16_gemm(Xt: torch.Tensor, w_codes: torch.Tensor, w_scales: torch.Tensor, N: int, Y=None,
+                     stream=None):
+    """Y = Xt . Wd^T (W4A16): bf16 activations times the MXFP4 weight expanded
+    to bf16 on chip, fp32 accumulation."""
     _dev(Xt, "Xt")
     M, K = Xt.shape
-    N = Wd.shape[0]
-    if Wd.shape[1] != K or not Wd.is_contiguous():
-        raise ValueError("Wd must be contiguous [N, K]")
     if Y is None:
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=Xt.device)
-    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("macaq_w4a16_gemm", lib().macaq_w4a16_gemm(
-        _ptr(Xt), _ld(Xt), _ptr(Wd), M, N, K, _ptr(Y), _ld(Y), _ptr(workspace), nbytes,
-        _stream(stream)))
+        _ptr(Xt), _ld(Xt), _ptr(w_codes), _ptr(w_scales), M, N, K, _ptr(Y), _ld(Y), _stream(stream)))
     return Y
 
 
@@ -350,22 +347,20 @@ def macaq_w4a16_linear_workspace_bytes(M: int, K: int) -> int:
     return int(lib().macaq_w4a16_linear_workspace_bytes(M, K))
 
 
-def macaq_w4a16_linear(X: torch.Tensor, inv_s, Wd: torch.Tensor, hadamard_block: int = 32, Y=None,
-                       workspace=None, stream=None):
-    """W4A16 layer: bf16 transform of X, then Y = Xt . Wd^T (bf16 GEMM)."""
+def macaq_w4a16_linear(X: torch.Tensor, inv_s, w_codes: torch.Tensor, w_scales: torch.Tensor, N: int,
+                       hadamard_block: int = 32, Y=None, workspace=None, stream=None):
+    """W4A16 layer: bf16 transform of X, then Y = Xt . Wd^T with the MXFP4
+    weight expanded on chip."""
     _dev(X, "X")
     M, K = X.shape
-    N = Wd.shape[0]
-    if Wd.shape[1] != K or not Wd.is_contiguous():
-        raise ValueError("Wd must be contiguous [N, K]")
     if Y is None:
         Y = torch.empty(M, N, dtype=torch.bfloat16, device=X.device)
     if workspace is None:
         workspace = torch.empty(max(macaq_w4a16_linear_workspace_bytes(M, K), 1), dtype=torch.uint8,
                                 device=X.device)
     _check("macaq_w4a16_linear", lib().macaq_w4a16_linear(
-        _ptr(X), _ld(X), _ptr(inv_s), _ptr(Wd), M, N, K, hadamard_block, _ptr(Y), _ld(Y),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        _ptr(X), _ld(X), _ptr(inv_s), _ptr(w_codes), _ptr(w_scales), M, N, K, hadamard_block, _ptr(Y),
+        _ld(Y), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return Y
 
 

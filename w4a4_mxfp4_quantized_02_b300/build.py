@@ -6,8 +6,8 @@ GEMM, whose epilogue can encode MXFP4) additionally with ``-fmad=false`` (their
 arithmetic must not be contracted into FMAs).  The CUDA runtime is linked
 statically and the driver API is reached through the runtime's entry-point
 query, so the library loads on machines without a GPU driver (for symbol and
-argument checks) and needs no JIT cache at run time.  cuBLASLt (the plain bf16
-GEMM of the W4A16 fallback) is the one shared library it links.
+argument checks) and needs no JIT cache at run time.  It links no other
+library: every kernel is the library's own.
 """
 from __future__ import annotations
 
@@ -30,11 +30,10 @@ UNITS = {
     "gemm.cu": ["-fmad=false"],
     "api.cu": [],
     "static_scratch.cu": [],
-    "w4a16.cu": [],
     "flip.cu": ["-fmad=false"],
     "moe.cu": ["-fmad=false"],
 }
-HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh", "mx_block.cuh"]
+HEADERS = ["internal.h", "ptx.cuh", "gemm_skinny.cuh", "gemm_w4a16.cuh", "mx_block.cuh"]
 
 
 def _mtime(path: str) -> float:
@@ -57,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             subprocess.check_call(cmd)
     if force or _mtime(LIB) < max(_mtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, *objs, "-lcublasLt"]
+        cmd = [NVCC, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.check_call(cmd)

@@ -41,7 +41,6 @@ macaq_status check_rows(int64_t rows)
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // scratch the W4A16 bf16 GEMM may use (part of its workspace)
-constexpr size_t kW4A16GemmWorkspace = size_t{32} << 20;
 
 }  // namespace
 
@@ -297,33 +296,36 @@ macaq_status macaq_dequant_weight_bf16(const uint8_t *w_codes, const uint8_t *w_
 size_t macaq_w4a16_linear_workspace_bytes(int64_t M, int64_t K)
 {
     if (M < 0 || K <= 0 || K % 32 != 0) return 0;
-    return align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2) + kW4A16GemmWorkspace;
+    return align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
 }
 
-macaq_status macaq_w4a16_gemm(const void *Xt, int64_t ldxt, const void *Wd, int64_t M, int64_t N,
-                              int64_t K, void *Y, int64_t ldy, void *workspace, size_t ws_bytes,
-                              macaq_stream_t stream)
+macaq_status macaq_w4a16_gemm(const void *Xt, int64_t ldxt, const uint8_t *w_codes, const uint8_t *w_scales,
+                              int64_t M, int64_t N, int64_t K, void *Y, int64_t ldy, macaq_stream_t stream)
 {
     MACAQ_TRY(check_k(K));
     MACAQ_TRY(check_rows(M));
     MACAQ_TRY(check_rows(N));
     if (M == 0 || N == 0) return MACAQ_OK;
-    if (!Xt || !Wd || !Y || ldxt < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
-    if (ws_bytes > 0 && !workspace) return MACAQ_ERR_WORKSPACE;
-    if (!aligned16(Xt) || !aligned16(Wd) || !aligned16(Y) || (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) ||
-        ldxt % 8 != 0 || ldy % 8 != 0)
+    if (!Xt || !w_codes || !w_scales || !Y || ldxt < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
+    if (!aligned16(Xt) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(Y) || ldxt % 8 != 0 ||
+        ldy % 8 != 0)
         return MACAQ_ERR_ALIGNMENT;
-    const cudaError_t e = launch_bf16_gemm_nt(static_cast<const uint16_t *>(Xt), ldxt,
-                                              static_cast<const uint16_t *>(Wd), M, N, K,
-                                              static_cast<uint16_t *>(Y), ldy, workspace, ws_bytes,
-                                              static_cast<cudaStream_t>(stream));
-    if (e == cudaErrorNotSupported) return MACAQ_ERR_UNSUPPORTED;
-    return from_cuda(e);
+    W4A16Args g{};
+    g.Xt = Xt;
+    g.ldx = ldxt;
+    g.w_codes = w_codes;
+    g.w_scales = w_scales;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.Y = Y;
+    g.ldy = ldy;
+    return from_cuda(launch_w4a16_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
-macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, const void *Wd,
-                                int64_t M, int64_t N, int64_t K, int64_t hadamard_block, void *Y,
-                                int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream)
+macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, const uint8_t *w_codes,
+                                const uint8_t *w_scales, int64_t M, int64_t N, int64_t K, int64_t hadamard_block,
+                                void *Y, int64_t ldy, void *workspace, size_t ws_bytes, macaq_stream_t stream)
 {
     if (hadamard_block != 32 && hadamard_block != 64) return MACAQ_ERR_INVALID_ARG;
     MACAQ_TRY(check_k(K));
@@ -331,15 +333,15 @@ macaq_status macaq_w4a16_linear(const void *X, int64_t ldx, const float *inv_s, 
     MACAQ_TRY(check_rows(M));
     MACAQ_TRY(check_rows(N));
     if (M == 0 || N == 0) return MACAQ_OK;
-    if (!X || !inv_s || !Wd || !Y || ldx < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
+    if (!X || !inv_s || !w_codes || !w_scales || !Y || ldx < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < macaq_w4a16_linear_workspace_bytes(M, K)) return MACAQ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MACAQ_ERR_ALIGNMENT;
-    if (!aligned16(X) || !aligned16(Wd) || !aligned16(Y) || ldx % 8 != 0 || ldy % 8 != 0)
+    if (!aligned16(X) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(Y) || ldx % 8 != 0 ||
+        ldy % 8 != 0)
         return MACAQ_ERR_ALIGNMENT;
     uint8_t *xt = static_cast<uint8_t *>(workspace);
-    const size_t xt_bytes = align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
     MACAQ_TRY(macaq_transform_act_bf16(X, ldx, inv_s, M, K, hadamard_block, xt, K, stream));
-    return macaq_w4a16_gemm(xt, K, Wd, M, N, K, Y, ldy, xt + xt_bytes, kW4A16GemmWorkspace, stream);
+    return macaq_w4a16_gemm(xt, K, w_codes, w_scales, M, N, K, Y, ldy, stream);
 }
 
 macaq_status macaq_transform_f32(const void *X, int64_t ldx, const float *f, int64_t M, int64_t K,

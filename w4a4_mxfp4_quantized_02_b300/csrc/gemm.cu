@@ -656,6 +656,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 #include "gemm_skinny.cuh"
+#include "gemm_w4a16.cuh"
 
 __global__ void wait_probe_kernel()
 {
@@ -1040,6 +1041,97 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, p);
+}
+
+// W4A16: token tile NT (16 .. 256); RS raw stages and XS expanded tiles as
+// shared memory allows (small tiles: two CTAs per SM, the epilogue in the
+// expander warps).
+template <int NT, int RS, int XS, bool kSepEpi>
+cudaError_t launch_w4a16_tile(const W4A16Args &g, cudaStream_t stream, int slot)
+{
+    using L = w4a16::Layout<NT, RS, XS, kSepEpi>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kern = w4a16::gemm_w4a16_kernel<NT, RS, XS, kSepEpi>;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        DeviceInfo &di = g_dev[dev];
+        if (di.sms == 0) {
+            err = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err != cudaSuccess) return err;
+        }
+        if (!di.attr_set[slot]) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+            if (err != cudaSuccess) return err;
+            // all of the unified L1 as shared memory, so that two CTAs of the
+            // small-tile variants fit on an SM
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            if (err != cudaSuccess) return err;
+            di.attr_set[slot] = true;
+        }
+    }
+    const int sms = g_dev[dev].sms;
+    CUtensorMap tmX, tmWc;
+    {
+        uint64_t dims[2] = {static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M)};
+        uint64_t strides[1] = {static_cast<uint64_t>(g.ldx) * 2};
+        uint32_t box[2] = {64, NT};
+        if (!encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.Xt, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {static_cast<uint64_t>(g.K / 2), static_cast<uint64_t>(g.N)};
+        uint64_t strides[1] = {static_cast<uint64_t>(g.K / 2)};
+        uint32_t box[2] = {32, 128};
+        if (!encode(&tmWc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, g.w_codes, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    w4a16::Params p;
+    p.sfw = g.w_scales;
+    p.Y = static_cast<uint16_t *>(g.Y);
+    p.ldy = g.ldy;
+    p.M = static_cast<int32_t>(g.M);
+    p.N = static_cast<int32_t>(g.N);
+    p.num_kstages = static_cast<int32_t>((g.K + 63) / 64);
+    p.nka = static_cast<int32_t>(pad_scale_cols(g.K) / 4);
+    p.n_wb = static_cast<int32_t>((g.N + 127) / 128);
+    const int64_t tiles = static_cast<int64_t>((g.M + NT - 1) / NT) * p.n_wb;
+    if (tiles > (int64_t{1} << 30)) return cudaErrorInvalidValue;
+    p.n_tiles = static_cast<int32_t>(tiles);
+    // CTAs resident per SM by shared memory (1 KB reserved per CTA): every
+    // tile gets its own CTA while they all fit, else a persistent grid
+    int smem_sm = 0;
+    err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (err != cudaSuccess) return err;
+    int per_sm = smem_sm / (L::ALLOC + 1024);
+    per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+    const int64_t slots = static_cast<int64_t>(sms) * per_sm;
+    const int64_t grid = tiles < slots ? tiles : slots;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(L::THREADS);
+    cfg.dynamicSmemBytes = L::ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmX, tmWc, p);
+}
+
+cudaError_t launch_w4a16_gemm(const W4A16Args &g, cudaStream_t stream)
+{
+    if (g.M <= 16) return launch_w4a16_tile<16, 8, 3, false>(g, stream, 8);
+    if (g.M <= 32) return launch_w4a16_tile<32, 6, 3, false>(g, stream, 9);
+    if (g.M <= 64) return launch_w4a16_tile<64, 4, 3, false>(g, stream, 10);
+    if (g.M <= 128) return launch_w4a16_tile<128, 6, 3, true>(g, stream, 11);
+    return launch_w4a16_tile<256, 4, 3, true>(g, stream, 12);
 }
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)

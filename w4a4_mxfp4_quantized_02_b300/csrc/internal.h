@@ -52,11 +52,7 @@ struct QuantArgs {
 cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream);
 cudaError_t launch_dequant_bf16(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t K,
                                 uint16_t *out, cudaStream_t stream);
-// W4A16: Y[M, N] = Xt[M, K] . Wd[N, K]^T in bf16 with fp32 accumulation
-// (a plain library GEMM; ws is its scratch).
-cudaError_t launch_bf16_gemm_nt(const uint16_t *Xt, int64_t ldx, const uint16_t *Wd, int64_t M, int64_t N,
-                                int64_t K, uint16_t *Y, int64_t ldy, void *ws, size_t ws_bytes,
-                                cudaStream_t stream);
+
 
 // Flip Refinement: H = A^T A (+ damp on the diagonal) of fp32 calibration rows
 // a [m, k]; the descent over rows wt [n, k] of round-to-nearest codes (in/out)
@@ -108,6 +104,20 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);
+
+// W4A16: Y[M, N] = Xt[M, K] . Wd[N, K]^T with Wd the bf16 expansion of the
+// MXFP4 weight (codes [N, K/2], tiled scales), expanded tile by tile in
+// shared memory; bf16 products, fp32 accumulation (tcgen05 kind::f16).
+struct W4A16Args {
+    const void *Xt;
+    int64_t ldx;
+    const uint8_t *w_codes;
+    const uint8_t *w_scales;
+    int64_t M, N, K;
+    void *Y;
+    int64_t ldy;
+};
+cudaError_t launch_w4a16_gemm(const W4A16Args &g, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda
 // link), interleave none, 256-byte L2 promotion, zero fill out of bounds.

@@ -196,6 +196,19 @@ __device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// D(tmem) (+)= A(smem) x B(smem), 16-bit inputs (kind::f16: bf16 or f16 as
+// the instruction descriptor says), fp32 accumulation, K = 16.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 {
@@ -265,6 +278,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32
            ((M >> 4) << 24) | (a_sf_id << 29);
 }
 
+
+// Instruction descriptor of tcgen05.mma.kind::f16 with bf16 A and B, fp32
+// D, both K-major, shape M x N (x K = 16).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
 
 // ------------------------------------------------------------------ clusters
 
