@@ -141,6 +141,27 @@ __device__ __forceinline__ uint32_t silu_mul_word(uint32_t gw, uint32_t uw)
 // half).  After the five 32-point stages the stride-32 stage pairs element i
 // of the two halves through a shuffle, and the normalisation is the exact
 // 1/8; the MX block stays these 32 values.
+// Packed fp32x2 subtraction, each lane rounded to nearest.
+__device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float max3_f32(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <bool kH64>
 __device__ __forceinline__ void hadamard_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
                                                      float2 (&v)[16])
@@ -162,7 +183,7 @@ __device__ __forceinline__ void hadamard_block_pairs(const uint32_t (&raw)[16], 
             // sums of sums: no multiply feeds these adds, so the packed
             // intrinsics cannot be contracted into an FMA
             v[i] = __fadd2_rn(a, b);
-            v[i + hh] = __fadd2_rn(a, make_float2(-b.x, -b.y));
+            v[i + hh] = fsub2_rn(a, b);
         }
     }
     if (kH64) {
@@ -182,6 +203,49 @@ __device__ __forceinline__ void hadamard_block_pairs(const uint32_t (&raw)[16], 
 
 // The W4A16 activation: the normalised transform rounded once to bf16
 // (element 2i in the low half of word i).
+// The 32-channel transform with the block maximum of |v| taken from the last
+// butterfly stage: for its pairs (a, b) -> (a + b, a - b), max(|RN(a + b)|,
+// |RN(a - b)|) = RN(|a| + |b|) because rounding to nearest is monotone and
+// symmetric, so eight packed adds of magnitudes and a short max chain give the
+// maximum of all 32 outputs exactly.
+__device__ __forceinline__ float hadamard32_pairs_amax(const uint32_t (&raw)[16], const float2 (&f)[16],
+                                                       float2 (&v)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 ab = __fmul2_rn(make_float2(bf16lo(raw[i]), bf16hi(raw[i])), f[i]);
+        v[i] = make_float2(__fadd_rn(ab.x, ab.y), __fsub_rn(ab.x, ab.y));
+    }
+#pragma unroll
+    for (int hh = 1; hh < 8; hh <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & hh) continue;
+            const float2 a = v[i];
+            const float2 b = v[i + hh];
+            v[i] = __fadd2_rn(a, b);
+            v[i + hh] = fsub2_rn(a, b);
+        }
+    }
+    float2 t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 a = v[i];
+        const float2 b = v[i + 8];
+        v[i] = __fadd2_rn(a, b);
+        v[i + 8] = fsub2_rn(a, b);
+        t[i] = __fadd2_rn(make_float2(fabsf(a.x), fabsf(a.y)), make_float2(fabsf(b.x), fabsf(b.y)));
+    }
+    float m = max3_f32(t[0].x, t[0].y, t[1].x);
+    m = max3_f32(m, t[1].y, t[2].x);
+    m = max3_f32(m, t[2].y, t[3].x);
+    m = max3_f32(m, t[3].y, t[4].x);
+    m = max3_f32(m, t[4].y, t[5].x);
+    m = max3_f32(m, t[5].y, t[6].x);
+    m = max3_f32(m, t[6].y, t[7].x);
+    return fmaxf(m, t[7].y);
+}
+
 template <bool kH64>
 __device__ __forceinline__ void bf16_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
                                                  uint32_t (&out)[16])
@@ -201,17 +265,11 @@ __device__ __forceinline__ void bf16_block_pairs(const uint32_t (&raw)[16], cons
 // element 2i+1) after the butterflies (unnormalised): the block maximum, the
 // E8M0 byte, the normalise-and-scale multiply and the E2M1 codes (element 2i
 // in the low nibble of byte i).  kH64: the 64-channel normalisation 1/8.
+// The same with the block maximum of |v| already known.
 template <bool kH64>
-__device__ __forceinline__ uint32_t encode_block_pairs(float2 (&v)[16], uint4 &codes)
+__device__ __forceinline__ uint32_t encode_block_pairs_vmax(float2 (&v)[16], float vmax, uint4 &codes)
 {
     constexpr float kNorm = kH64 ? 0.125f : kInvSqrt32;
-    float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        m0 = fmaxf(m0, fabsf(v[i].x));
-        m1 = fmaxf(m1, fabsf(v[i].y));
-    }
-    const float vmax = fmaxf(m0, m1);
     const float amax = __fmul_rn(vmax, kNorm);
     const int ef = static_cast<int>(__float_as_uint(amax) >> 23);
     const uint32_t sbyte = static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
@@ -245,12 +303,29 @@ __device__ __forceinline__ uint32_t encode_block_pairs(float2 (&v)[16], uint4 &c
 }
 
 template <bool kH64>
+__device__ __forceinline__ uint32_t encode_block_pairs(float2 (&v)[16], uint4 &codes)
+{
+    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        m0 = fmaxf(m0, fabsf(v[i].x));
+        m1 = fmaxf(m1, fabsf(v[i].y));
+    }
+    return encode_block_pairs_vmax<kH64>(v, fmaxf(m0, m1), codes);
+}
+
+template <bool kH64>
 __device__ __forceinline__ uint32_t quant_block_pairs(const uint32_t (&raw)[16], const float2 (&f)[16],
                                                       uint4 &codes)
 {
     float2 v[16];
-    hadamard_block_pairs<kH64>(raw, f, v);
-    return encode_block_pairs<kH64>(v, codes);
+    if constexpr (kH64) {
+        hadamard_block_pairs<kH64>(raw, f, v);
+        return encode_block_pairs<kH64>(v, codes);
+    } else {
+        const float vmax = hadamard32_pairs_amax(raw, f, v);
+        return encode_block_pairs_vmax<false>(v, vmax, codes);
+    }
 }
 
 // A whole 64-channel Hadamard block held by one thread (two MX blocks): the
