@@ -466,13 +466,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
                                lambda k: Yh[k].copy_(sets[k]["Y"], non_blocking=True))
         e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
 
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "gemm_traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            tj = json.load(f)
-        if tj.get("workload") == wl.name and tj.get("kernel_source_sha") == kernel_source_sha():
-            traffic = tj.get("dram_bytes_per_launch")
+    traffic = recorded_traffic(gemm_kernel_name(M), wl.name)
 
     if rank != 0:
         return None
@@ -503,7 +497,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         roofline = {"bound": "hbm",
                     "kernel": gemm_kernel_name(M),
                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": gemm_bytes,
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "bytes_per_launch": gemm_bytes,
                     "peak_note": f"{peaks['source']} HBM copy bandwidth",
                     "tflops": gemm_tflops, "avg_launch_us": gemm_avg * 1e3, "timing": timing}
 
@@ -528,6 +522,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
                       else "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
+                      "traffic": None if fused else recorded_traffic("quant_dense_tma_kernel", wl.name),
                       "avg_launch_us": quant_avg * 1e3},
         "cpu_baseline": cpu,
         "e2e": None if light else {
@@ -1299,15 +1294,39 @@ def capture_graph(fn):
     return g
 
 
-def kernel_source_sha() -> str:
-    """Hash of the GEMM kernel sources: a recorded traffic figure is only used
-    while the kernel it was measured on is unchanged."""
+# The sources each kernel family is compiled from: a recorded DRAM traffic
+# figure is used only while the hash of its kernel's sources is unchanged.
+KERNEL_SOURCES = {
+    "gemm_mxf4_pair_kernel": ("gemm.cu", "ptx.cuh", "mx_block.cuh", "internal.h"),
+    "gemm_mxf4_skinny_kernel": ("gemm.cu", "gemm_skinny.cuh", "ptx.cuh", "internal.h"),
+    "gemm_w4a16_kernel": ("gemm.cu", "gemm_w4a16.cuh", "ptx.cuh", "internal.h"),
+    "quant_dense_tma_kernel": ("quant.cu", "mx_block.cuh", "ptx.cuh", "internal.h"),
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "w4a4_mxfp4_quantized_02_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum of one launch of `kernel`
+    on `workload`, from the ncu record under profiles/, or None when there is
+    none or the kernel's sources changed since it was taken."""
+    prof = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(prof):
+        return None
+    with open(prof) as f:
+        entries = json.load(f).get("entries", [])
+    for e in entries:
+        if (e.get("kernel") == kernel and e.get("workload") == workload
+                and e.get("source_sha") == kernel_source_sha(kernel)):
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 def mma_probe():
@@ -1326,6 +1345,53 @@ def mma_probe():
             ns = out[1:2 * sms:2].median().item()
             flops = sms * 4 * iters * 2 * 128 * n * 64
             print(f"| {n} | {names[mode]} | {cyc / iters:.1f} | {flops / ns / 1e6:.2f} | {cyc / ns:.3f} |")
+    return 0
+
+
+def read_probe():
+    """Read bandwidth a library reaches on this GPU, beside the copy peak:
+    torch's sum over a bf16 vector (reads only), torch's copy (reads and
+    writes), and cuBLAS bf16 products shaped like decode (the weight streamed
+    once).  Each timing is the median of 20 runs, L2 flushed before each."""
+    import torch
+    dev = torch.device("cuda:0")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, iters=20, warm=3):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(iters):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ts = sorted(a.elapsed_time(b) for a, b in evs)
+        return ts[len(ts) // 2] * 1e-3
+
+    print("| operation | bytes (MB) | time (us) | GB/s |")
+    print("|---|---|---|---|")
+    for mib in (64, 512, 2048):
+        n = (mib << 20) // 2
+        x = torch.empty(n, dtype=torch.bfloat16, device=dev).normal_()
+        y = torch.empty_like(x)
+        t = timed(lambda: x.sum(dtype=torch.float32))
+        print(f"| torch sum, {mib} MiB bf16 (read) | {2 * n / 1e6:.1f} | {t * 1e6:.1f} | {2 * n / t / 1e9:.0f} |")
+        t = timed(lambda: y.copy_(x))
+        print(f"| torch copy, {mib} MiB bf16 (read + write) | {4 * n / 1e6:.1f} | {t * 1e6:.1f} | "
+              f"{4 * n / t / 1e9:.0f} |")
+        del x, y
+    for (m, n, k) in ((16, 6400, 5120), (16, 25600, 5120), (16, 51200, 5120)):
+        w = torch.empty(n, k, dtype=torch.bfloat16, device=dev).normal_()
+        a = torch.empty(m, k, dtype=torch.bfloat16, device=dev).normal_()
+        t = timed(lambda: a @ w.t())
+        print(f"| cuBLAS bf16 [{m}, {k}] x [{n}, {k}]^T (weight read once) | {n * k * 2 / 1e6:.1f} | "
+              f"{t * 1e6:.1f} | {n * k * 2 / t / 1e9:.0f} |")
+        del w, a
     return 0
 
 
@@ -1394,10 +1460,12 @@ def main():
                     help="launch every step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--kernel-events-every", type=int, default=4,
                     help="bracket the kernels of every n-th timed step with CUDA events")
-    ap.add_argument("--probe", choices=["mma"], help="print a hardware probe table and exit")
+    ap.add_argument("--probe", choices=["mma", "read"], help="print a hardware probe table and exit")
     args = ap.parse_args()
     if args.probe == "mma":
         return mma_probe()
+    if args.probe == "read":
+        return read_probe()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -269,46 +269,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     griddep_launch_dependents();
-    griddep_wait();
 
     int32_t *s_off = reinterpret_cast<int32_t *>(smem + L::OFF_OFFS);  // expert row offsets
     int32_t *s_ppb = s_off + (kMaxExperts + 1);    // pair-tiles before expert e
     int32_t *s_pst = s_ppb + (kMaxExperts + 1);    // first padded row of expert e
     int32_t num_mp = (p.M + 2 * BM - 1) / (2 * BM);
     int32_t num_full = p.num_full, num_split = p.num_split;
-    if (GROUPED) {
-        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int32_t pairs = 0, rows = 0;
-            for (int e = 0; e < p.E; ++e) {
-                const int32_t blocks = (s_off[e + 1] - s_off[e] + BM - 1) / BM;
-                s_ppb[e] = pairs;
-                s_pst[e] = rows;
-                pairs += (blocks + 1) / 2;
-                rows += blocks * BM;
-            }
-            s_ppb[p.E] = pairs;
-            s_pst[p.E] = rows;
-        }
-        __syncthreads();
-        // the same last-round split as the host makes for dense problems
-        num_mp = s_ppb[p.E];
-        const int32_t tiles = num_mp * p.num_nb;
-        const int32_t pairs = static_cast<int32_t>(gridDim.x >> 1);
-        const int32_t rem = tiles % pairs;
-        num_full = tiles;
-        num_split = 0;
-        if (rem > 0 && 2 * rem <= pairs) {
-            num_full = tiles - rem;
-            num_split = rem;
-        }
-    }
-    const int64_t total_units = static_cast<int64_t>(num_full) + 2 * static_cast<int64_t>(num_split);
     const int nks = p.num_kstages;
     // scale atoms of stage st -> its tensor-memory slot (A: atom `at` at column
-    // 4*at; B: atom `at` of row block r at 4*(2*at + r)), in both CTAs
-    auto copy_scales = [&](uint32_t st) {
+    // 4*at; B: atom `at` of row block r at 4*(2*at + r)), in both CTAs; a
+    // 128-column unit reads only B's first row block
+    auto copy_scales = [&](uint32_t st, bool whole) {
         const uint64_t da = smem_desc(sbase + L::OFF_SFA + st * L::SFA_STAGE, 0, 128, kSwizzleNone);
         const uint64_t db = smem_desc(sbase + L::OFF_SFB + st * L::SFB_STAGE, 0, 128, kSwizzleNone);
         const uint32_t sfa_t = tmem + SF_TMEM_BASE + st * L::SF_COLS;
@@ -319,7 +290,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_cp_pair_32x128b_warpx4(sfa_t + 4 * at, da + at * kAtom);
 #pragma unroll
             for (int r = 0; r < BN / 128; ++r)
-                tc_cp_pair_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r, db + (r * L::KATOMS + at) * kAtom);
+                if (r == 0 || whole)
+                    tc_cp_pair_32x128b_warpx4(sfb_t + at * 4 * (BN / 128) + 4 * r, db + (r * L::KATOMS + at) * kAtom);
         }
     };
     // Tiles t run over (pair m-block t % num_mp (m fastest), n-block t / num_mp),
@@ -367,6 +339,47 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
+    if (!GROUPED && warp == 0 && lane == 0 && first_unit < static_cast<int64_t>(num_full) + 2 * num_split) {
+        // The weight does not depend on the kernel this one may overlap (A
+        // does): start the first unit's weight stages towards L2 meanwhile.  A
+        // prefetch is only a hint; the loads after the wait read the latest data.
+        Tile ti;
+        tile_of(first_unit, ti);
+        const int32_t brow = ti.n0 + static_cast<int32_t>(rank) * (ti.ncols / 2);
+        for (int ks = 0; ks < min(nks, STAGES); ++ks)
+            tma_prefetch_2d(ti.ncols == BN ? &tmB : &tmB64, ks * KB, brow);
+    }
+    griddep_wait();
+
+    if (GROUPED) {
+        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t pairs = 0, rows = 0;
+            for (int e = 0; e < p.E; ++e) {
+                const int32_t blocks = (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+                s_ppb[e] = pairs;
+                s_pst[e] = rows;
+                pairs += (blocks + 1) / 2;
+                rows += blocks * BM;
+            }
+            s_ppb[p.E] = pairs;
+            s_pst[p.E] = rows;
+        }
+        __syncthreads();
+        // the same last-round split as the host makes for dense problems
+        num_mp = s_ppb[p.E];
+        const int32_t tiles = num_mp * p.num_nb;
+        const int32_t pairs = static_cast<int32_t>(gridDim.x >> 1);
+        const int32_t rem = tiles % pairs;
+        num_full = tiles;
+        num_split = 0;
+        if (rem > 0 && 2 * rem <= pairs) {
+            num_full = tiles - rem;
+            num_split = rem;
+        }
+    }
+    const int64_t total_units = static_cast<int64_t>(num_full) + 2 * static_cast<int64_t>(num_split);
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
@@ -489,6 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t st = 0, ph = 0, it = 0;
             bool ok = true;
             for (int64_t u = first_unit; u < total_units && ok; u += unit_stride) {
+                const bool whole = u < num_full;
                 for (int ks = 0; ks < nks; ++ks, ++it) {
                     // both CTAs' data of the stage have landed
                     MACAQ_TRACE(9, it);
@@ -497,7 +511,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     MACAQ_TRACE(10, it);
-                    copy_scales(st);
+                    copy_scales(st, whole);
                     tc_commit_pair(ready_bar(static_cast<int>(st)));
                     MACAQ_TRACE(11, it);
                     if (++st == STAGES) {

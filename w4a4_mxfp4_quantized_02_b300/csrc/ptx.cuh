@@ -414,6 +414,10 @@ __device__ __forceinline__ void tc_mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc
 }
 
 // ---------------------------------------------------------------- L2 prefetch
+//
+// Prefetches are hints: L2 is where every SM's writes meet, so a line fetched
+// early still reads the latest data when a later load asks for it.  Boxes of
+// a tensor map skip their out-of-range parts.
 
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y)
 {
