@@ -690,14 +690,14 @@ def gpu_arm_w4a16(args, rank: int, world: int):
     if flops / gemm_bytes >= bf16_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
         roofline = {"bound": "tensor", "kernel": "gemm_w4a16_kernel",
                     "achieved": gemm_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": gemm_tflops / bf16_peak, "traffic": None,
+                    "frac": gemm_tflops / bf16_peak, "traffic": recorded_traffic("gemm_w4a16_kernel", wl.name),
                     "peak_note": f"{peaks['source']} bf16 burst", "avg_launch_us": g_ms * 1e3,
                     "timing": timing}
     else:
         gbs = gemm_bytes / (g_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "kernel": "gemm_w4a16_kernel", "achieved": gbs,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                    "traffic": None, "bytes_per_launch": gemm_bytes,
+                    "traffic": recorded_traffic("gemm_w4a16_kernel", wl.name), "bytes_per_launch": gemm_bytes,
                     "peak_note": f"{peaks['source']} HBM copy bandwidth", "tflops": gemm_tflops,
                     "avg_launch_us": g_ms * 1e3, "timing": timing}
     line = {
@@ -1120,7 +1120,8 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
                      "kernel": ("gemm_mxf4_pair_kernel<6, true, 1> (grouped gate+up, MXFP4 h epilogue)" if fused
                                 else "gemm_mxf4_pair_kernel<6, true> (grouped, gate+up)"),
                      "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": gu_gbs / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("gemm_mxf4_pair_kernel", wl.name) if fused else None,
                      "bytes_per_launch": gu_bytes, "avg_launch_us": avg[1] * 1e3,
                      "tflops": wl.flops_gate_up / (avg[1] * 1e-3) / 1e12,
                      "timing": f"CUDA events around kernel groups: {batches.describe()} of the "
