@@ -589,8 +589,11 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 // the transform with that expert's balance factors; padding rows get zero
 // scales and no codes.  The stage layout and the consumer are those of the
 // dense kernel; the producer lands each row of a stage with its own TMA box
-// (one row high), so the rows can come from anywhere in X.  The rows of this
-// CTA are resolved once, up front, into a table in shared memory.
+// (one row high), so the rows can come from anywhere in X.  Only the experts'
+// real rows run through the pipeline (padding is a fifth of the padded rows
+// at 4096 tokens x top-8 of 128 experts); each CTA resolves its rows (token
+// row, expert, padded destination row) once, up front, into a table in
+// shared memory, and afterwards writes the zero scales of padding rows.
 // kSilu: the rows are the sorted rows of a [rows, 2F] gate|up matrix; each
 // stage lands the gate and the up slab of every row and the consumer forms
 // h = SiLU(g) * u before the transform.
@@ -614,8 +617,9 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc);
     int32_t *s_off = reinterpret_cast<int32_t *>(misc + 16);
     int32_t *s_poff = s_off + (kMaxExperts + 1);
-    int32_t *m_src = s_poff + (kMaxExperts + 1);  // token row, -1 padding, -2 past the end
+    int32_t *m_src = s_poff + (kMaxExperts + 1);  // token row, -2 past the end
     int32_t *m_exp = m_src + per_cta * RT;
+    int32_t *m_dst = m_exp + per_cta * RT;        // padded output row
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int32_t slab0 = static_cast<int32_t>(blockIdx.x) * TB;
@@ -646,36 +650,34 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
 
     // A contiguous range of row groups per CTA (consecutive rows mostly share
     // an expert, so the balance factors are reloaded rarely), dealt over the
-    // rows the experts actually use; the rest of the padded capacity only needs
-    // zero scales, written after the pipeline.
+    // experts' real rows in sorted order; padding rows and the rest of the
+    // padded capacity only need zero scales, written after the pipeline.
     const int64_t used = s_poff[a.E];
-    const int32_t groups_used = static_cast<int32_t>((used + RT - 1) / RT);
-    const int32_t per = (groups_used + static_cast<int32_t>(gridDim.y) - 1) / static_cast<int32_t>(gridDim.y);
+    const int64_t r0 = s_off[0], nreal = static_cast<int64_t>(s_off[a.E]) - s_off[0];
+    const int32_t groups_real = static_cast<int32_t>((nreal + RT - 1) / RT);
+    const int32_t per = (groups_real + static_cast<int32_t>(gridDim.y) - 1) / static_cast<int32_t>(gridDim.y);
     const int32_t g0 = static_cast<int32_t>(blockIdx.y) * per;
-    const int32_t my_groups = g0 < groups_used ? min(per, groups_used - g0) : 0;
+    const int32_t my_groups = g0 < groups_real ? min(per, groups_real - g0) : 0;
     (void)groups;
     (void)per_cta;
-    // row i of local group j is padded row (g0 + j) * RT + i
+    // row i of local group j is sorted row r0 + (g0 + j) * RT + i
     for (int idx = t; idx < my_groups * RT; idx += blockDim.x) {
         const int j = idx / RT, i = idx - (idx / RT) * RT;
-        const int64_t p = (static_cast<int64_t>(g0) + j) * RT + i;
-        int32_t src = -2, ex = 0;
-        if (p < used) {
-            src = -1;
-            if (p < s_poff[a.E]) {
-                int lo = 0, hi = a.E;  // s_poff[lo] <= p < s_poff[hi]
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (s_poff[mid] <= p) lo = mid; else hi = mid;
-                }
-                const int64_t jj = p - s_poff[lo];
-                ex = lo;
-                if (jj < s_off[lo + 1] - s_off[lo])
-                    src = kSilu ? static_cast<int32_t>(s_off[lo] + jj) : a.row_src[s_off[lo] + jj];
+        const int64_t r = r0 + (static_cast<int64_t>(g0) + j) * RT + i;
+        int32_t src = -2, ex = 0, dst = -1;
+        if (r < s_off[a.E]) {
+            int lo = 0, hi = a.E;  // s_off[lo] <= r < s_off[lo + 1] (the last such expert)
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= r) lo = mid; else hi = mid;
             }
+            ex = lo;
+            dst = static_cast<int32_t>(s_poff[lo] + (r - s_off[lo]));
+            src = kSilu ? static_cast<int32_t>(r) : a.row_src[r];
         }
         m_src[idx] = src;
         m_exp[idx] = ex;
+        m_dst[idx] = dst;
     }
     __syncthreads();
 
@@ -742,7 +744,7 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
         if (!ok) break;
         const int32_t src = m_src[j * RT + ty];
         const int32_t ex = m_exp[j * RT + ty];
-        const int64_t p = (static_cast<int64_t>(g0) + j) * RT + ty;
+        const int64_t p = m_dst[j * RT + ty];
         uint32_t sbyte = 0;
         const bool valid = src >= 0 && has_kb;
         uint32_t raw[16];
@@ -804,12 +806,22 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
         uint32_t word = sbyte << (8 * (lane & 3));
         word |= __shfl_xor_sync(0xffffffffu, word, 1);
         word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        if (writes_scale && src != -2) {
+        if (writes_scale && src >= 0) {
             const int64_t off = ((p / 128) * nka + kb / 4) * 512 + (p % 32) * 16 + ((p % 128) / 32) * 4;
             *reinterpret_cast<uint32_t *>(a.scales + off) = word;
         }
     }
-    // zero scales for the padded capacity past the experts' rows
+    // zero scales for the padding rows of this CTA's experts ...
+    if (writes_scale) {
+        for (int e = static_cast<int>(blockIdx.y); e < a.E; e += static_cast<int>(gridDim.y)) {
+            for (int64_t p = static_cast<int64_t>(s_poff[e]) + (s_off[e + 1] - s_off[e]) + ty; p < s_poff[e + 1];
+                 p += RT) {
+                const int64_t off = ((p / 128) * nka + kb / 4) * 512 + (p % 32) * 16 + ((p % 128) / 32) * 4;
+                *reinterpret_cast<uint32_t *>(a.scales + off) = 0u;
+            }
+        }
+    }
+    // ... and for the padded capacity past the experts' rows
     if (writes_scale) {
         for (int64_t p = used + static_cast<int64_t>(blockIdx.y) * RT + ty; p < a.rows_out;
              p += static_cast<int64_t>(gridDim.y) * RT) {
@@ -1085,7 +1097,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     ctas_y = (groups + per_cta - 1) / per_cta;
     const int64_t max_rows = per_cta * rt;
     if (max_rows > 4096) return cudaSuccess;  // row table too large: register-staged kernel
-    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 2 * max_rows * 4 + 1024;
+    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 3 * max_rows * 4 + 1024;
     const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : (4 * stage + 16 * 4 + fixed <= 210 * 1024) ? 4 : 3;
     const int64_t smem = stages * stage + 16 * stages + fixed;
     if (smem > 210 * 1024) return cudaSuccess;
