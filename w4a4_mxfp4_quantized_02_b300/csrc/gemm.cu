@@ -183,8 +183,11 @@ struct PairLayout {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
-    // store staging per epilogue warp: double-buffered when it fits
-    static constexpr int EPI_NBUF = STAGES >= 6 ? 1 : 2;
+    // store staging per epilogue warp: one 32 x 16 buffer beside six stages;
+    // beside four (short K: the next tile's accumulator is full after three or
+    // four stages) all eight of a warp's 128 columns, written in one pass and
+    // published to the store unit by one proxy fence
+    static constexpr int EPI_NBUF = STAGES >= 6 ? 1 : 8;
     static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * EPI_NBUF * EPI_BUF;
     static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -614,54 +617,89 @@ __global__ void __launch_bounds__(THREADS, 1)
             // in Y, so a warp with some of them stores row by row.
             const bool use_tma = !GROUPED || row0 + 32 <= ti.rows_valid;
             const bool my_row = row0 + lane < ti.rows_valid;
+            if (L::EPI_NBUF >= 8 && use_tma) {
+                // the previous tile's stores must be done reading the staging
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                int nchunks = 0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int32_t ncol = ti.n0 + half * 128 + 16 * c;
-                if (ncol >= p.N) break;
-                uint32_t packed[8];
+                for (int c = 0; c < 8; ++c) {
+                    if (ti.n0 + half * 128 + 16 * c >= p.N) break;
+                    uint32_t packed[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
-                    const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                    packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
-                }
-                if (!use_tma) {
-                    if (my_row) {
-                        uint16_t *dst = p.Y + static_cast<int64_t>(ti.y_row0 + row0 + lane) * p.ldy + ncol;
-                        if (ncol + 16 <= p.N) {
-                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-                            d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                            d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                        } else {
-                            for (int i = 0; i < 16 && ncol + i < p.N; ++i)
-                                dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
-                        }
+                    for (int i = 0; i < 8; ++i) {
+                        const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
+                        const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                        packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
                     }
-                } else {
-                    // rows past M and columns past N are clipped by the store
-                    const uint32_t buf = ebuf + (chunk % L::EPI_NBUF) * EPI_BUF;
-                    ++chunk;
-                    // the store that last read this buffer must be done with it
-                    if (lane == 0) {
-                        if (L::EPI_NBUF == 2) bulk_wait_read_le1();
-                        else bulk_wait_read_all();
-                    }
-                    __syncwarp();
+                    const uint32_t buf = ebuf + c * EPI_BUF;
                     const uint32_t sw = (lane >> 2) & 1;
-                    const uint32_t r0 = buf + lane * 32 + 16 * (0 ^ sw);
-                    const uint32_t r1 = buf + lane * 32 + 16 * (1 ^ sw);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r0), "r"(packed[0]),
-                                 "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * sw),
+                                 "r"(packed[0]), "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
                                  : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r1), "r"(packed[4]),
-                                 "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * (1 ^ sw)),
+                                 "r"(packed[4]), "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
                                  : "memory");
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, buf, ncol, ti.y_row0 + row0);
-                        bulk_commit();
+                    ++nchunks;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // rows past M and columns past N are clipped by the stores
+                    for (int c = 0; c < nchunks; ++c)
+                        tma_store_2d(&tmY, ebuf + c * EPI_BUF, ti.n0 + half * 128 + 16 * c, ti.y_row0 + row0);
+                    bulk_commit();
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int32_t ncol = ti.n0 + half * 128 + 16 * c;
+                    if (ncol >= p.N) break;
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
+                        const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                        packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    if (!use_tma) {
+                        if (my_row) {
+                            uint16_t *dst = p.Y + static_cast<int64_t>(ti.y_row0 + row0 + lane) * p.ldy + ncol;
+                            if (ncol + 16 <= p.N) {
+                                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                                d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                                d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                            } else {
+                                for (int i = 0; i < 16 && ncol + i < p.N; ++i)
+                                    dst[i] = static_cast<uint16_t>(packed[i >> 1] >> (16 * (i & 1)));
+                            }
+                        }
+                    } else {
+                        // rows past M and columns past N are clipped by the store
+                        const uint32_t buf = ebuf + (chunk % L::EPI_NBUF) * EPI_BUF;
+                        ++chunk;
+                        // the store that last read this buffer must be done with it
+                        if (lane == 0) {
+                            bulk_wait_read_le<L::EPI_NBUF - 1>();
+                        }
+                        __syncwarp();
+                        const uint32_t sw = (lane >> 2) & 1;
+                        const uint32_t r0 = buf + lane * 32 + 16 * (0 ^ sw);
+                        const uint32_t r1 = buf + lane * 32 + 16 * (1 ^ sw);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r0), "r"(packed[0]),
+                                     "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r1), "r"(packed[4]),
+                                     "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
+                                     : "memory");
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmY, buf, ncol, ti.y_row0 + row0);
+                            bulk_commit();
+                        }
                     }
                 }
             }
@@ -1181,8 +1219,11 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     // everything else: CTA pairs on 256 x 256 tiles (grouped: per-expert B)
     if (g.E > 0 && g.epi == 1) return launch_pair<6, true, 1>(g, stream, 0);
     if (g.E > 0 && g.epi == 2) return launch_pair<6, true, 2>(g, stream, 1);
-    if (g.E > 0) return launch_pair<6, true>(g, stream, 7);
-    return launch_pair<6, false>(g, stream, 3);
+    // at most four 256-wide K stages per tile: four stages and four store
+    // buffers per epilogue warp
+    const bool short_k = g.K <= 4 * 256;
+    if (g.E > 0) return short_k ? launch_pair<4, true>(g, stream, 13) : launch_pair<6, true>(g, stream, 7);
+    return short_k ? launch_pair<4, false>(g, stream, 14) : launch_pair<6, false>(g, stream, 3);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)

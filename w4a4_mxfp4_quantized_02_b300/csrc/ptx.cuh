@@ -120,14 +120,16 @@ __device__ __forceinline__ void bulk_commit()
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_read_le1()
-{
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-
 __device__ __forceinline__ void bulk_wait_read_all()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until at most N of this thread's bulk store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_le()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all()
