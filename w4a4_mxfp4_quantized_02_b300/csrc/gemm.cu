@@ -59,7 +59,10 @@ constexpr int BM = 128;
 constexpr int SF_ATOM = 512;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int EPI_WARP0 = 3;  // warps 0..2: TMA producer, MMA issuer, scale copier
-constexpr int THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
+// The gate+up epilogue with 32-channel blocks (EPI 1) runs sixteen warps, two
+// per lane quarter and column half, each taking one block of a 64-channel chunk.
+__host__ __device__ constexpr int pair_epi_warps(int epi) { return epi == 1 ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS; }
+__host__ __device__ constexpr int pair_threads(int epi) { return (EPI_WARP0 + pair_epi_warps(epi)) * 32; }
 constexpr int TMEM_COLS = 512;
 constexpr int SF_TMEM_BASE = 256;
 constexpr int EPI_BUF = 32 * 32;  // 32 rows x 16 bf16
@@ -216,7 +219,7 @@ struct PairLayout {
 // the down input's padded rows.  Padding rows of an expert's last block get
 // zero scales; a block past the expert's rows writes nothing.
 template <int STAGES, bool GROUPED, int EPI = 0>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(pair_threads(EPI), 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmY,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(ready_bar(s), 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 2 * NUM_EPI_WARPS);  // every epilogue warp of the pair
+        mbar_init(acc_empty, 2 * pair_epi_warps(EPI));  // every epilogue warp of the pair
         mbar_init(drain_bar, 1);
         mbar_init(drain_bar2, 1);
         *abort_flag = 0;
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     griddep_wait();
 
     if (GROUPED) {
-        for (int e = threadIdx.x; e <= p.E; e += THREADS) s_off[e] = p.offsets[e];
+        for (int e = threadIdx.x; e <= p.E; e += static_cast<int>(blockDim.x)) s_off[e] = p.offsets[e];
         __syncthreads();
         if (threadIdx.x == 0) {
             int32_t pairs = 0, rows = 0;
@@ -525,6 +528,74 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_commit_pair(drain_bar2);
             wait_fixed(drain_bar2, 0);
+        }
+        __syncwarp();
+    } else if constexpr (EPI == 1) {
+        // ------------------------------------ epilogue: gate+up, 32-channel blocks
+        // warp (q, half, sub): rows 32q.. of this CTA, channels 32 sub .. of the
+        // 64-channel chunk in columns half * 128 .. (gate columns 32 sub .., up
+        // columns 64 + 32 sub ..): one MX block of h per row
+        const int ew = warp - EPI_WARP0;
+        const int q = warp & 3;
+        const int half = (ew >> 2) & 1;
+        const int sub = ew >> 3;
+        const uint32_t leader_acc_empty = mapa_shared(acc_empty, 0);
+        uint32_t tc = 0;
+        for (int64_t u = first_unit; u < total_units; u += unit_stride, ++tc) {
+            Tile ti;
+            tile_of(u, ti);
+            if (warp == EPI_WARP0) MACAQ_TRACE(6, tc);
+            if (!warp_wait_bounded(acc_full, tc & 1u, abort_flag, kErrEpilogue, wait_ns)) break;
+            if (warp == EPI_WARP0) MACAQ_TRACE(7, tc);
+            tc_fence_after();
+            uint32_t g[32], up[32];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + half * 128 + 32 * sub;
+            tmem_ld_32x32b_x32(taddr, g);
+            tmem_ld_32x32b_x32(taddr + 64, up);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+            if (warp == EPI_WARP0) MACAQ_TRACE(8, tc);
+
+            if (ti.rows_valid <= 0 || half * 128 >= ti.ncols) continue;
+            const int32_t c0 = ((ti.n0 + half * 128) >> 7) * 64 + 32 * sub;  // this warp's 32 channels
+            if (c0 >= p.F) continue;
+            const int r = 32 * q + lane;
+            const int64_t prow = static_cast<int64_t>(ti.a_row) + r;
+            uint32_t sbyte = 0;
+            if (r < ti.rows_valid) {
+                uint32_t h[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __nv_bfloat162 gb = __floats2bfloat162_rn(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                    const __nv_bfloat162 ub =
+                        __floats2bfloat162_rn(__uint_as_float(up[2 * i]), __uint_as_float(up[2 * i + 1]));
+                    h[i] = mx::silu_mul_word(*reinterpret_cast<const uint32_t *>(&gb),
+                                             *reinterpret_cast<const uint32_t *>(&ub));
+                }
+                const float4 *f4 = reinterpret_cast<const float4 *>(p.h_f + static_cast<int64_t>(ti.expert) * p.F + c0);
+                float2 f[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 a4 = __ldg(f4 + j);
+                    f[2 * j] = make_float2(a4.x, a4.y);
+                    f[2 * j + 1] = make_float2(a4.z, a4.w);
+                }
+                uint4 codes;
+                sbyte = mx::quant_block_pairs<false>(h, f, codes);
+                *reinterpret_cast<uint4 *>(p.h_codes + prow * (p.F / 2) + c0 / 2) = codes;
+            }
+            // the row's scale byte (zero on padding rows), and after the last
+            // block the row's padding scale columns
+            const int64_t rb = (prow >> 7) * p.h_nka;
+            const int64_t in_atom = (prow & 31) * 16 + ((prow & 127) >> 5) * 4;
+            const int32_t kb = c0 / 32;
+            p.h_scales[(rb + (kb >> 2)) * 512 + in_atom + (kb & 3)] = static_cast<uint8_t>(sbyte);
+            if (c0 + 32 == p.F) {
+                for (int32_t k2 = kb + 1; k2 < p.h_pad_cols; ++k2)
+                    p.h_scales[(rb + (k2 >> 2)) * 512 + in_atom + (k2 & 3)] = 0;
+            }
         }
         __syncwarp();
     } else {
@@ -999,7 +1070,7 @@ cudaError_t launch_pair(const GemmArgs &g, cudaStream_t stream, int slot)
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(pair_threads(EPI));
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
