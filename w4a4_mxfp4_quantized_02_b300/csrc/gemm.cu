@@ -187,10 +187,10 @@ struct PairLayout {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_STAGE;
     // store staging per epilogue warp: one 32 x 16 buffer beside six stages;
-    // beside four (short K: the next tile's accumulator is full after three or
-    // four stages) all eight of a warp's 128 columns, written in one pass and
-    // published to the store unit by one proxy fence
-    static constexpr int EPI_NBUF = STAGES >= 6 ? 1 : 8;
+    // beside five (short K: the next tile's accumulator is full after three or
+    // four stages) four, beside four all eight of a warp's 16-column pieces,
+    // written in batches that one proxy fence each publishes to the store unit
+    static constexpr int EPI_NBUF = STAGES >= 6 ? 1 : STAGES == 5 ? 4 : 8;
     static constexpr int OFF_BAR = OFF_EPI + NUM_EPI_WARPS * EPI_NBUF * EPI_BUF;
     static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -688,13 +688,15 @@ __global__ void __launch_bounds__(pair_threads(EPI), 1)
             // in Y, so a warp with some of them stores row by row.
             const bool use_tma = !GROUPED || row0 + 32 <= ti.rows_valid;
             const bool my_row = row0 + lane < ti.rows_valid;
-            if (L::EPI_NBUF >= 8 && use_tma) {
-                // the previous tile's stores must be done reading the staging
+            if (L::EPI_NBUF >= 4 && use_tma) {
+#pragma unroll
+              for (int c0 = 0; c0 < 8; c0 += L::EPI_NBUF) {
+                // the previous batch's stores must be done reading the staging
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
                 int nchunks = 0;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = c0; c < c0 + L::EPI_NBUF; ++c) {
                     if (ti.n0 + half * 128 + 16 * c >= p.N) break;
                     uint32_t packed[8];
 #pragma unroll
@@ -704,7 +706,7 @@ __global__ void __launch_bounds__(pair_threads(EPI), 1)
                         const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
                         packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
                     }
-                    const uint32_t buf = ebuf + c * EPI_BUF;
+                    const uint32_t buf = ebuf + (c - c0) * EPI_BUF;
                     const uint32_t sw = (lane >> 2) & 1;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * sw),
                                  "r"(packed[0]), "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
@@ -719,9 +721,11 @@ __global__ void __launch_bounds__(pair_threads(EPI), 1)
                 if (lane == 0) {
                     // rows past M and columns past N are clipped by the stores
                     for (int c = 0; c < nchunks; ++c)
-                        tma_store_2d(&tmY, ebuf + c * EPI_BUF, ti.n0 + half * 128 + 16 * c, ti.y_row0 + row0);
+                        tma_store_2d(&tmY, ebuf + c * EPI_BUF, ti.n0 + half * 128 + 16 * (c0 + c), ti.y_row0 + row0);
                     bulk_commit();
                 }
+                if (nchunks < L::EPI_NBUF) break;
+              }
             } else {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -1290,11 +1294,11 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     // everything else: CTA pairs on 256 x 256 tiles (grouped: per-expert B)
     if (g.E > 0 && g.epi == 1) return launch_pair<6, true, 1>(g, stream, 0);
     if (g.E > 0 && g.epi == 2) return launch_pair<6, true, 2>(g, stream, 1);
-    // at most four 256-wide K stages per tile: four stages and four store
-    // buffers per epilogue warp
+    // at most four 256-wide K stages per tile: five stages and batched store
+    // staging (four 16-column pieces per warp and proxy fence)
     const bool short_k = g.K <= 4 * 256;
-    if (g.E > 0) return short_k ? launch_pair<4, true>(g, stream, 13) : launch_pair<6, true>(g, stream, 7);
-    return short_k ? launch_pair<4, false>(g, stream, 14) : launch_pair<6, false>(g, stream, 3);
+    if (g.E > 0) return short_k ? launch_pair<5, true>(g, stream, 13) : launch_pair<6, true>(g, stream, 7);
+    return short_k ? launch_pair<5, false>(g, stream, 14) : launch_pair<6, false>(g, stream, 3);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)
