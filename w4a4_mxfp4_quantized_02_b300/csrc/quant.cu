@@ -404,10 +404,12 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
 // 96 registers each, so the warps of the one resident CTA hide more latency.
 constexpr int kTmaConsumersMax = 640;
 constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
-// The grouped kernel keeps its balance factors in registers (they change with
-// the expert): 16 consumer warps.
-constexpr int kGroupedConsumersMax = 512;
-constexpr int kGroupedThreadsMax = kGroupedConsumersMax + 32;
+// The grouped kernel takes its balance factors from a shared-memory table of
+// the first kGroupedFacSlots experts of its rows (L1 for any further expert):
+// up to 20 consumer warps, as the dense kernel; 16 when it also forms the
+// SwiGLU step (more registers per thread).
+__host__ __device__ constexpr int grouped_consumers_max(bool silu) { return silu ? 512 : 640; }
+constexpr int kGroupedFacSlots = 4;
 
 // kOut: kOutMx writes MXFP4 codes and scales; kOutBf16 the normalised
 // transform as bf16 (the W4A16 activation) to a.codes viewed as bf16
@@ -599,7 +601,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 // h = SiLU(g) * u before the transform.
 
 template <int STAGES, bool kSilu, bool kH64>
-__global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(grouped_consumers_max(kSilu) + 32, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
                                                                     int32_t RT, int32_t per_cta)
 {
@@ -620,6 +622,9 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     int32_t *m_src = s_poff + (kMaxExperts + 1);  // token row, -2 past the end
     int32_t *m_exp = m_src + per_cta * RT;
     int32_t *m_dst = m_exp + per_cta * RT;        // padded output row
+    // factor table: slot x TB blocks x 32 floats, block bx's 16-byte chunk c at
+    // position (c + bx) mod 8 (conflict-free reads)
+    const uint32_t ftab = (ptx::smem_u32(m_dst + per_cta * RT) + 15u) & ~15u;
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int32_t slab0 = static_cast<int32_t>(blockIdx.x) * TB;
@@ -728,10 +733,24 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
     const int64_t kb = static_cast<int64_t>(slab0) + tx;
     const bool has_kb = kb < nkb;
     const bool writes_scale = (lane & 3) == 0 && kb < nkb_pad;
-    float2 f[16];
-    int32_t cur_e = -1;
     const uint32_t swz = (static_cast<uint32_t>(t) >> 1) & 3u;
     const int64_t half_k = a.K / 2;
+    // the factors of this CTA's first experts (its rows are sorted by expert),
+    // filled while the producer's first copies are in flight
+    const int32_t e_lo = my_groups > 0 ? m_exp[0] : 0;
+    for (int idx = t; idx < kGroupedFacSlots * TB * 8; idx += NC) {
+        const int slot = idx / (TB * 8), rem = idx - slot * (TB * 8);
+        const int bx = rem >> 3, c = rem & 7;
+        const int32_t e = e_lo + slot;
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < a.E && slab0 + bx < nkb)
+            v4 = __ldg(reinterpret_cast<const float4 *>(a.f + static_cast<int64_t>(e) * a.K + 32 * (slab0 + bx)) + c);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         ftab + static_cast<uint32_t>(slot * TB * 128 + 128 * bx + 16 * ((c + bx) & 7))),
+                     "f"(v4.x), "f"(v4.y), "f"(v4.z), "f"(v4.w)
+                     : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory");
 
     for (int32_t j = 0; j < my_groups; ++j) {
         const int s = j % STAGES;
@@ -786,11 +805,22 @@ __global__ void __launch_bounds__(kGroupedThreadsMax, 1) quant_grouped_tma_kerne
 #pragma unroll
                 for (int i = 0; i < 16; ++i) raw[i] = silu_mul_word(raw[i], up[i]);
             }
-            // the row's expert factors: kept across rows of the same expert,
-            // except in the SwiGLU path, which reloads them (from L1) after h
-            // is formed so that they are not live during the SwiGLU step
-            if (kSilu || ex != cur_e) {
-                cur_e = ex;
+            // the row's expert factors: from the table, or from L1 for an
+            // expert past the table's slots
+            float2 f[16];
+            const int slot = ex - e_lo;
+            if (slot < kGroupedFacSlots) {
+                const uint32_t fb = ftab + static_cast<uint32_t>(slot * TB * 128 + 128 * tx);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float x0, x1, x2, x3;
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3)
+                                 : "r"(fb + 16 * ((c + tx) & 7)));
+                    f[2 * c] = make_float2(x0, x1);
+                    f[2 * c + 1] = make_float2(x2, x3);
+                }
+            } else {
                 const float4 *f4 = reinterpret_cast<const float4 *>(a.f + static_cast<int64_t>(ex) * a.K + 32 * kb);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -1084,7 +1114,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     const int64_t nkb_pad = pad_scale_cols(a.K);
     int64_t tb = 0, rt = 0;
     // SwiGLU rows land two slabs (gate and up) per row
-    if (!pick_tma_tile(nkb_pad, kGroupedConsumersMax, 32768, &tb, &rt)) return cudaSuccess;
+    if (!pick_tma_tile(nkb_pad, grouped_consumers_max(silu), silu ? 32768 : 40960, &tb, &rt)) return cudaSuccess;
     const int64_t slabs = (nkb_pad + tb - 1) / tb;
     const int64_t stage = tb * rt * 64 * (silu ? 2 : 1);
     int sms = 148;
@@ -1097,7 +1127,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     ctas_y = (groups + per_cta - 1) / per_cta;
     const int64_t max_rows = per_cta * rt;
     if (max_rows > 4096) return cudaSuccess;  // row table too large: register-staged kernel
-    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 3 * max_rows * 4 + 1024;
+    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 3 * max_rows * 4 + 16 + kGroupedFacSlots * tb * 128 + 1024;
     const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : (4 * stage + 16 * 4 + fixed <= 210 * 1024) ? 4 : 3;
     const int64_t smem = stages * stage + 16 * stages + fixed;
     if (smem > 210 * 1024) return cudaSuccess;
