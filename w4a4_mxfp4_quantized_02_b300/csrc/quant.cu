@@ -405,11 +405,11 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
 constexpr int kTmaConsumersMax = 640;
 constexpr int kTmaThreadsMax = kTmaConsumersMax + 32;
 // The grouped kernel takes its balance factors from a shared-memory table of
-// the first kGroupedFacSlots experts of its rows (L1 for any further expert):
-// up to 20 consumer warps, as the dense kernel; 16 when it also forms the
-// SwiGLU step (more registers per thread).
+// the first experts of its rows (up to four, as shared memory allows; L1 for
+// any further expert): up to 20 consumer warps, as the dense kernel; 16 when
+// it also forms the SwiGLU step (more registers per thread).
 __host__ __device__ constexpr int grouped_consumers_max(bool silu) { return silu ? 512 : 640; }
-constexpr int kGroupedFacSlots = 4;
+constexpr int kGroupedFacSlotsMax = 4;
 
 // kOut: kOutMx writes MXFP4 codes and scales; kOutBf16 the normalised
 // transform as bf16 (the W4A16 activation) to a.codes viewed as bf16
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
 template <int STAGES, bool kSilu, bool kH64>
 __global__ void __launch_bounds__(grouped_consumers_max(kSilu) + 32, 1) quant_grouped_tma_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                     QuantArgs a, int32_t groups, int32_t TB,
-                                                                    int32_t RT, int32_t per_cta)
+                                                                    int32_t RT, int32_t per_cta, int32_t fac_slots)
 {
     extern __shared__ uint8_t qsmem_raw[];
     const uint32_t raw_base = ptx::smem_u32(qsmem_raw);
@@ -738,7 +738,7 @@ __global__ void __launch_bounds__(grouped_consumers_max(kSilu) + 32, 1) quant_gr
     // the factors of this CTA's first experts (its rows are sorted by expert),
     // filled while the producer's first copies are in flight
     const int32_t e_lo = my_groups > 0 ? m_exp[0] : 0;
-    for (int idx = t; idx < kGroupedFacSlots * TB * 8; idx += NC) {
+    for (int idx = t; idx < fac_slots * TB * 8; idx += NC) {
         const int slot = idx / (TB * 8), rem = idx - slot * (TB * 8);
         const int bx = rem >> 3, c = rem & 7;
         const int32_t e = e_lo + slot;
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(grouped_consumers_max(kSilu) + 32, 1) quant_gr
             // expert past the table's slots
             float2 f[16];
             const int slot = ex - e_lo;
-            if (slot < kGroupedFacSlots) {
+            if (slot < fac_slots) {
                 const uint32_t fb = ftab + static_cast<uint32_t>(slot * TB * 128 + 128 * tx);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -1127,10 +1127,19 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     ctas_y = (groups + per_cta - 1) / per_cta;
     const int64_t max_rows = per_cta * rt;
     if (max_rows > 4096) return cudaSuccess;  // row table too large: register-staged kernel
-    const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 3 * max_rows * 4 + 16 + kGroupedFacSlots * tb * 128 + 1024;
-    const int stages = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : (4 * stage + 16 * 4 + fixed <= 210 * 1024) ? 4 : 3;
-    const int64_t smem = stages * stage + 16 * stages + fixed;
-    if (smem > 210 * 1024) return cudaSuccess;
+    // the most factor-table slots (4, 2, 1) beside the deepest ring that fits
+    int stages = 0, slots = 0;
+    int64_t smem = 0;
+    for (int sl = kGroupedFacSlotsMax; sl >= 1 && stages == 0; sl /= 2) {
+        const int64_t fixed = 16 + 2 * (kMaxExperts + 1) * 4 + 3 * max_rows * 4 + 16 + sl * tb * 128 + 1024;
+        const int st = (6 * stage + 16 * 6 + fixed <= 200 * 1024) ? 6 : (4 * stage + 16 * 4 + fixed <= 210 * 1024) ? 4 : 3;
+        if (st * stage + 16 * st + fixed <= 210 * 1024) {
+            stages = st;
+            slots = sl;
+            smem = st * stage + 16 * st + fixed;
+        }
+    }
+    if (stages == 0) return cudaSuccess;
     CUtensorMap tm;
     // the token rows are whatever row_src names (valid by contract): no row bound
     // (SwiGLU: the gate|up row holds 2 * K / 32 blocks)
@@ -1140,7 +1149,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     if (!encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.src, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaSuccess;
-    void (*kern)(CUtensorMap, QuantArgs, int32_t, int32_t, int32_t, int32_t);
+    void (*kern)(CUtensorMap, QuantArgs, int32_t, int32_t, int32_t, int32_t, int32_t);
     if (a.had == 64)
         kern = silu ? (stages == 6 ? quant_grouped_tma_kernel<6, true, true>
                                    : stages == 4 ? quant_grouped_tma_kernel<4, true, true>
@@ -1160,7 +1169,7 @@ cudaError_t launch_quant_grouped_tma(const QuantArgs &a, bool silu, cudaStream_t
     dim3 block(static_cast<unsigned>(tb * rt + 32));
     MACAQ_TRY_CUDA(launch_pdl(kern, grid, block, static_cast<size_t>(smem), stream, tm, a,
                               static_cast<int32_t>(groups), static_cast<int32_t>(tb), static_cast<int32_t>(rt),
-                              static_cast<int32_t>(per_cta)));
+                              static_cast<int32_t>(per_cta), static_cast<int32_t>(slots)));
     *done = true;
     return cudaGetLastError();
 }
