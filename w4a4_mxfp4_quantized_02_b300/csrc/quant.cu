@@ -1189,7 +1189,10 @@ cudaError_t launch_quant(QuantMode mode, const QuantArgs &a, cudaStream_t stream
             best_t = t;
         }
     }
-    if (mode == QuantMode::Dense && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1) {
+    // a few rows (decode): the register-staged kernel spreads them over more
+    // CTAs than the TMA ring's row groups, for a shorter launch
+    const bool few_rows = a.rows_valid <= 64 && a.had == 32 && a.out_kind == kOutMx;
+    if (mode == QuantMode::Dense && (a.ld_src * 2) % 16 == 0 && a.rows_valid >= 1 && !few_rows) {
         bool done = false;
         cudaError_t err = launch_quant_dense_tma(a, stream, &done);
         if (err != cudaSuccess || done) return err;
