@@ -519,10 +519,11 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
                           if fused else {})),
         "roofline": roofline,
         "act_quant": {"kernel": "quant_grouped_tma_kernel<.., true> (SwiGLU, one group)" if fused
+                      else "quant_kernel (register-staged: a few rows)" if M <= 64 and hb == 32
                       else "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": quant_gbs / peaks["hbm_gbs"], "bytes_per_launch": quant_bytes,
-                      "traffic": None if fused else recorded_traffic("quant_dense_tma_kernel", wl.name),
+                      "traffic": None if fused or (M <= 64 and hb == 32) else recorded_traffic("quant_dense_tma_kernel", wl.name),
                       "avg_launch_us": quant_avg * 1e3},
         "cpu_baseline": cpu,
         "e2e": None if light else {
