@@ -169,7 +169,8 @@ __device__ __forceinline__ bool wait_fixed(uint32_t bar, uint32_t parity)
 //   warp 2      rank 0: scale copier (tcgen05.cp into both CTAs' tensor
 //               memory, each from its own shared memory).
 //   warps 3..10 epilogue, each CTA for its own 128 rows; release of the
-//               accumulator is an arrival on rank 0's barrier.
+//               accumulator is an arrival on rank 0's barrier (warps 3..18
+//               for the gate+up epilogue with 32-channel blocks, EPI 1).
 template <int STAGES>
 struct PairLayout {
     static constexpr int BN = 256;           // tile columns (both CTAs)
