@@ -3,7 +3,9 @@
 
 One step = the whole online hot path on one batch: the activation transform
 (balance, 32-channel block Hadamard, MXFP4 encode; one CUDA kernel) followed by
-the block-scaled MXFP4 GEMM (one tcgen05 kernel), i.e. ``macaq_linear`` on the
+the block-scaled MXFP4 GEMM (one tcgen05 kernel) -- up to 6 token rows one
+kernel does both (``macaq_linear``: the transform inside the few-rows GEMM) --
+i.e. ``macaq_linear`` on the
 prefill MLP down-projection M=8192 tokens, K=25600, N=5120 (the largest
 single-GPU configuration; ``--config`` picks another workload).  Weights are
 prepared once, outside the timed region (balance from a 512-row calibration
@@ -89,6 +91,16 @@ class _NvmlCtypes:
         self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(c))
         return c.value
 
+    def mem_clock(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 2, self.ct.byref(c))  # NVML_CLOCK_MEM
+        return c.value
+
+    def max_mem_clock(self):
+        c = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 2, self.ct.byref(c))
+        return c.value
+
     def reasons(self):
         r = self.ct.c_ulonglong()
         self._reasons(self.h, self.ct.byref(r))
@@ -96,7 +108,8 @@ class _NvmlCtypes:
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event (throttle) reasons through NVML while running."""
+    """Samples SM and memory clocks and clock-event (throttle) reasons through NVML
+    while running (read-only queries: no setting of the GPU is changed)."""
 
     REASONS = {
         0x0000000000000001: "gpu_idle", 0x0000000000000002: "applications_clocks_setting",
@@ -108,6 +121,7 @@ class ClockSampler:
 
     def __init__(self, bus_id: str | None, period_s: float = 0.001):
         self.samples = []
+        self.mem_samples = []
         self.reasons = set()
         self.period = period_s
         self.ok = False
@@ -115,6 +129,7 @@ class ClockSampler:
         try:
             self.nv = _NvmlCtypes(bus_id)
             self.max_mhz = self.nv.max_sm_clock()
+            self.max_mem_mhz = self.nv.max_mem_clock()
             self.ok = True
         except Exception as e:  # noqa: BLE001 - clocks are then reported as unavailable
             self.err = str(e)
@@ -125,6 +140,7 @@ class ClockSampler:
         while not self._stop.is_set():
             try:
                 self.samples.append(self.nv.sm_clock())
+                self.mem_samples.append(self.nv.mem_clock())
                 r = self.nv.reasons()
                 for bit, name in self.REASONS.items():
                     if r & bit:
@@ -149,7 +165,8 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.err}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
-                "samples": len(self.samples)}
+                "mem_mhz": statistics.median(self.mem_samples) if self.mem_samples else None,
+                "mem_max_mhz": self.max_mem_mhz, "samples": len(self.samples)}
 
 
 def pci_bus_id(dev) -> str | None:
@@ -323,6 +340,10 @@ def gemm_kernel_name(M: int) -> str:
     return "gemm_mxf4_skinny_kernel" if M <= 64 else "gemm_mxf4_pair_kernel"
 
 
+FUSED_LINEAR_MAX_ROWS = 6    # macaq_linear: one launch, the transform inside the few-rows GEMM
+FUSED_LINEAR_KERNEL = "gemm_mxf4_skinny_kernel<16, 5, true>"
+
+
 # ------------------------------------------------------------------- GPU arm
 
 def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool = False):
@@ -356,6 +377,9 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     w_codes, w_scales = mq.macaq_quant_weight_hb(W, s, hb)
     del W, Xc
 
+    # up to 6 token rows (Hadamard block 32) the layer is one launch
+    # (macaq_linear: the transform inside the few-rows GEMM)
+    one_launch = not fused and hb == 32 and M <= FUSED_LINEAR_MAX_ROWS
     ws_bytes = mq.macaq_linear_workspace_bytes(M, K)
     step_bytes = M * xcols * 2 + ws_bytes * 2 + w_codes.numel() + w_scales.numel() + M * N * 2
     nsets = max(2, math.ceil(2.5 * L2_BYTES / step_bytes) + 1)
@@ -369,7 +393,12 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
             "Y": torch.empty(M, N, dtype=torch.bfloat16, device=dev),
             "a_codes": torch.empty(M, K // 2, dtype=torch.uint8, device=dev),
             "a_scales": torch.empty(mq.macaq_scale_bytes(M, K), dtype=torch.uint8, device=dev),
+            "lws": torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev),
         })
+
+    def linear_part(i):
+        b = sets[i % nsets]
+        mq.macaq_linear(b["X"], inv, b["wc"], b["ws"], N, Y=b["Y"], workspace=b["lws"])
 
     def quant_part(i):
         b = sets[i % nsets]
@@ -382,9 +411,11 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         b = sets[i % nsets]
         mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
 
+    parts = [linear_part] if one_launch else [quant_part, gemm_part]
+
     def step(i):
-        quant_part(i)
-        gemm_part(i)
+        for part in parts:
+            part(i)
 
     for i in range(args.warmup):
         step(i)
@@ -395,7 +426,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     chunk = nsets * max(1, math.ceil(8 / nsets))
     graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
-    batches = KernelBatches(plan.eager_steps, min(nsets, 4), 2)
+    batches = KernelBatches(plan.eager_steps, min(nsets, 4), len(parts))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -407,7 +438,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         h0 = time.perf_counter()
         for _ in range(plan.replays):
             graph.replay()
-        batches.run([quant_part, gemm_part], stream)
+        batches.run(parts, stream)
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -415,7 +446,11 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    quant_avg, gemm_avg = batches.per_launch_ms()
+    if one_launch:
+        (gemm_avg,) = batches.per_launch_ms()
+        quant_avg = None
+    else:
+        quant_avg, gemm_avg = batches.per_launch_ms()
     status = mq.macaq_check_device_error()
     if status != 0:
         raise RuntimeError(f"device error in the timed region: {mq.macaq_status_string(status)}")
@@ -424,7 +459,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     value = flops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
     gemm_tflops = flops / (gemm_avg * 1e-3) / 1e12
     quant_bytes = M * xcols * 2 + M * K // 2 + M * K // 32
-    quant_gbs = quant_bytes / (quant_avg * 1e-3) / 1e9
+    quant_gbs = None if quant_avg is None else quant_bytes / (quant_avg * 1e-3) / 1e9
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
 
     e2e_value = e2e_ms = e2e_serial_ms = None
@@ -466,7 +501,8 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
                                lambda k: Yh[k].copy_(sets[k]["Y"], non_blocking=True))
         e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
 
-    traffic = recorded_traffic(gemm_kernel_name(M), wl.name)
+    gemm_kernel = FUSED_LINEAR_KERNEL if one_launch else gemm_kernel_name(M)
+    traffic = recorded_traffic(gemm_kernel, wl.name)
 
     if rank != 0:
         return None
@@ -483,10 +519,12 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
 
     # the GEMM's bound: FP4 tensor throughput above the ridge intensity, HBM
     # bytes below it (decode: the weight bytes)
-    gemm_bytes = M * (K // 2 + K // 32) + N * (K // 2 + K // 32) + M * N * 2
+    # (one launch: the kernel reads X in bf16 instead of the transformed codes)
+    x_bytes = M * K * 2 if one_launch else M * (K // 2 + K // 32)
+    gemm_bytes = x_bytes + N * (K // 2 + K // 32) + M * N * 2
     timing = (f"CUDA events around kernel groups: {batches.describe()} of the {args.steps} timed steps")
     if flops / gemm_bytes >= fp4_peak * 1e12 / (peaks["hbm_gbs"] * 1e9):
-        roofline = {"bound": "tensor", "kernel": gemm_kernel_name(M),
+        roofline = {"bound": "tensor", "kernel": gemm_kernel,
                     "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
                     "frac": gemm_tflops / fp4_peak, "traffic": traffic,
                     "peak_note": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x "
@@ -495,7 +533,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     else:
         gbs = gemm_bytes / (gemm_avg * 1e-3) / 1e9
         roofline = {"bound": "hbm",
-                    "kernel": gemm_kernel_name(M),
+                    "kernel": gemm_kernel,
                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "bytes_per_launch": gemm_bytes,
                     "peak_note": f"{peaks['source']} HBM copy bandwidth",
@@ -518,7 +556,10 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
                        **({"input": "gate|up [M, 2K]; SiLU(gate) * up fused into the transform"}
                           if fused else {})),
         "roofline": roofline,
-        "act_quant": {"kernel": "quant_grouped_tma_kernel<.., true> (SwiGLU, one group)" if fused
+        "act_quant": {"kernel": f"inside {FUSED_LINEAR_KERNEL} (no launch of its own)", "achieved": None,
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": None, "bytes_per_launch": 0,
+                      "traffic": None, "avg_launch_us": None} if one_launch else
+                     {"kernel": "quant_grouped_tma_kernel<.., true> (SwiGLU, one group)" if fused
                       else "quant_kernel (register-staged: a few rows)" if M <= 64 and hb == 32
                       else "quant_dense_tma_kernel", "achieved": quant_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -531,7 +572,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
             "d2h_bytes_per_step": M * N * 2, "ms_per_step": e2e_ms,
             "copies": f"overlapped across steps ({nslot} buffer slots, separate copy streams)",
             "serial_ms_per_step": e2e_serial_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": len(parts) * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "clocks": sampler.summary(),
@@ -1301,6 +1342,7 @@ def capture_graph(fn):
 KERNEL_SOURCES = {
     "gemm_mxf4_pair_kernel": ("gemm.cu", "ptx.cuh", "mx_block.cuh", "internal.h"),
     "gemm_mxf4_skinny_kernel": ("gemm.cu", "gemm_skinny.cuh", "ptx.cuh", "internal.h"),
+    FUSED_LINEAR_KERNEL: ("gemm.cu", "gemm_skinny.cuh", "ptx.cuh", "mx_block.cuh", "internal.h"),
     "gemm_w4a16_kernel": ("gemm.cu", "gemm_w4a16.cuh", "ptx.cuh", "internal.h"),
     "quant_dense_tma_kernel": ("quant.cu", "mx_block.cuh", "ptx.cuh", "internal.h"),
 }

@@ -163,7 +163,10 @@ size_t macaq_linear_workspace_bytes(int64_t M, int64_t K);
 /* The whole online layer: macaq_quant_act into `workspace`, then
  * macaq_w4a4_gemm, both on `stream`.  Y = X diag(1/s) H (W diag(s) H)^T up
  * to MXFP4 rounding.  workspace: device, ws_bytes >=
- * macaq_linear_workspace_bytes(M, K), 256-byte aligned, contents scratch. */
+ * macaq_linear_workspace_bytes(M, K), 256-byte aligned, contents scratch.
+ * Up to 6 token rows (decode) both steps run as one kernel -- the GEMM forms
+ * the transformed token rows itself, stage by stage -- and the workspace is
+ * left untouched; Y is bit for bit the two calls' result either way. */
 macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s,
                           const uint8_t *w_codes, const uint8_t *w_scales, int64_t M,
                           int64_t N, int64_t K, void *Y, int64_t ldy, void *workspace,

@@ -167,3 +167,36 @@ def test_linear_workspace_matches_two_calls(M, N, K):
     np.testing.assert_array_equal(u8(ws[:nc]).reshape(M, K // 2), u8(a_codes))
     np.testing.assert_array_equal(u8(ws[off:off + a_scales.numel()]), u8(a_scales))
     assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 32), (2, 200, 288), (5, 1000, 1056), (6, 256, 4096),
+                                   (3, 25600, 256), (6, 520, 5152), (4, 2048, 5120), (7, 2048, 5120)])
+def test_linear_few_rows_fused(M, N, K):
+    """Up to 6 token rows macaq_linear forms the token operand inside the
+    few-rows GEMM (one launch; 7 rows: the two launches).  Y must equal
+    macaq_quant_act + macaq_w4a4_gemm bit for bit -- the same codes, scales
+    and MMAs -- across K not a multiple of 256, N not a multiple of 128, a
+    strided X with a zero row, and few weight tiles with long K (K split over
+    a cluster); and it must agree with the oracle."""
+    Xs = workloads.make_matrix(M, K + 40, seed=7 * M + K, outlier_channels=(3, K - 5))
+    Xs[M // 2, :] = 0.0
+    X = Xs[:, :K]
+    Xc = workloads.make_matrix(64, K, seed=5 + K, outlier_channels=(3, K - 5))
+    W = workloads.make_weight(N, K, seed=N + K)
+    s_ref, inv_ref = oracle.balance_scales(Xc, W)
+    s, inv = mq.macaq_balance_scales(to_dev(Xc), to_dev(W))
+    w_codes, w_scales = mq.macaq_quant_weight(to_dev(W), s)
+    Xd = to_dev(Xs)[:, :K]
+    assert Xd.stride(0) == K + 40
+    Y = mq.macaq_linear(Xd, inv, w_codes, w_scales, N)
+    a_codes, a_scales = mq.macaq_quant_act(Xd, inv)
+    Y2 = mq.macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K)
+    torch.cuda.synchronize()
+    assert mq.macaq_check_device_error() == 0
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert torch.all(Y[M // 2] == 0)
+    ca, sa = oracle.quantize(X, inv_ref)
+    cw, sw = oracle.quantize(W, s_ref)
+    da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
+    frac, canc = check_gemm(bf16_to_np(Y), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
+    assert frac > 0.999, (frac, canc)

@@ -247,6 +247,25 @@ macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s, const 
     if (!X || !inv_s || !w_codes || !w_scales || !Y || ldx < K || ldy < N) return MACAQ_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < macaq_linear_workspace_bytes(M, K)) return MACAQ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MACAQ_ERR_ALIGNMENT;
+    if (M <= kFusedLinearMaxRows) {
+        // a few token rows (decode): one launch, the transform inside the GEMM
+        // (the same checks as the two calls below make)
+        if (!aligned16(X) || !aligned16(inv_s) || ldx % 8 != 0 || !aligned16(w_codes) ||
+            !aligned16(w_scales) || !aligned16(Y) || ldy % 8 != 0)
+            return MACAQ_ERR_ALIGNMENT;
+        GemmArgs g{};
+        g.w_codes = w_codes;
+        g.w_scales = w_scales;
+        g.M = M;
+        g.a_rows = M;
+        g.N = N;
+        g.K = K;
+        g.E = 0;
+        g.Y = Y;
+        g.ldy = ldy;
+        return from_cuda(launch_linear_fused(g, static_cast<const uint16_t *>(X), ldx, inv_s,
+                                             static_cast<cudaStream_t>(stream)));
+    }
     uint8_t *a_codes = static_cast<uint8_t *>(workspace);
     uint8_t *a_scales = a_codes + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
     MACAQ_TRY(macaq_quant_act(X, ldx, inv_s, M, K, a_codes, a_scales, stream));

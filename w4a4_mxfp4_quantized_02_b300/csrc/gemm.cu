@@ -1121,15 +1121,18 @@ bool encode_tensor_map(CUtensorMap *m, CUtensorMapDataType dt, uint32_t rank, co
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NT, int STAGES>
-cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
+// FUSED: x / ldx / inv carry the layer input and balance factors, and the
+// kernel forms the token operand itself (a_codes / a_scales unused).
+template <int NT, int STAGES, bool FUSED = false>
+cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot, const uint16_t *x = nullptr,
+                          int64_t ldx = 0, const float *inv = nullptr)
 {
     using L = skinny::Layout<NT, STAGES>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kern = skinny::gemm_mxf4_skinny_kernel<NT, STAGES>;
+    auto kern = skinny::gemm_mxf4_skinny_kernel<NT, STAGES, FUSED>;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         DeviceInfo &di = g_dev[dev];
@@ -1156,7 +1159,9 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
                     CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    {
+    if (FUSED) {
+        std::memset(&tmX, 0, sizeof(tmX));  // the token operand is formed in the kernel: never read
+    } else {
         uint64_t dims[2] = {kb, static_cast<uint64_t>(g.M)};
         uint64_t strides[1] = {kb};
         uint32_t box[2] = {128, NT};
@@ -1167,6 +1172,10 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
     skinny::Params p;
     p.sfw = g.w_scales;
     p.sfx = g.a_scales;
+    p.x = x;
+    p.ldx = ldx;
+    p.inv = inv;
+    p.nkb = static_cast<int32_t>(g.K / 32);
     p.Y = static_cast<uint16_t *>(g.Y);
     p.ldy = g.ldy;
     p.M = static_cast<int32_t>(g.M);
@@ -1180,7 +1189,7 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot)
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_tiles * ks));
-    cfg.blockDim = dim3(skinny::kThreads);
+    cfg.blockDim = dim3(skinny::skinny_threads(FUSED));
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1300,6 +1309,13 @@ cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream)
     const bool short_k = g.K <= 4 * 256;
     if (g.E > 0) return short_k ? launch_pair<5, true>(g, stream, 13) : launch_pair<6, true>(g, stream, 7);
     return short_k ? launch_pair<5, false>(g, stream, 14) : launch_pair<6, false>(g, stream, 3);
+}
+
+cudaError_t launch_linear_fused(const GemmArgs &g, const uint16_t *X, int64_t ldx, const float *inv_s,
+                                cudaStream_t stream)
+{
+    if (g.E != 0 || g.M > kFusedLinearMaxRows) return cudaErrorNotSupported;
+    return launch_skinny<16, 5, true>(g, stream, 15, X, ldx, inv_s);
 }
 
 cudaError_t read_and_clear_device_error(unsigned *flags)

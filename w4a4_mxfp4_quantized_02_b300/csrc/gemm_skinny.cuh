@@ -19,12 +19,30 @@
 //
 // Warps: 0 TMA producer, 1 MMA issuer, 2 scale copier, 3..6 epilogue (tensor
 // memory lanes 0..127 = the tile's weight rows).
+//
+// FUSED (the whole online layer for a few token rows, NT = 16): the token
+// operand is not read from a transformed copy in HBM but formed inside the
+// kernel, stage by stage, from the bf16 rows of X.  Eight transform warps
+// (3..10; 3..6 then run the epilogue), in four groups that each take every
+// fourth stage, run the work items (stage, token row, 32-value block): each
+// item the balance, 32-point Hadamard, E8M0 scale and E2M1 codes of one
+// block -- the activation transform of the layer, the same arithmetic as the
+// standalone transform -- stored as 16 code bytes into the stage's
+// 128-byte-swizzled token tile and a scale byte into its scale atoms, in the
+// byte positions the TMA copies of the transformed operand would have.  Each
+// item then arrives on the stage's "full" barrier, which so completes once
+// the weight copies and all of the stage's items are in.  The weight stream
+// thus starts right after the grid-dependency wait, with no separate
+// transform launch before it.
 
 namespace skinny {
 
-constexpr int kThreads = 7 * 32;
 constexpr int kEpiWarp0 = 3;
+constexpr int kXformWarps = 8;  // FUSED: warps 3 .. 10 form the token tiles ...
+constexpr int kXformGroups = 4;  // ... in four groups of two warps, each its own stages
+constexpr int kXformGroupThreads = kXformWarps * 32 / kXformGroups;
 constexpr int kTmemCols = 128;
+__host__ __device__ constexpr int skinny_threads(bool fused) { return (fused ? kEpiWarp0 + kXformWarps : 7) * 32; }
 
 template <int NT, int STAGES>
 struct Layout {
@@ -59,10 +77,17 @@ struct Params {
     int32_t M, N;
     int32_t num_kstages;
     int32_t nka;          // 4-scale atoms per 128-row block
+    // FUSED: the layer input X bf16 [M, ldx] and the balance factors 1/s [K]
+    const uint16_t *x;
+    int64_t ldx;
+    const float *inv;
+    int32_t nkb;          // 32-value blocks of K
 };
 
-template <int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// FUSED asks for registers that let two of its CTAs share an SM (as the
+// unfused kernel's fit), so 200 weight tiles still run in one wave.
+template <int NT, int STAGES, bool FUSED = false>
+__global__ void __launch_bounds__(skinny_threads(FUSED), FUSED ? 2 : 1)
     gemm_mxf4_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                             const Params p)
 {
@@ -93,9 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ks_end = static_cast<int>((static_cast<int64_t>(nks) * (ks_rank + 1)) / KS);
     const int my_stages = ks_end - ks_begin;
 
+    // FUSED: token rows 0 .. xrows-1 are formed in the kernel (8 items per
+    // row and stage); the rest of each token tile and every scale byte not
+    // rewritten per stage stay zero, set once here
+    const int xrows = FUSED ? (p.M < NT ? p.M : NT) : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), FUSED ? 1u + 8u * static_cast<uint32_t>(xrows) : 1u);
             mbar_init(empty_bar(s), 1);
             mbar_init(ready_bar(s), 1);
         }
@@ -104,6 +133,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain_bar2, 1);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    if constexpr (FUSED) {
+        for (int i = threadIdx.x; i < STAGES * (L::X_STAGE + L::SF_STAGE) / 16; i += blockDim.x) {
+            const int s = i / ((L::X_STAGE + L::SF_STAGE) / 16);
+            const int o = (i - s * ((L::X_STAGE + L::SF_STAGE) / 16)) * 16;
+            const uint32_t addr = o < L::X_STAGE ? sbase + L::OFF_X + s * L::X_STAGE + o
+                                                 : sbase + L::OFF_SFX + s * L::SF_STAGE + (o - L::X_STAGE);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();
     }
     if (warp == 1) {
         tmem_alloc(sbase + L::OFF_MISC, kTmemCols);
@@ -119,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            constexpr uint32_t kBytes = L::W_STAGE + L::X_STAGE + 2 * L::SF_STAGE;
+            constexpr uint32_t kBytes = FUSED ? L::W_STAGE + L::SF_STAGE : L::W_STAGE + L::X_STAGE + 2 * L::SF_STAGE;
             const uint8_t *sfw = p.sfw + static_cast<size_t>(n0 / 128) * p.nka * SF_ATOM;
             uint32_t issued = 0, last_parity = 0;
             for (int i = 0; i < my_stages; ++i) {
@@ -130,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = full_bar(s);
                 mbar_arrive_expect_tx(fb, kBytes);
                 tma_load_2d(sbase + L::OFF_W + s * L::W_STAGE, &tmW, fb, ks * L::KB, n0);
-                tma_load_2d(sbase + L::OFF_X + s * L::X_STAGE, &tmX, fb, ks * L::KB, 0);
                 bulk_load(sbase + L::OFF_SFW + s * L::SF_STAGE, sfw + static_cast<size_t>(2 * ks) * SF_ATOM,
                           L::SF_STAGE, fb);
-                bulk_load(sbase + L::OFF_SFX + s * L::SF_STAGE, p.sfx + static_cast<size_t>(2 * ks) * SF_ATOM,
-                          L::SF_STAGE, fb);
+                if (!FUSED) {
+                    tma_load_2d(sbase + L::OFF_X + s * L::X_STAGE, &tmX, fb, ks * L::KB, 0);
+                    bulk_load(sbase + L::OFF_SFX + s * L::SF_STAGE,
+                              p.sfx + static_cast<size_t>(2 * ks) * SF_ATOM, L::SF_STAGE, fb);
+                }
                 issued |= 1u << s;
                 last_parity = (last_parity & ~(1u << s)) | (ph << s);
             }
@@ -199,6 +240,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
+        if constexpr (FUSED) {
+            // ------------------------------------------------ token transform
+            // The transform warps form four groups of two; group g takes stages
+            // g, g + 4, g + 8, ... in order, its 64 threads the stage's items
+            // (row r, block b) in turn.  A stage's buffers are free once the
+            // MMAs of stage i - STAGES have read them ("empty", a parity wait).
+            // A parity wait cannot tell a phase from the one two before it, so
+            // no thread may wait more than one phase ahead: a thread's previous
+            // stage was at most 4 <= STAGES stages earlier, and its wait then
+            // proved every stage up to STAGES before that consumed.
+            // Item (i, r, b): the 16 code bytes at row r, 16-byte chunk b of the
+            // stage's token tile (128-byte swizzle: chunk b sits at b ^ (r % 8))
+            // and the scale byte at block b of row r in the stage's two scale
+            // atoms (row 32q + p, block c of an atom at byte 16p + 4q + c);
+            // blocks past K get zero codes and a zero scale.
+            static_assert(kXformGroups <= STAGES, "a transform group may run at most one ring ahead");
+            const int tid = static_cast<int>(threadIdx.x) - kEpiWarp0 * 32;
+            const int grp = tid / kXformGroupThreads, gt = tid % kXformGroupThreads;
+            const int per_stage = 8 * xrows;
+            bool ok = true;
+            for (int i = grp; i < my_stages && ok; i += kXformGroups) {
+                const int s = i % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
+                for (int item = gt; item < per_stage; item += kXformGroupThreads) {
+                    const int r = item >> 3, b = item & 7;
+                    const int32_t kblk = (ks_begin + i) * 8 + b;
+                    uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+                    uint32_t sbyte = 0;
+                    if (kblk < p.nkb) {
+                        uint32_t raw[16];
+                        float2 f[16];
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            p.x + static_cast<int64_t>(r) * p.ldx + 32 * static_cast<int64_t>(kblk));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 w = __ldg(src + j);
+                            raw[4 * j + 0] = w.x;
+                            raw[4 * j + 1] = w.y;
+                            raw[4 * j + 2] = w.z;
+                            raw[4 * j + 3] = w.w;
+                        }
+                        const float4 *f4 = reinterpret_cast<const float4 *>(p.inv + 32 * static_cast<int64_t>(kblk));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 a4 = __ldg(f4 + j);
+                            f[2 * j] = make_float2(a4.x, a4.y);
+                            f[2 * j + 1] = make_float2(a4.z, a4.w);
+                        }
+                        sbyte = mx::quant_block_pairs<false>(raw, f, codes);
+                    }
+                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrEpilogue, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t xa = sbase + L::OFF_X + s * L::X_STAGE + r * L::KB + ((b ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xa), "r"(codes.x),
+                                 "r"(codes.y), "r"(codes.z), "r"(codes.w)
+                                 : "memory");
+                    const uint32_t sa = sbase + L::OFF_SFX + s * L::SF_STAGE + (b >> 2) * SF_ATOM +
+                                        16 * (r & 31) + 4 * (r >> 5) + (b & 3);
+                    asm volatile("st.shared.u8 [%0], %1;" ::"r"(sa), "r"(sbyte) : "memory");
+                    // the tensor core reads both through the async proxy
+                    fence_proxy_async_smem();
+                    mbar_arrive(full_bar(s));
+                }
+            }
+            // lanes leave the loop at different times (each waited for its own
+            // stages); what follows -- tcgen05.ld and the cluster barriers --
+            // is .aligned and must be reached by the whole warp together
+            __syncwarp();
+        }
+    }
+    if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;                 // tensor-memory lanes 32q..32q+31
         const int row = 32 * q + lane;          // weight row within the tile
@@ -263,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
 
-    if (warp < kEpiWarp0) {
+    if (warp < kEpiWarp0 || warp >= kEpiWarp0 + 4) {
         // the non-epilogue warps take part in the epilogue's two cluster barriers
         asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
         asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

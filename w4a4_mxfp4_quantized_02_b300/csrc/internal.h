@@ -105,6 +105,19 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);
 
+// The whole dense layer for a few token rows in one launch: the few-rows GEMM
+// forms its token operand from X bf16 [M, ldx] and the balance factors inv_s
+// [K] (Hadamard block 32) stage by stage, instead of reading a_codes /
+// a_scales (which it ignores).  Every CTA transforms all M rows of its K
+// range, so the work grows with M while the weight stream it hides behind
+// does not: at K = 5120, N = 25600 one launch took 15.2-16.1 us for M = 1..4
+// and 18.9 us for M = 6 against 20.6-21.3 us for the transform and GEMM
+// launches, but 21.8 us for M = 8 against 20.9.  Returns
+// cudaErrorNotSupported for larger M.
+constexpr int64_t kFusedLinearMaxRows = 6;
+cudaError_t launch_linear_fused(const GemmArgs &g, const uint16_t *X, int64_t ldx, const float *inv_s,
+                                cudaStream_t stream);
+
 // W4A16: Y[M, N] = Xt[M, K] . Wd[N, K]^T with Wd the bf16 expansion of the
 // MXFP4 weight (codes [N, K/2], tiled scales), expanded tile by tile in
 // shared memory; bf16 products, fp32 accumulation (tcgen05 kind::f16).
