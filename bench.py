@@ -411,9 +411,17 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         b = sets[i % nsets]
         mq.macaq_w4a4_gemm(b["a_codes"], b["a_scales"], b["wc"], b["ws"], M, N, K, Y=b["Y"])
 
+    # per-kernel timing (the eager kernel-group batches) needs the kernels as
+    # separate calls; the other steps are the layer as a user calls it
+    # (macaq_linear, Hadamard block 32: its GEMM may load its first weight
+    # stages while its own transform still runs)
     parts = [linear_part] if one_launch else [quant_part, gemm_part]
+    layer_call = not fused and hb == 32
 
     def step(i):
+        if layer_call:
+            linear_part(i)
+            return
         for part in parts:
             part(i)
 

@@ -170,14 +170,17 @@ def test_linear_workspace_matches_two_calls(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 32), (2, 200, 288), (5, 1000, 1056), (6, 256, 4096),
-                                   (3, 25600, 256), (6, 520, 5152), (4, 2048, 5120), (7, 2048, 5120)])
+                                   (3, 25600, 256), (6, 520, 5152), (4, 2048, 5120), (7, 2048, 5120),
+                                   (40, 1000, 1056), (64, 256, 4096), (23, 25600, 5152)])
 def test_linear_few_rows_fused(M, N, K):
-    """Up to 6 token rows macaq_linear forms the token operand inside the
-    few-rows GEMM (one launch; 7 rows: the two launches).  Y must equal
-    macaq_quant_act + macaq_w4a4_gemm bit for bit -- the same codes, scales
-    and MMAs -- across K not a multiple of 256, N not a multiple of 128, a
-    strided X with a zero row, and few weight tiles with long K (K split over
-    a cluster); and it must agree with the oracle."""
+    """The few-rows layer.  Up to 6 token rows macaq_linear forms the token
+    operand inside the few-rows GEMM (one launch); from 7 rows it runs the
+    transform and the GEMM, whose weight stages may then load before its
+    grid-dependency wait.  Y must equal macaq_quant_act + macaq_w4a4_gemm bit
+    for bit -- the same codes, scales and MMAs -- across K not a multiple of
+    256, N not a multiple of 128, a strided X with a zero row, token tiles of
+    16, 32 and 64, and few weight tiles with long K (K split over a cluster);
+    and it must agree with the oracle."""
     Xs = workloads.make_matrix(M, K + 40, seed=7 * M + K, outlier_channels=(3, K - 5))
     Xs[M // 2, :] = 0.0
     X = Xs[:, :K]

@@ -203,9 +203,23 @@ macaq_status macaq_quant_weight_grouped_hb(const void *W, const float *s, int64_
     return MACAQ_OK;
 }
 
+namespace {
+macaq_status w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *w_codes,
+                       const uint8_t *w_scales, int64_t M, int64_t N, int64_t K, void *Y, int64_t ldy,
+                       bool weight_early, macaq_stream_t stream);
+}  // namespace
+
 macaq_status macaq_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                              const uint8_t *w_codes, const uint8_t *w_scales, int64_t M, int64_t N,
                              int64_t K, void *Y, int64_t ldy, macaq_stream_t stream)
+{
+    return w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K, Y, ldy, false, stream);
+}
+
+namespace {
+macaq_status w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *w_codes,
+                       const uint8_t *w_scales, int64_t M, int64_t N, int64_t K, void *Y, int64_t ldy,
+                       bool weight_early, macaq_stream_t stream)
 {
     MACAQ_TRY(check_k(K));
     MACAQ_TRY(check_rows(M));
@@ -227,8 +241,10 @@ macaq_status macaq_w4a4_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
     g.E = 0;
     g.Y = Y;
     g.ldy = ldy;
+    g.weight_early = weight_early;
     return from_cuda(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
+}  // namespace
 
 size_t macaq_linear_workspace_bytes(int64_t M, int64_t K)
 {
@@ -269,7 +285,9 @@ macaq_status macaq_linear(const void *X, int64_t ldx, const float *inv_s, const 
     uint8_t *a_codes = static_cast<uint8_t *>(workspace);
     uint8_t *a_scales = a_codes + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
     MACAQ_TRY(macaq_quant_act(X, ldx, inv_s, M, K, a_codes, a_scales, stream));
-    return macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K, Y, ldy, stream);
+    // the GEMM follows its own transform, which lets it start only after
+    // everything before the layer has completed: its weight may load early
+    return w4a4_gemm(a_codes, a_scales, w_codes, w_scales, M, N, K, Y, ldy, true, stream);
 }
 
 macaq_status macaq_transform_act_bf16(const void *X, int64_t ldx, const float *inv_s, int64_t M,

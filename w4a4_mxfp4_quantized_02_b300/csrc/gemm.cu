@@ -1176,6 +1176,7 @@ cudaError_t launch_skinny(const GemmArgs &g, cudaStream_t stream, int slot, cons
     p.ldx = ldx;
     p.inv = inv;
     p.nkb = static_cast<int32_t>(g.K / 32);
+    p.weight_early = (!FUSED && g.weight_early) ? 1 : 0;
     p.Y = static_cast<uint16_t *>(g.Y);
     p.ldy = g.ldy;
     p.M = static_cast<int32_t>(g.M);

@@ -82,6 +82,10 @@ struct Params {
     int64_t ldx;
     const float *inv;
     int32_t nkb;          // 32-value blocks of K
+    // the weight was complete before the preceding kernel started (a
+    // transform that lets this kernel start only after its own wait): the
+    // producer issues the weight's first stages before the grid-dependency wait
+    int32_t weight_early;
 };
 
 // FUSED asks for registers that let two of its CTAs share an SM (as the
@@ -153,7 +157,10 @@ __global__ void __launch_bounds__(skinny_threads(FUSED), FUSED ? 2 : 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     griddep_launch_dependents();
-    griddep_wait();
+    const bool weight_early = !FUSED && p.weight_early != 0;
+    // (with weight_early the producer thread waits itself, after issuing the
+    // weight's first stages)
+    if (!(weight_early && threadIdx.x == 0)) griddep_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -161,7 +168,25 @@ __global__ void __launch_bounds__(skinny_threads(FUSED), FUSED ? 2 : 1)
             constexpr uint32_t kBytes = FUSED ? L::W_STAGE + L::SF_STAGE : L::W_STAGE + L::X_STAGE + 2 * L::SF_STAGE;
             const uint8_t *sfw = p.sfw + static_cast<size_t>(n0 / 128) * p.nka * SF_ATOM;
             uint32_t issued = 0, last_parity = 0;
-            for (int i = 0; i < my_stages; ++i) {
+            // the first round of stages: the slots are free; the weight part
+            // may go before the grid-dependency wait, the token part not
+            const int pre = weight_early ? (my_stages < STAGES ? my_stages : STAGES) : 0;
+            for (int i = 0; i < pre; ++i) {
+                const int ks = ks_begin + i;
+                mbar_arrive_expect_tx(full_bar(i), kBytes);
+                tma_load_2d(sbase + L::OFF_W + i * L::W_STAGE, &tmW, full_bar(i), ks * L::KB, n0);
+                bulk_load(sbase + L::OFF_SFW + i * L::SF_STAGE, sfw + static_cast<size_t>(2 * ks) * SF_ATOM,
+                          L::SF_STAGE, full_bar(i));
+            }
+            if (weight_early) griddep_wait();
+            for (int i = 0; i < pre; ++i) {
+                const int ks = ks_begin + i;
+                tma_load_2d(sbase + L::OFF_X + i * L::X_STAGE, &tmX, full_bar(i), ks * L::KB, 0);
+                bulk_load(sbase + L::OFF_SFX + i * L::SF_STAGE, p.sfx + static_cast<size_t>(2 * ks) * SF_ATOM,
+                          L::SF_STAGE, full_bar(i));
+                issued |= 1u << i;  // round 0: parity 0
+            }
+            for (int i = pre; i < my_stages; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
                 if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer, wait_ns)) break;

@@ -101,6 +101,12 @@ struct GemmArgs {
     uint8_t *h_codes = nullptr;
     uint8_t *h_scales = nullptr;
     const float *h_f = nullptr;
+    // the weight was complete before the preceding kernel on the stream
+    // started, and that kernel lets dependents start only after its own
+    // grid-dependency wait (the transform kernels do): the few-rows GEMM then
+    // issues the weight's first stages before its wait.  Set only by
+    // macaq_linear, whose GEMM always follows its own transform.
+    bool weight_early = false;
 };
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t stream);

@@ -294,10 +294,11 @@ __global__ void __launch_bounds__(256) quant_kernel(QuantArgs a, int64_t rows_pe
     constexpr int R = 2;  // rows per iteration (loads of all R rows in flight together)
     __shared__ int32_t s_off[kMaxExperts + 1];
     __shared__ int32_t s_poff[kMaxExperts + 1];
-    // launched with programmatic stream serialisation: let the next kernel
-    // start its set-up, and wait for the previous one before touching memory
-    ptx::griddep_launch_dependents();
+    // launched with programmatic stream serialisation: wait for the previous
+    // kernel before touching memory, then let the next kernel start (after the
+    // wait: see the dense TMA kernel)
     ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     if (MODE == QuantMode::ActGrouped) {
         for (int e = threadIdx.x; e <= a.E; e += blockDim.x) s_off[e] = a.offsets[e];
         __syncthreads();
@@ -446,11 +447,13 @@ __global__ void __launch_bounds__(kTmaThreadsMax, 1) quant_dense_tma_kernel(cons
         ptx::fence_mbar_init();
     }
     __syncthreads();
-    // launched with programmatic stream serialisation: let the next kernel
-    // start its set-up, and wait for the previous one (which may produce X or
-    // still read the codes) before touching global memory
-    ptx::griddep_launch_dependents();
+    // launched with programmatic stream serialisation: wait for the previous
+    // kernel (which may produce X or still read the codes) before touching
+    // global memory, and only then let the next kernel start -- so a GEMM
+    // launched right after a transform starts only once everything before the
+    // transform has completed, and may load its weight before its own wait
     ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     const int32_t my_groups = blockIdx.y < static_cast<uint32_t>(groups)
                                   ? (groups - 1 - static_cast<int32_t>(blockIdx.y)) / static_cast<int32_t>(gridDim.y) + 1
@@ -637,8 +640,8 @@ __global__ void __launch_bounds__(grouped_consumers_max(kSilu) + 32, 1) quant_gr
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     // no offsets: one group of all rows (the dense SwiGLU input)
     for (int e = t; e <= a.E; e += blockDim.x)
         s_off[e] = a.offsets ? a.offsets[e] : (e == 0 ? 0 : static_cast<int32_t>(a.rows_valid));
@@ -873,8 +876,8 @@ __global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t *codes,
     const int64_t nka = ((nkb + 7) / 8 * 8) / 4;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= rows * nkb) return;
-    ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int64_t r = idx / nkb, kb = idx - (idx / nkb) * nkb;
     const uint8_t sb = scales[((r / 128) * nka + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4)];
     // 2^se with se = sb - 127 (sb = 0 gives 2^-127, a subnormal)
