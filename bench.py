@@ -435,6 +435,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
     graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
     batches = KernelBatches(plan.eager_steps, min(nsets, 4), len(parts))
+    batches.calibrate(parts, stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -452,7 +453,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = t_start.elapsed_time(t_end) - batches.padding_ms()
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     if one_launch:
         (gemm_avg,) = batches.per_launch_ms()
@@ -583,6 +584,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         "gpu_launches": len(parts) * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
+        "eager_delay_ms": batches.padding_ms(),
         "clocks": sampler.summary(),
     }
     return line
@@ -675,6 +677,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
     graph = None if args.no_graphs else capture_graph(lambda: [step(i) for i in range(chunk)])
     plan = StepPlan(args.steps, args.kernel_events_every, chunk if graph is not None else 0)
     batches = KernelBatches(plan.eager_steps, min(nsets, 4), 2)
+    batches.calibrate([transform_part, gemm_part], stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -690,7 +693,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = t_start.elapsed_time(t_end) - batches.padding_ms()
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     q_ms, g_ms = batches.per_launch_ms()
     status = mq.macaq_check_device_error()
@@ -768,6 +771,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
                 "copies": f"overlapped across steps ({nslot} buffer slots, separate copy streams)"},
         "gpu_launches": 2 * args.steps,
         "launch": plan.describe(),
+        "eager_delay_ms": batches.padding_ms(),
         "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -1069,6 +1073,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
     # every step computes the same layer on the same tokens, so a batch of
     # steps may share the one set of intermediate buffers
     batches = KernelBatches(plan.eager_steps, 2, len(parts))
+    batches.calibrate(parts, stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -1086,7 +1091,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = t_start.elapsed_time(t_end) - batches.padding_ms()
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     avg = batches.per_launch_ms()
     if fused:
@@ -1203,6 +1208,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         "gpu_launches": len(parts) * args.steps,
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
+        "eager_delay_ms": batches.padding_ms(),
         "clocks": sampler.summary(),
     }
     return line
@@ -1244,6 +1250,8 @@ class KernelBatches:
     per group instead of once per launch.  Every step still runs all of its
     kernels on its own buffers; a batch never reuses a buffer set."""
 
+    CYCLES_PER_US = 2000  # SM cycles per microsecond (about 2 GHz) for the delays
+
     def __init__(self, steps: list, nb: int, nparts: int):
         import torch
 
@@ -1252,14 +1260,58 @@ class KernelBatches:
         self.nparts = nparts
         self.events = [[torch.cuda.Event(enable_timing=True) for _ in range(nparts + 1)]
                        for _ in self.groups]
+        self.pad_cycles = 0
+        self.pad_events = []
+        self.host_us = self.device_us = None
+
+    def calibrate(self, parts, stream):
+        """Short kernels can finish before the host has enqueued the next one;
+        the group's events then time the host, not the kernels.  Run the
+        first group once (untimed) queued behind a device-side delay, compare
+        the host's enqueue time with the group's device time, and when the
+        host is not well ahead, precede every timed group by a delay of twice
+        the host time, so that the whole group is queued before its first
+        event.  The delays lie outside the groups' events and are subtracted
+        from the timed region's device time (padding_ms)."""
+        import torch
+
+        if not self.groups:
+            return
+        group = self.groups[0]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(20000 * self.CYCLES_PER_US)  # about 20 ms to enqueue behind
+        e0.record(stream)
+        h0 = time.perf_counter()
+        for part in parts:
+            for i in group:
+                part(i)
+        host_s = time.perf_counter() - h0
+        e1.record(stream)
+        torch.cuda.synchronize()
+        self.host_us = host_s * 1e6
+        self.device_us = e0.elapsed_time(e1) * 1e3
+        if self.host_us > 0.5 * self.device_us:
+            self.pad_cycles = int(2 * self.host_us * self.CYCLES_PER_US)
 
     def run(self, parts, stream):
+        import torch
+
         for group, ev in zip(self.groups, self.events):
+            if self.pad_cycles:
+                pe = torch.cuda.Event(enable_timing=True)
+                pe.record(stream)
+                torch.cuda._sleep(self.pad_cycles)
+                self.pad_events.append((pe, ev[0]))
             ev[0].record(stream)
             for j, part in enumerate(parts):
                 for i in group:
                     part(i)
                 ev[j + 1].record(stream)
+
+    def padding_ms(self) -> float:
+        """Device time of the delays before the groups (after a synchronize)."""
+        return sum(a.elapsed_time(b) for a, b in self.pad_events)
 
     def per_launch_ms(self) -> list:
         """Average device time per launch of each kernel (after a synchronize)."""
@@ -1268,7 +1320,12 @@ class KernelBatches:
 
     def describe(self) -> str:
         sizes = sorted({len(g) for g in self.groups})
-        return f"{sum(len(g) for g in self.groups)} eager steps in kernel-by-kernel batches of {sizes}"
+        out = f"{sum(len(g) for g in self.groups)} eager steps in kernel-by-kernel batches of {sizes}"
+        if self.pad_cycles:
+            out += (f"; the host enqueued a batch in {self.host_us:.0f} us against {self.device_us:.0f} us "
+                    f"on the device, so each batch followed a device-side delay of about "
+                    f"{2 * self.host_us:.0f} us (outside its events; subtracted from the region's time)")
+        return out
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -1456,6 +1513,7 @@ def _summary(line: dict) -> dict:
     keep_q = ("kernel", "achieved", "unit", "frac", "avg_launch_us", "bytes_per_launch")
     out = {"workload": line["config"]["workload"], "value": line["value"], "unit": line["unit"],
            "ms_per_step": line["ms_per_step"], "steps": line["steps"],
+           "eager_delay_ms": line.get("eager_delay_ms", 0.0),
            "roofline": {k: v for k, v in line["roofline"].items() if k in keep_r},
            "act_quant": {k: v for k, v in line["act_quant"].items() if k in keep_q}}
     for k in ("down_gemm", "combine"):
