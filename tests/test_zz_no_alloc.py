@@ -7,7 +7,8 @@ scratch array inside the library instead of a caller workspace.  These tests
 call it through the C ABI twice in a row (the second call runs over the first
 call's leftover scratch) and compare with macaq_linear bit for bit (the same
 kernels on the same inputs: a stale scratch byte would show as a difference);
-one problem fills the array exactly, so the tiled scales end on its last byte.
+one problem fills the array exactly, so the tiled scales end on its last byte,
+and one pair of problems takes the one-launch path of a few token rows.
 They pass in a fresh process and after the rest of the suite.
 """
 import ctypes
@@ -43,6 +44,7 @@ def test_rejects_oversized_problem_before_launch():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("shapes", [((16, 128, 64), (300, 640, 200)), ((4096, 5120, 256), (8, 5120, 512)),
+                                    ((3, 5120, 1024), (1, 256, 64)),
                                     ((FULL_M, FULL_K, 256), (FULL_M, FULL_K, 256))])
 def test_matches_workspace_entry_point_twice(shapes):
     require_gpu()
