@@ -36,6 +36,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "mx_block.cuh"
@@ -199,6 +200,7 @@ struct PairLayout {
     static constexpr int BYTES = OFF_OFFS + 3 * (static_cast<int>(kMaxExperts) + 1) * 4;
     static constexpr int ALLOC = BYTES + 1024;
     static_assert(OFF_EPI % 1024 == 0, "epilogue buffers must be 1 KB aligned");
+    static_assert(STAGES * A_STAGE >= NUM_EPI_WARPS * 8 * EPI_BUF, "last tile's staging must fit the A ring");
     static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory overflow");
     static_assert(ALLOC <= 232448, "shared memory");
 };
@@ -689,44 +691,58 @@ __global__ void __launch_bounds__(pair_threads(EPI), 1)
             // in Y, so a warp with some of them stores row by row.
             const bool use_tma = !GROUPED || row0 + 32 <= ti.rows_valid;
             const bool my_row = row0 + lane < ti.rows_valid;
-            if (L::EPI_NBUF >= 4 && use_tma) {
+            // Staging in batches of NB 16-column pieces (1 KB each) from sbuf:
+            // each batch is written, published to the store unit with one proxy
+            // fence and stored, after the previous batch's stores have read it.
+            auto store_batched = [&](auto nb_c, uint32_t sbuf) {
+                constexpr int NB = decltype(nb_c)::value;
 #pragma unroll
-              for (int c0 = 0; c0 < 8; c0 += L::EPI_NBUF) {
-                // the previous batch's stores must be done reading the staging
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-                int nchunks = 0;
+                for (int c0 = 0; c0 < 8; c0 += NB) {
+                    // the previous batch's stores must be done reading the staging
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    int nchunks = 0;
 #pragma unroll
-                for (int c = c0; c < c0 + L::EPI_NBUF; ++c) {
-                    if (ti.n0 + half * 128 + 16 * c >= p.N) break;
-                    uint32_t packed[8];
+                    for (int c = c0; c < c0 + NB; ++c) {
+                        if (ti.n0 + half * 128 + 16 * c >= p.N) break;
+                        uint32_t packed[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
-                        const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-                        packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                        for (int i = 0; i < 8; ++i) {
+                            const float lo = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i]);
+                            const float hi = __uint_as_float(acc[c >> 1][(c & 1) * 16 + 2 * i + 1]);
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                            packed[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        const uint32_t buf = sbuf + (c - c0) * EPI_BUF;
+                        const uint32_t sw = (lane >> 2) & 1;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * sw),
+                                     "r"(packed[0]), "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * (1 ^ sw)),
+                                     "r"(packed[4]), "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
+                                     : "memory");
+                        ++nchunks;
                     }
-                    const uint32_t buf = ebuf + (c - c0) * EPI_BUF;
-                    const uint32_t sw = (lane >> 2) & 1;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * sw),
-                                 "r"(packed[0]), "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 32 + 16 * (1 ^ sw)),
-                                 "r"(packed[4]), "r"(packed[5]), "r"(packed[6]), "r"(packed[7])
-                                 : "memory");
-                    ++nchunks;
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // rows past M and columns past N are clipped by the stores
+                        for (int c = 0; c < nchunks; ++c)
+                            tma_store_2d(&tmY, sbuf + c * EPI_BUF, ti.n0 + half * 128 + 16 * (c0 + c),
+                                         ti.y_row0 + row0);
+                        bulk_commit();
+                    }
+                    if (nchunks < NB) break;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    // rows past M and columns past N are clipped by the stores
-                    for (int c = 0; c < nchunks; ++c)
-                        tma_store_2d(&tmY, ebuf + c * EPI_BUF, ti.n0 + half * 128 + 16 * (c0 + c), ti.y_row0 + row0);
-                    bulk_commit();
-                }
-                if (nchunks < L::EPI_NBUF) break;
-              }
+            };
+            if (use_tma && u + unit_stride >= total_units) {
+                // The CTA's last tile: the accumulator is full, so every MMA has
+                // read its stages, and no stage is loaded again; the A part of
+                // the operand ring (at least 80 KB) stages all eight of this
+                // warp's pieces at once (8 KB per warp).
+                store_batched(std::integral_constant<int, 8>{}, sbase + L::OFF_A + ew * 8 * EPI_BUF);
+            } else if (L::EPI_NBUF >= 4 && use_tma) {
+                store_batched(std::integral_constant<int, L::EPI_NBUF>{}, ebuf);
             } else {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
