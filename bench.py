@@ -1291,7 +1291,10 @@ class KernelBatches:
         torch.cuda.synchronize()
         self.host_us = host_s * 1e6
         self.device_us = e0.elapsed_time(e1) * 1e3
-        if self.host_us > 0.5 * self.device_us:
+        # only where the device would otherwise run dry: a delay in front of
+        # a group the host keeps queued anyway would only add idle time (and
+        # idle time lets a power-capped GPU recover, flattering the kernels)
+        if self.host_us > 0.8 * self.device_us:
             self.pad_cycles = int(2 * self.host_us * self.CYCLES_PER_US)
 
     def run(self, parts, stream):
