@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(skinny_threads(FUSED), FUSED ? 2 : 1)
                 tma_load_2d(sbase + L::OFF_X + i * L::X_STAGE, &tmX, full_bar(i), ks * L::KB, 0);
                 bulk_load(sbase + L::OFF_SFX + i * L::SF_STAGE, p.sfx + static_cast<size_t>(2 * ks) * SF_ATOM,
                           L::SF_STAGE, full_bar(i));
-                issued |= 1u << i;  // round 0: parity 0
+                issued |= 1u << i;  // first pass of the ring: parity 0
             }
             for (int i = pre; i < my_stages; ++i) {
                 const int s = i % STAGES;
