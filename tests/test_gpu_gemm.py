@@ -203,3 +203,29 @@ def test_linear_few_rows_fused(M, N, K):
     da, dw = oracle.dequant(ca, sa), oracle.dequant(cw, sw)
     frac, canc = check_gemm(bf16_to_np(Y), oracle.gemm_ref(da, dw), oracle.abs_gemm_ref(da, dw), K)
     assert frac > 0.999, (frac, canc)
+
+
+def test_linear_few_rows_fused_special_values():
+    """The one-launch path (6 rows) on the transform's special inputs --
+    negative zeros, 1e30 spikes, subnormals, a single Hadamard spike, exact
+    ties -- gives the two calls' Y bit for bit."""
+    K, N = 32 * 12, 256
+    x = np.zeros((6, K), np.float32)
+    x[1, :] = -0.0
+    x[2, ::7] = 1e30
+    x[3, :] = np.float32(1e-40)
+    x[4, :32] = [(-1.0) ** i for i in range(32)]
+    x[5, 32:64] = 0.5 * np.arange(32) - 8
+    x[5, 64] = -1e-3
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    X = to_dev(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+    ones = torch.ones(K, dtype=torch.float32, device=DEV)
+    W = workloads.make_weight(N, K, seed=77)
+    w_codes, w_scales = mq.macaq_quant_weight(to_dev(W), ones)
+    Y = mq.macaq_linear(X, ones, w_codes, w_scales, N)
+    a_codes, a_scales = mq.macaq_quant_act(X, ones)
+    Y2 = mq.macaq_w4a4_gemm(a_codes, a_scales, w_codes, w_scales, 6, N, K)
+    torch.cuda.synchronize()
+    assert mq.macaq_check_device_error() == 0
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+    assert torch.all(Y[0] == 0) and torch.all(Y[1] == 0)
