@@ -445,9 +445,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         h0 = time.perf_counter()
-        for _ in range(plan.replays):
-            graph.replay()
-        batches.run(parts, stream)
+        batches.run(parts, stream, graph, plan.replays)
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -585,6 +583,7 @@ def gpu_arm(args, rank: int, world: int, config: str | None = None, light: bool 
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "eager_delay_ms": batches.padding_ms(),
+        "eager_batch_host_us": batches.host_us, "eager_batch_device_us": batches.device_us,
         "clocks": sampler.summary(),
     }
     return line
@@ -686,9 +685,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for _ in range(plan.replays):
-            graph.replay()
-        batches.run([transform_part, gemm_part], stream)
+        batches.run([transform_part, gemm_part], stream, graph, plan.replays)
         t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -772,6 +769,7 @@ def gpu_arm_w4a16(args, rank: int, world: int):
         "gpu_launches": 2 * args.steps,
         "launch": plan.describe(),
         "eager_delay_ms": batches.padding_ms(),
+        "eager_batch_host_us": batches.host_us, "eager_batch_device_us": batches.device_us,
         "clocks": sampler.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -1083,9 +1081,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         h0 = time.perf_counter()
-        for _ in range(plan.replays):
-            graph.replay()
-        batches.run(parts, stream)
+        batches.run(parts, stream, graph, plan.replays)
         host_enqueue_s = time.perf_counter() - h0
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -1209,6 +1205,7 @@ def gpu_arm_moe(args, rank: int, world: int, config: str | None = None, light: b
         "host_enqueue_us_per_step": host_enqueue_s / args.steps * 1e6,
         "launch": plan.describe(),
         "eager_delay_ms": batches.padding_ms(),
+        "eager_batch_host_us": batches.host_us, "eager_batch_device_us": batches.device_us,
         "clocks": sampler.summary(),
     }
     return line
@@ -1236,8 +1233,8 @@ class StepPlan:
 
     def describe(self) -> str:
         if self.replays:
-            return (f"{self.replays} replays of a CUDA graph of {self.chunk} steps, then "
-                    f"{len(self.eager_steps)} eager steps in kernel-by-kernel batches with CUDA events")
+            return (f"{self.replays} replays of a CUDA graph of {self.chunk} steps, spread evenly in front "
+                    f"of {len(self.eager_steps)} eager steps in kernel-by-kernel batches with CUDA events")
         return "eager launches in kernel-by-kernel batches with CUDA events"
 
 
@@ -1297,10 +1294,20 @@ class KernelBatches:
         if self.host_us > 0.8 * self.device_us:
             self.pad_cycles = int(2 * self.host_us * self.CYCLES_PER_US)
 
-    def run(self, parts, stream):
+    def run(self, parts, stream, graph=None, replays: int = 0):
+        """The timed steps: `replays` replays of `graph` (whole steps), spread
+        evenly in front of the groups, so that each group is enqueued while the
+        device still runs the replayed steps before it (real work, not idle
+        time), then each group kernel by kernel between its events."""
         import torch
 
-        for group, ev in zip(self.groups, self.events):
+        G = len(self.groups)
+        if G == 0:
+            for _ in range(replays):
+                graph.replay()
+        for k, (group, ev) in enumerate(zip(self.groups, self.events)):
+            for _ in range((k + 1) * replays // G - k * replays // G):
+                graph.replay()
             if self.pad_cycles:
                 pe = torch.cuda.Event(enable_timing=True)
                 pe.record(stream)
