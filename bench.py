@@ -1238,6 +1238,15 @@ class StepPlan:
         return "eager launches in kernel-by-kernel batches with CUDA events"
 
 
+def replay_schedule(replays: int, groups: int) -> list:
+    """How many graph replays go in front of each of `groups` eager groups:
+    all `replays`, spread as evenly as whole numbers allow (no group gets more
+    than one more than another); with no groups, one entry holding them all."""
+    if groups <= 0:
+        return [replays]
+    return [(k + 1) * replays // groups - k * replays // groups for k in range(groups)]
+
+
 class KernelBatches:
     """The eager steps of the timed region, run in batches of `nb` whole steps
     kernel by kernel -- every step's first kernel, then every step's second,
@@ -1301,12 +1310,12 @@ class KernelBatches:
         time), then each group kernel by kernel between its events."""
         import torch
 
-        G = len(self.groups)
-        if G == 0:
-            for _ in range(replays):
+        schedule = replay_schedule(replays, len(self.groups))
+        if not self.groups:
+            for _ in range(schedule[0]):
                 graph.replay()
         for k, (group, ev) in enumerate(zip(self.groups, self.events)):
-            for _ in range((k + 1) * replays // G - k * replays // G):
+            for _ in range(schedule[k]):
                 graph.replay()
             if self.pad_cycles:
                 pe = torch.cuda.Event(enable_timing=True)
