@@ -94,8 +94,9 @@ extern "C" macaq_status macaq_linear_no_alloc(const void *X, int64_t ldx, const 
     void *scratch = nullptr;
     if (macaq::scratch_address(&scratch) != cudaSuccess) return MACAQ_ERR_CUDA;
     // macaq_linear checks every other argument; its quantisation kernel
-    // writes every scratch byte the GEMM then reads, so the contents left by
-    // an earlier call need no clearing.
+    // writes every scratch byte the GEMM then reads (up to 6 token rows the
+    // layer is one kernel that uses no scratch), so the contents left by an
+    // earlier call need no clearing.
     return macaq_linear(X, ldx, inv_s, w_codes, w_scales, M, N, K, Y, ldy, scratch,
                         MACAQ_LINEAR_STATIC_SCRATCH_BYTES, stream);
 }
